@@ -1,0 +1,179 @@
+"""Oracle for the fused MoE permute + grouped-matmul backward (d_x only).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product path
+(``permute_grouped_gemm_gb300``) never imports, links or calls it, and this
+package never imports the product.
+
+The arithmetic lives in ``oracle_dx.cpp`` (plain C++17 loops, fp64
+accumulation, multithreaded over tokens); this module compiles it with g++
+and marshals arguments. It follows the element-wise gradient formula of the
+page "MoeInitRoutingGroupedMatmulGrad design" (section "数学定义和公式"):
+
+    d_x[b, k] = sum_{i : batch(i) = b} sum_n d_y[i, n] * weight[g(i), k, n]
+
+with batch(i) = original_pos(i) // topK (same section, Step 2) and
+expandedRowIdx read in gather (rowIdxType 0) or scatter (rowIdxType 1) form
+(section "输入输出", note 1).
+
+Pins (``tests/test_oracle_pins.py``): a pure-Python indicator-sum brute force,
+the unfused two-step form written with numpy, ``torch.matmul`` for the
+one-expert identity-routing case, hand-derived closed forms, a hand-worked
+example in ``tests/golden/``, and invariants (column sums, expert relabelling,
+empty experts, gather vs scatter index, linearity). The dtype decoders are
+pinned against numpy / torch conversions of every 16-bit pattern.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle_dx.cpp")
+_LIB = os.path.join(_HERE, "_build", "liboracle_dx.so")
+
+F32, F16, BF16 = 0, 1, 2
+
+ERRORS = {
+    0: "ok",
+    1: "null pointer",
+    2: "shape",
+    3: "attribute",
+    4: "dtype",
+    16: "index out of range",
+    17: "groupList sum != M or negative count",
+    18: "index is not a permutation",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library with g++ (no CUDA)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load_library(path: str):
+    """ctypes handle with the oracle's signatures (also used by the mutation tests)."""
+    lib = ctypes.CDLL(path)
+    i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+    lib.oracle_dx.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64,
+                              i64, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
+    lib.oracle_dx.restype = ctypes.c_int
+    lib.oracle_decode.argtypes = [vp, ctypes.c_int, i64, dp]
+    lib.oracle_decode.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def _raw(a):
+    """(contiguous numpy array of the raw element bits, dtype code)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(a, torch.Tensor):
+        a = a.detach().cpu().contiguous()
+        if a.dtype == torch.bfloat16:
+            return a.view(torch.int16).numpy(), BF16
+        if a.dtype == torch.float16:
+            return a.view(torch.int16).numpy(), F16
+        if a.dtype == torch.float32:
+            return a.numpy(), F32
+        raise TypeError(f"unsupported dtype {a.dtype}")
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return a.view(np.int16), F16
+    if a.dtype == np.float32:
+        return a, F32
+    raise TypeError(f"unsupported dtype {a.dtype}")
+
+
+def _i64(a):
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"oracle rejected the inputs: {ERRORS.get(code, code)} (code {code})")
+        self.code = code
+
+
+def dx(grad_y, weight, expanded_row_idx, group_list, batch: int, top_k: int,
+       row_idx_type: int, tokens=None, nthreads: int = 0, lib=None) -> np.ndarray:
+    """fp64 d_x rows for ``tokens`` (all tokens if None): array [len(tokens), K].
+
+    grad_y: [M, N], weight: [G, K, N] (torch CPU/CUDA tensors or numpy; fp32,
+    fp16 or bf16, same dtype), expanded_row_idx: int64 [M], group_list: int64
+    [G] counts. Raises OracleError with the constraint that failed. ``lib``
+    selects another build of the same source (mutation tests only).
+    """
+    lib = lib or _load()
+    dy, dt = _raw(grad_y)
+    w, dtw = _raw(weight)
+    if dt != dtw:
+        raise OracleError(4)
+    M, N = dy.shape
+    G, K, Nw = w.shape
+    if Nw != N:
+        raise OracleError(2)
+    idx = _i64(expanded_row_idx)
+    gl = _i64(group_list)
+    if idx.shape != (M,) or gl.shape != (G,):
+        raise OracleError(2)
+    if tokens is None:
+        tok = None
+        nt = batch
+    else:
+        tok = _i64(tokens)
+        nt = tok.shape[0]
+    out = np.empty((nt, K), dtype=np.float64)
+    rc = lib.oracle_dx(dy.ctypes.data, w.ctypes.data, dt, idx.ctypes.data, gl.ctypes.data,
+                       M, N, K, G, batch, top_k, row_idx_type,
+                       None if tok is None else tok.ctypes.data, nt, out.ctypes.data,
+                       int(nthreads))
+    if rc != 0:
+        raise OracleError(rc)
+    return out
+
+
+def decode(raw_bits: np.ndarray, dtype_code: int, lib=None) -> np.ndarray:
+    """Widen raw element bits (uint16 for fp16/bf16, float32 for fp32) to fp64."""
+    lib = lib or _load()
+    src = np.ascontiguousarray(raw_bits)
+    out = np.empty(src.size, dtype=np.float64)
+    rc = lib.oracle_decode(src.ctypes.data, dtype_code, src.size, out.ctypes.data)
+    if rc != 0:
+        raise OracleError(rc)
+    return out.reshape(src.shape)
+
+
+def host_cores() -> int:
+    """Threads the oracle uses by default (std::thread::hardware_concurrency)."""
+    return os.cpu_count() or 1

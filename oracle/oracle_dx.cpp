@@ -1,0 +1,232 @@
+// Oracle for the fused MoE permute + grouped-matmul backward (input gradient only).
+//
+// TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, load or call
+// this file; only the tests, the smoke check and the benchmark's CPU-baseline
+// leg do. It shares no code, header, table or constant with the CUDA library.
+//
+// What it computes (page "MoeInitRoutingGroupedMatmulGrad design", section
+// "数学定义和公式", element-wise gradient formula and its scalar form):
+//
+//     d_x[b, k] = sum over expanded rows i with batch(i) == b of
+//                 sum over n of d_y[i, n] * weight[g(i), k, n]
+//
+// where g(i) is the expert whose block of the expanded order holds row i
+// (groupList gives the per-expert row counts, not a cumulative sum: section
+// "输入输出"), and batch(i) = original_pos(i) / topK (section "数学定义",
+// Step 2). expandedRowIdx is read according to rowIdxType (section "输入输出",
+// note 1): 0 = gather form, entry i holds the original position of expanded
+// row i; 1 = scatter form, entry p holds the expanded row of original
+// position p.
+//
+// The steps follow the definition directly and in this order:
+//   1. every input element is widened exactly to double (fp32, fp16 and bf16
+//      values are all exactly representable in double);
+//   2. the expert of each expanded row is found by walking groupList;
+//   3. the original-position -> expanded-row map is built from the index;
+//   4. for each requested token b, for j = 0 .. topK-1 in increasing order,
+//      with i the expanded row of original position b*topK + j, the dot
+//      products sum_n d_y[i,n]*weight[g(i),k,n] are formed in double (n
+//      ascending) and added into an accumulator row; the accumulator is the
+//      output row.
+// No blocking, no fusion beyond the formula, no reordering of the sum over n.
+//
+// Input validation mirrors the constraint table (section "约束"): batch > 0,
+// topK > 0, rowIdxType in {0, 1}, M == batch * topK, every groupList entry
+// >= 0 and their sum == M, expandedRowIdx a permutation of [0, M).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+enum { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+enum {
+  kOk = 0,
+  kErrNull = 1,
+  kErrShape = 2,
+  kErrAttr = 3,
+  kErrDtype = 4,
+  kErrIndex = 16,
+  kErrGroupSum = 17,
+  kErrNotPerm = 18,
+};
+
+// IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+double decode_binary16(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1f;
+  const int f = h & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = std::ldexp(static_cast<double>(f), -24);  // subnormal: f * 2^-14 * 2^-10
+  } else if (e == 31) {
+    v = (f == 0) ? INFINITY : NAN;
+  } else {
+    v = std::ldexp(static_cast<double>(1024 + f), e - 25);  // (1 + f/1024) * 2^(e-15)
+  }
+  return sign ? -v : v;
+}
+
+// bfloat16: the upper 16 bits of an IEEE 754 binary32.
+double decode_bfloat16(uint16_t h) {
+  const uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+double decode_binary32(const void* p, int64_t idx) {
+  float f;
+  std::memcpy(&f, static_cast<const char*>(p) + 4 * idx, sizeof f);
+  return static_cast<double>(f);
+}
+
+struct Decoder {
+  int dtype;
+  std::vector<double> f16_table;  // all 65536 binary16 values, built by decode_binary16
+  explicit Decoder(int dt) : dtype(dt) {
+    if (dt == kF16) {
+      f16_table.resize(65536);
+      for (uint32_t h = 0; h < 65536; ++h) f16_table[h] = decode_binary16(static_cast<uint16_t>(h));
+    }
+  }
+  double at(const void* base, int64_t idx) const {
+    if (dtype == kF32) return decode_binary32(base, idx);
+    const uint16_t h = static_cast<const uint16_t*>(base)[idx];
+    return dtype == kF16 ? f16_table[h] : decode_bfloat16(h);
+  }
+};
+
+struct Routing {
+  std::vector<int64_t> group_of_row;  // g(i) for every expanded row i
+  std::vector<int64_t> row_of_pos;    // expanded row of original position p
+};
+
+// Validates the inputs against the constraint table and builds g(i) and the
+// original-position -> expanded-row map.
+int build_routing(const int64_t* idx, const int64_t* group_list, int64_t M, int64_t G,
+                  int row_idx_type, Routing* r) {
+  int64_t total = 0;
+  for (int64_t g = 0; g < G; ++g) {
+    if (group_list[g] < 0 || group_list[g] > M) return kErrGroupSum;
+    total += group_list[g];
+  }
+  if (total != M) return kErrGroupSum;
+
+  r->group_of_row.assign(M, -1);
+  int64_t i = 0;
+  for (int64_t g = 0; g < G; ++g)
+    for (int64_t c = 0; c < group_list[g]; ++c) r->group_of_row[i++] = g;
+
+  for (int64_t q = 0; q < M; ++q)
+    if (idx[q] < 0 || idx[q] >= M) return kErrIndex;
+
+  r->row_of_pos.assign(M, -1);
+  if (row_idx_type == 0) {
+    // gather form: idx[i] = original position of expanded row i
+    for (int64_t row = 0; row < M; ++row) {
+      if (r->row_of_pos[idx[row]] != -1) return kErrNotPerm;
+      r->row_of_pos[idx[row]] = row;
+    }
+  } else {
+    // scatter form: idx[p] = expanded row of original position p
+    std::vector<char> seen(M, 0);
+    for (int64_t p = 0; p < M; ++p) {
+      if (seen[idx[p]]) return kErrNotPerm;
+      seen[idx[p]] = 1;
+      r->row_of_pos[p] = idx[p];
+    }
+  }
+  return kOk;
+}
+
+struct Job {
+  const void* dy;
+  const void* w;
+  const Decoder* dec;
+  const Routing* routing;
+  const int64_t* tokens;
+  int64_t ntokens, N, K, topK;
+  double* out;
+};
+
+void run_tokens(const Job& job, int64_t t_begin, int64_t t_end) {
+  const int64_t N = job.N, K = job.K;
+  std::vector<double> dy_row(N);
+  std::vector<double> acc(K);
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    const int64_t b = job.tokens ? job.tokens[t] : t;
+    for (int64_t k = 0; k < K; ++k) acc[k] = 0.0;
+    for (int64_t j = 0; j < job.topK; ++j) {
+      const int64_t i = job.routing->row_of_pos[b * job.topK + j];
+      const int64_t g = job.routing->group_of_row[i];
+      for (int64_t n = 0; n < N; ++n) dy_row[n] = job.dec->at(job.dy, i * N + n);
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t wbase = (g * K + k) * N;
+        double s = 0.0;
+        for (int64_t n = 0; n < N; ++n) s += dy_row[n] * job.dec->at(job.w, wbase + n);
+        acc[k] += s;
+      }
+    }
+    double* o = job.out + t * K;
+    for (int64_t k = 0; k < K; ++k) o[k] = acc[k];
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Widens n elements of the given dtype to double (exposed so that the tests
+// can pin the decoders against independent conversions).
+int oracle_decode(const void* src, int dtype, int64_t n, double* dst) {
+  if (!src || !dst) return kErrNull;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return kErrDtype;
+  Decoder dec(dtype);
+  for (int64_t q = 0; q < n; ++q) dst[q] = dec.at(src, q);
+  return kOk;
+}
+
+// d_x rows for the requested tokens (all tokens when tokens == NULL, then
+// ntokens must equal batch). out is [ntokens, K] double, row-major.
+// dy is [M, N], w is [G, K, N], both row-major in the given dtype.
+int oracle_dx(const void* dy, const void* w, int dtype, const int64_t* expanded_row_idx,
+              const int64_t* group_list, int64_t M, int64_t N, int64_t K, int64_t G,
+              int64_t batch, int64_t topK, int row_idx_type, const int64_t* tokens,
+              int64_t ntokens, double* out, int nthreads) {
+  if (!dy || !w || !expanded_row_idx || !group_list || !out) return kErrNull;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return kErrDtype;
+  if (batch <= 0 || topK <= 0 || (row_idx_type != 0 && row_idx_type != 1)) return kErrAttr;
+  if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return kErrShape;
+  if (M != batch * topK) return kErrShape;
+  if (!tokens && ntokens != batch) return kErrShape;
+  for (int64_t t = 0; tokens && t < ntokens; ++t)
+    if (tokens[t] < 0 || tokens[t] >= batch) return kErrShape;
+
+  Routing routing;
+  const int rc = build_routing(expanded_row_idx, group_list, M, G, row_idx_type, &routing);
+  if (rc != kOk) return rc;
+
+  Decoder dec(dtype);
+  Job job{dy, w, &dec, &routing, tokens, ntokens, N, K, topK, out};
+  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
+  if (nthreads <= 0) nthreads = 1;
+  if (nthreads > ntokens) nthreads = static_cast<int>(ntokens > 0 ? ntokens : 1);
+
+  std::vector<std::thread> pool;
+  const int64_t per = (ntokens + nthreads - 1) / nthreads;
+  for (int th = 0; th < nthreads; ++th) {
+    const int64_t lo = th * per;
+    const int64_t hi = lo + per < ntokens ? lo + per : ntokens;
+    if (lo >= hi) break;
+    pool.emplace_back(run_tokens, std::cref(job), lo, hi);
+  }
+  for (auto& t : pool) t.join();
+  return kOk;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+"""Plausible mistakes planted in copies of the oracle source are caught.
+
+Each mutant is the oracle's C++ source with one edit (a dropped term, a wrong
+index, a transposed operand, swapped index forms, a wrong exponent bias),
+compiled to a temporary library on the CPU. The check fails if any mutant
+passes every pin below, i.e. if the pins could not tell it from the real
+oracle. Every mutant keeps all memory accesses in bounds.
+"""
+
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import make_case
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle_dx.cpp")
+
+MUTANTS = {
+    "drop_last_topk_term": ("for (int64_t j = 0; j < job.topK; ++j)",
+                            "for (int64_t j = 0; j < job.topK - 1; ++j)"),
+    "j_major_original_position": ("row_of_pos[b * job.topK + j]",
+                                  "row_of_pos[b + j * static_cast<int64_t>("
+                                  "job.routing->row_of_pos.size() / job.topK)]"),
+    "transposed_weight": ("const int64_t wbase = (g * K + k) * N;\n        double s = 0.0;\n"
+                          "        for (int64_t n = 0; n < N; ++n) s += dy_row[n] * job.dec->at(job.w, wbase + n);",
+                          "const int64_t wbase = g * K * N;\n        double s = 0.0;\n"
+                          "        for (int64_t n = 0; n < N; ++n) s += dy_row[n] * "
+                          "job.dec->at(job.w, wbase + (n * K + k) % (K * N));"),
+    "swapped_index_forms": ("if (row_idx_type == 0) {", "if (row_idx_type == 1) {"),
+    "group_off_by_one": ("r->group_of_row[i++] = g;", "r->group_of_row[i++] = (g + 1) % G;"),
+    "fp16_exponent_bias": ("e - 25", "e - 24"),
+    "bf16_wrong_half": ("static_cast<uint32_t>(h) << 16;", "static_cast<uint32_t>(h) << 15;"),
+}
+
+
+def build_mutant(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    path = tmp_path / f"{name}.cpp"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.check_call(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread",
+                           str(path), "-o", str(lib)])
+    return oracle.load_library(str(lib))
+
+
+def pins_pass(lib) -> bool:
+    from test_oracle_pins import brute_force, unfused_numpy, rel_err
+    # decoders against numpy / torch
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref16 = bits.view(np.float16).astype(np.float64)
+    got16 = oracle.decode(bits, oracle.F16, lib=lib)
+    fin = np.isfinite(ref16)
+    if not np.array_equal(got16[fin], ref16[fin]):
+        return False
+    import torch
+    refb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    gotb = oracle.decode(bits, oracle.BF16, lib=lib)
+    fin = np.isfinite(refb)
+    if not np.array_equal(gotb[fin], refb[fin]):
+        return False
+    # brute force and unfused form, both index forms, K == N so that a
+    # transposed weight stays in bounds
+    for rit in (0, 1):
+        for dt in ("fp32", "fp16"):
+            inp = make_case(batch=5, top_k=3, G=3, K=6, N=6, dtype=dt, seed=21, row_idx_type=rit)
+            try:
+                got = oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                                inp.batch, inp.top_k, rit, lib=lib)
+            except oracle.OracleError:
+                return False
+            if rel_err(got, brute_force(inp)) > 1e-12:
+                return False
+            if rel_err(got, unfused_numpy(inp)[0]) > 1e-12:
+                return False
+    return True
+
+
+def test_real_oracle_passes_the_pins(oracle_lib):
+    assert pins_pass(oracle._load())
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    assert not pins_pass(build_mutant(tmp_path, name))
