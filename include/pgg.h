@@ -1,0 +1,183 @@
+/*
+ * pgg.h -- C ABI of the GB300 (sm_103a) fused MoE permute + grouped-matmul
+ * backward, input gradient only.
+ *
+ * Operation (page "MoeInitRoutingGroupedMatmulGrad design", section
+ * "数学定义和公式", element-wise gradient formula):
+ *
+ *     d_x[b, k] = sum_{i : batch(i) = b} sum_n gradY[i, n] * weight[g(i), k, n]
+ *
+ *   gradY  [M, N]     upstream gradient d_y in expanded (expert-sorted) order,
+ *                     M = batch * topK                       (section "输入输出")
+ *   weight [G, K, N]  expert weights, same dtype as gradY     (section "输入输出")
+ *   g(i)              expert whose block of rows holds row i; block g has
+ *                     groupList[g] rows (counts, not a cumulative sum; a count
+ *                     of 0 is an empty expert)         (sections "输入输出", "约束")
+ *   batch(i)          original_pos(i) / topK, original_pos = b * topK + j
+ *                     (section "数学定义和公式", Step 2)
+ *   expandedRowIdx    int64 [L], L == M. rowIdxType 0 (gather form): entry i is
+ *                     the original position of expanded row i. rowIdxType 1
+ *                     (scatter form): entry p is the expanded row of original
+ *                     position p                 (section "输入输出", note 1)
+ *   out               FP32 [batch, K], always FP32 whatever the input dtype
+ *                     (section "输入输出", note 2; section 2.6.2)
+ *
+ * The [M, K] intermediate d_y @ weight^T is never materialised (section 1.1).
+ * The result is bitwise identical from run to run: the topK contributions to
+ * each out element are added in increasing expanded-row order (section 2.4.1
+ * asks for deterministic computation).
+ *
+ * Conventions shared by every call below:
+ *   - All tensors are dense and row-major. Device pointers are addresses in the
+ *     current CUDA device's memory; the caller owns every buffer and keeps it
+ *     alive until the work on `stream` has finished. The library allocates no
+ *     memory and keeps no state between calls except per-device cached device
+ *     attributes and the test hooks at the end of this file.
+ *   - Calls only enqueue work on `stream` (NULL = legacy default stream) and
+ *     never synchronise. Inputs are not modified.
+ *   - Host-detected errors are returned synchronously and nothing is enqueued.
+ *   - Device-detected errors (bad index, groupList sum, not a permutation,
+ *     a wait that ran out) are written to the status word, the first uint32 of
+ *     the workspace: 0 means success, otherwise one of PGG_ERR_INDEX ..
+ *     PGG_ERR_TIMEOUT. Read it after the stream has finished. When routing
+ *     validation fails, `out` is zero-filled instead of computed.
+ *   - Alignment (a restriction of this library, from the tensor-memory-access
+ *     unit): gradY and weight must be 16-byte aligned and N * sizeof(dtype)
+ *     must be a multiple of 16 bytes; workspace must be 256-byte aligned; out
+ *     must be 16-byte aligned. Otherwise PGG_ERR_ALIGN.
+ */
+#ifndef PGG_H
+#define PGG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pgg_stream_t;
+
+/* Input dtype of gradY and weight (section "输入输出": FLOAT / FLOAT16 / BF16). */
+typedef enum { PGG_F32 = 0, PGG_F16 = 1, PGG_BF16 = 2 } pgg_dtype;
+
+typedef enum {
+  PGG_OK = 0,
+  PGG_ERR_NULL = 1,      /* a required pointer is NULL */
+  PGG_ERR_SHAPE = 2,     /* sizes violate the constraint table (L != M, M != batch*topK, ...) */
+  PGG_ERR_ATTR = 3,      /* topK <= 0, batch <= 0, or rowIdxType not in {0, 1} */
+  PGG_ERR_DTYPE = 4,     /* dtype not in pgg_dtype */
+  PGG_ERR_WORKSPACE = 5, /* workspace smaller than pgg_dx_workspace_size reports */
+  PGG_ERR_CUDA = 6,      /* a CUDA runtime/driver call failed (launch, tensor map, device query) */
+  PGG_ERR_ALIGN = 7,     /* pointer or row-stride alignment, see above */
+  /* device-detected, written to the status word: */
+  PGG_ERR_INDEX = 16,    /* an expandedRowIdx entry outside [0, M) */
+  PGG_ERR_GROUPSUM = 17, /* a negative groupList entry, or sum(groupList) != M */
+  PGG_ERR_NOT_PERM = 18, /* expandedRowIdx is not a permutation of [0, M) */
+  PGG_ERR_TIMEOUT = 19   /* a bounded wait inside a kernel ran out (no hang; result invalid) */
+} pgg_status;
+
+/*
+ * Workspace bytes pgg_dx_execute needs for these sizes (the two-phase
+ * get-workspace-size / execute convention of section 2.2.2). Pure host code:
+ * no CUDA call. Arguments as for pgg_dx_execute; L is the length of
+ * expandedRowIdx. The figure grows as 12*M + 4*batch*ceil(K/128) bytes plus a
+ * few KB; it is independent of N and never holds an [M, K] array.
+ * Returns PGG_OK and writes *workspace_bytes, or a host error code.
+ */
+int pgg_dx_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                          int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                          size_t* workspace_bytes);
+
+/*
+ * Computes out[batch, K] (FP32, fully overwritten) from gradY, weight,
+ * expandedRowIdx and groupList as defined at the top of this file.
+ *
+ *   gradY          device, [M, N] of `dtype`
+ *   weight         device, [G, K, N] of `dtype`
+ *   expandedRowIdx device, int64 [L], L == M, form selected by rowIdxType
+ *   groupList      device, int64 [G], per-expert row counts (sum must be M)
+ *   M, N, K, G     sizes; M == batch * topK, all >= 1, M < 2^31
+ *   batch, topK    attributes (section "约束": both > 0)
+ *   rowIdxType     0 gather form, 1 scatter form
+ *   workspace      device scratch of at least pgg_dx_workspace_size bytes,
+ *                  256-byte aligned, contents on entry irrelevant; holds the
+ *                  status word at offset 0 after the call
+ *   out            device, FP32 [batch, K]
+ *   stream         CUDA stream the work is enqueued on
+ *
+ * Equivalent to pgg_dx_route_prep followed by pgg_dx_grouped_gemm on the same
+ * workspace and stream.
+ */
+int pgg_dx_execute(const void* gradY, const void* weight, const int64_t* expandedRowIdx,
+                   const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                   int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                   void* workspace, size_t workspace_bytes, float* out, pgg_stream_t stream);
+
+/*
+ * First stage of pgg_dx_execute, exposed so that each stage can be timed on
+ * its own: validates the routing on the device (writing the status word),
+ * builds the per-expert row offsets (exclusive scan of groupList), the list
+ * of row blocks that skips empty experts, the inverse of expandedRowIdx and,
+ * per expanded row, its token and its rank among that token's rows; resets
+ * the scatter-add tickets. Same arguments and errors as pgg_dx_execute,
+ * without the value tensors and `out`.
+ */
+int pgg_dx_route_prep(const int64_t* expandedRowIdx, const int64_t* groupList, int64_t M,
+                      int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                      int rowIdxType, pgg_dtype dtype, void* workspace, size_t workspace_bytes,
+                      pgg_stream_t stream);
+
+/*
+ * Second stage of pgg_dx_execute: the persistent grouped-GEMM kernel with the
+ * fused, ordered scatter-add into out. Requires a pgg_dx_route_prep with the
+ * same sizes, routing and workspace earlier on the same stream (or otherwise
+ * ordered before it). If the status word is non-zero on entry the kernel
+ * zero-fills out and returns. Same arguments and errors as pgg_dx_execute.
+ */
+int pgg_dx_grouped_gemm(const void* gradY, const void* weight, const int64_t* expandedRowIdx,
+                        const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                        int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                        void* workspace, size_t workspace_bytes, float* out,
+                        pgg_stream_t stream);
+
+/* How pgg_dx_execute will run a problem of these sizes (host only, no CUDA call). */
+typedef struct {
+  int32_t variant;          /* 0 = wide row blocks (tensor-bound), 1 = narrow row blocks (streaming) */
+  int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent */
+  int32_t k_per_block;      /* output columns per tile: the MMA M extent (128) */
+  int32_t stages;           /* shared-memory pipeline depth */
+  int32_t k_blocks;         /* ceil(K / k_per_block) */
+  int32_t band_k_blocks;    /* k-blocks per band of the tile order */
+  int64_t max_row_blocks;   /* upper bound on row blocks: ceil(M/rows_per_block) + G */
+  size_t workspace_bytes;   /* as pgg_dx_workspace_size */
+  int32_t threads;          /* threads per CTA of the grouped-GEMM kernel */
+  int32_t smem_bytes;       /* dynamic shared memory per CTA */
+} pgg_plan_info;
+
+int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
+
+/* Human-readable name of a pgg_status code (static string). */
+const char* pgg_status_string(int status);
+
+/*
+ * Test hooks (process-wide; not needed in normal use).
+ * pgg_debug_set_wait_limit_ns: time limit of every bounded wait inside the
+ *   kernels (default 2e9 ns). 0 restores the default.
+ * pgg_debug_set_ticket_bias: added to the ticket count each ordered
+ *   scatter-add waits for; a positive bias makes every wait of a row with
+ *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
+ * pgg_debug_force_variant: -1 = automatic (default), 0 or 1 = force the
+ *   variant reported by pgg_dx_plan.
+ */
+void pgg_debug_set_wait_limit_ns(uint64_t ns);
+void pgg_debug_set_ticket_bias(uint32_t bias);
+void pgg_debug_force_variant(int variant);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGG_H */

@@ -1,0 +1,82 @@
+"""GB300 (sm_103a) fused MoE permute + grouped-matmul backward, input gradient.
+
+    d_x[b, k] = sum_{i : batch(i) = b} sum_n grad_y[i, n] * weight[g(i), k, n]
+
+("MoeInitRoutingGroupedMatmulGrad design", section "数学定义和公式".) The work
+runs in libpgg.so (include/pgg.h); this package is its thin binding. PyTorch
+supplies device memory and the current stream only.
+"""
+
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    CODES, PGG_BF16, PGG_F16, PGG_F32, STATUS, PggError, load,
+    pgg_debug_force_variant, pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
+    pgg_dx_execute, pgg_dx_grouped_gemm, pgg_dx_plan, pgg_dx_route_prep,
+    pgg_dx_workspace_size, pgg_status_string,
+)
+
+_DT = None
+
+
+def dtype_code(torch_dtype) -> int:
+    global _DT
+    if _DT is None:
+        import torch
+        _DT = {torch.float32: PGG_F32, torch.float16: PGG_F16, torch.bfloat16: PGG_BF16}
+    if torch_dtype not in _DT:
+        raise PggError(CODES["PGG_ERR_DTYPE"], "dtype_code")
+    return _DT[torch_dtype]
+
+
+def _args(grad_y, weight, expanded_row_idx, group_list, batch, top_k):
+    M, N = grad_y.shape
+    G, K, _ = weight.shape
+    return M, N, K, G, expanded_row_idx.shape[0], batch, top_k
+
+
+def workspace_bytes(grad_y, weight, expanded_row_idx, group_list, batch, top_k,
+                    row_idx_type) -> int:
+    sizes = _args(grad_y, weight, expanded_row_idx, group_list, batch, top_k)
+    return pgg_dx_workspace_size(*sizes, row_idx_type, dtype_code(grad_y.dtype))
+
+
+def dx(grad_y, weight, expanded_row_idx, group_list, batch: int, top_k: int,
+       row_idx_type: int, out=None, workspace=None, stream=None):
+    """d_x [batch, K] fp32 on grad_y's device (torch tensors, contiguous, CUDA).
+
+    Allocates ``out`` and the workspace through torch when not given. The call
+    is asynchronous on ``stream`` (default: torch's current stream); the
+    device-detected status is the first int32 of the workspace.
+    Returns (out, workspace).
+    """
+    import torch
+    for t in (grad_y, weight, expanded_row_idx, group_list):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if expanded_row_idx.dtype != torch.int64 or group_list.dtype != torch.int64:
+        raise ValueError("expandedRowIdx and groupList must be int64")
+    sizes = _args(grad_y, weight, expanded_row_idx, group_list, batch, top_k)
+    dt = dtype_code(grad_y.dtype)
+    if weight.dtype != grad_y.dtype:
+        raise PggError(CODES["PGG_ERR_DTYPE"], "dx")
+    need = pgg_dx_workspace_size(*sizes, row_idx_type, dt)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=grad_y.device)
+    if out is None:
+        out = torch.empty(batch, sizes[2], dtype=torch.float32, device=grad_y.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(grad_y.device)
+    rc = pgg_dx_execute(grad_y.data_ptr(), weight.data_ptr(), expanded_row_idx.data_ptr(),
+                        group_list.data_ptr(), *sizes, row_idx_type, dt, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), out.data_ptr(),
+                        stream.cuda_stream)
+    if rc != 0:
+        raise PggError(rc, "pgg_dx_execute")
+    return out, workspace
+
+
+def status(workspace) -> int:
+    """Device-detected status word of a finished call (synchronises)."""
+    import torch
+    return int(workspace[:4].view(torch.int32).item())

@@ -1,0 +1,334 @@
+// C ABI of the fused MoE permute + grouped-matmul backward (include/pgg.h):
+// argument validation (the constraint table and infershape checks of the page
+// "MoeInitRoutingGroupedMatmulGrad design", sections "约束" and 2.3), the
+// execution plan and workspace layout, tensor-map encoding, and the launches.
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pgg.h"
+#include "pgg_internal.h"
+
+namespace pgg {
+
+cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
+                              void* workspace, int num_sms, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(int dtype, int variant, const CUtensorMap& tdy,
+                                const CUtensorMap& tw, const GemmArgs& args, int grid,
+                                cudaStream_t stream);
+bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem);
+
+namespace {
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+std::atomic<uint32_t> g_ticket_bias{0};
+std::atomic<int> g_force_variant{-1};
+
+constexpr int64_t kInt32Max = 2147483647;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_size(int dtype) { return dtype == PGG_F32 ? 4 : 2; }
+
+// Host checks of sizes and attributes; pointers are checked by the callers.
+int check_sizes(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                int rowIdxType, int dtype) {
+  if (dtype != PGG_F32 && dtype != PGG_F16 && dtype != PGG_BF16) return PGG_ERR_DTYPE;
+  if (batch <= 0 || topK <= 0 || (rowIdxType != 0 && rowIdxType != 1)) return PGG_ERR_ATTR;
+  if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return PGG_ERR_SHAPE;
+  if (M > kInt32Max || N > kInt32Max || K > kInt32Max || G > kInt32Max) return PGG_ERR_SHAPE;
+  if (L != M) return PGG_ERR_SHAPE;
+  if (batch > M || topK > M || batch * topK != M) return PGG_ERR_SHAPE;
+  if ((N * elem_size(dtype)) % 16 != 0) return PGG_ERR_ALIGN;
+  return PGG_OK;
+}
+
+int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
+              int rowIdxType, int dtype, Plan* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->dtype = dtype;
+  int variant = g_force_variant.load();
+  if (variant != 0 && variant != 1) variant = (M / G < 64) ? 1 : 0;
+  p->variant = variant;
+  if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes))
+    return PGG_ERR_DTYPE;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->G = G;
+  p->batch = batch;
+  p->topK = topK;
+  p->row_idx_type = rowIdxType;
+  p->k_blocks = static_cast<int>((K + kKBlock - 1) / kKBlock);
+  p->band_k_blocks = p->k_blocks;
+  const int elems_per_row = kRowBytes / elem_size(dtype);
+  p->nk = static_cast<int>((N + elems_per_row - 1) / elems_per_row);
+  p->max_row_blocks = (M + p->rows_per_block - 1) / p->rows_per_block + G;
+  if (p->max_row_blocks * p->k_blocks > kInt32Max) return PGG_ERR_SHAPE;
+
+  Layout& L = p->layout;
+  size_t a = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = a;
+    a = align_up(a + bytes, 256);
+    return o;
+  };
+  L.hdr = take(sizeof(WsHeader));
+  L.off = take(sizeof(int64_t) * static_cast<size_t>(G + 1));
+  L.rbstart = take(sizeof(int32_t) * static_cast<size_t>(G + 1));
+  L.rblist = take(sizeof(int4) * static_cast<size_t>(p->max_row_blocks));
+  L.inv = take(sizeof(int32_t) * static_cast<size_t>(M));
+  L.rowinfo = take(sizeof(RowInfo) * static_cast<size_t>(M));
+  L.n_tickets = (batch * p->k_blocks + 3) / 4 * 4;
+  L.tickets = take(sizeof(uint32_t) * static_cast<size_t>(L.n_tickets));
+  L.total = a;
+  return PGG_OK;
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PGG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev[dev].num_sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return PGG_ERR_CUDA;
+    g_dev[dev].num_sms = sms;
+  }
+  *out = g_dev[dev];
+  return PGG_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+CUtensorMapDataType tmap_type(int dtype) {
+  if (dtype == PGG_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (dtype == PGG_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// d_y [M, N] as a 2-D map; boxes of 32 rows x one 128-byte row segment.
+// weight [G, K, N] as a 3-D map; boxes of 1 expert x 128 k x one segment.
+// Rows or columns outside the tensor read as zero.
+int encode_maps(const Plan& p, const void* dy, const void* w, CUtensorMap* tdy, CUtensorMap* tw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PGG_ERR_CUDA;
+  const cuuint64_t es = static_cast<cuuint64_t>(elem_size(p.dtype));
+  const cuuint32_t box_n = static_cast<cuuint32_t>(kRowBytes / es);
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * es};
+    cuuint32_t box[2] = {box_n, static_cast<cuuint32_t>(kDyBoxRows)};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(tdy, tmap_type(p.dtype), 2, const_cast<void*>(dy), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PGG_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.K),
+                          static_cast<cuuint64_t>(p.G)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.N) * es,
+                             static_cast<cuuint64_t>(p.N) * static_cast<cuuint64_t>(p.K) * es};
+    cuuint32_t box[3] = {box_n, static_cast<cuuint32_t>(kKBlock), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(tw, tmap_type(p.dtype), 3, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PGG_ERR_CUDA;
+  }
+  return PGG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common front half of every entry point that enqueues work.
+int prepare(const void* gradY, const void* weight, const int64_t* idx, const int64_t* gl,
+            bool need_values, int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+            int64_t topK, int rowIdxType, int dtype, void* ws, size_t ws_bytes, const float* out,
+            Plan* plan) {
+  if (!idx || !gl || !ws) return PGG_ERR_NULL;
+  if (need_values && (!gradY || !weight || !out)) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, plan);
+  if (rc != PGG_OK) return rc;
+  if (!aligned(ws, 256) || !aligned(idx, 8) || !aligned(gl, 8)) return PGG_ERR_ALIGN;
+  if (need_values && (!aligned(gradY, 16) || !aligned(weight, 16) || !aligned(out, 16)))
+    return PGG_ERR_ALIGN;
+  if (ws_bytes < plan->layout.total) return PGG_ERR_WORKSPACE;
+  return PGG_OK;
+}
+
+int run_route_prep(const Plan& plan, const int64_t* idx, const int64_t* gl, void* ws,
+                   cudaStream_t stream) {
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  return launch_route_prep(plan, idx, gl, ws, di.num_sms, stream) == cudaSuccess ? PGG_OK
+                                                                                   : PGG_ERR_CUDA;
+}
+
+int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, void* ws, float* out,
+                     cudaStream_t stream) {
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  CUtensorMap tdy, tw;
+  int rc = encode_maps(plan, gradY, weight, &tdy, &tw);
+  if (rc != PGG_OK) return rc;
+  char* w = static_cast<char*>(ws);
+  GemmArgs a;
+  a.rblist = reinterpret_cast<const int4*>(w + plan.layout.rblist);
+  a.rowinfo = reinterpret_cast<const RowInfo*>(w + plan.layout.rowinfo);
+  a.tickets = reinterpret_cast<uint32_t*>(w + plan.layout.tickets);
+  a.hdr = reinterpret_cast<WsHeader*>(w + plan.layout.hdr);
+  a.out = out;
+  a.K = plan.K;
+  a.batch = plan.batch;
+  a.k_blocks = plan.k_blocks;
+  a.band_k_blocks = plan.band_k_blocks;
+  a.nk = plan.nk;
+  a.ticket_bias = g_ticket_bias.load();
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  const int64_t max_tiles = plan.max_row_blocks * plan.k_blocks;
+  const int grid = static_cast<int>(max_tiles < di.num_sms ? max_tiles : di.num_sms);
+  return launch_grouped_gemm(plan.dtype, plan.variant, tdy, tw, a, grid, stream) == cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pgg
+
+using namespace pgg;
+
+extern "C" {
+
+int pgg_dx_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                          int64_t topK, int rowIdxType, pgg_dtype dtype, size_t* workspace_bytes) {
+  if (!workspace_bytes) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  Plan plan;
+  rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &plan);
+  if (rc != PGG_OK) return rc;
+  *workspace_bytes = plan.layout.total;
+  return PGG_OK;
+}
+
+int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                int rowIdxType, pgg_dtype dtype, pgg_plan_info* info) {
+  if (!info) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  Plan p;
+  rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
+  if (rc != PGG_OK) return rc;
+  info->variant = p.variant;
+  info->rows_per_block = p.rows_per_block;
+  info->k_per_block = kKBlock;
+  info->stages = p.stages;
+  info->k_blocks = p.k_blocks;
+  info->band_k_blocks = p.band_k_blocks;
+  info->max_row_blocks = p.max_row_blocks;
+  info->workspace_bytes = p.layout.total;
+  info->threads = p.threads;
+  info->smem_bytes = p.smem_bytes;
+  return PGG_OK;
+}
+
+int pgg_dx_route_prep(const int64_t* expandedRowIdx, const int64_t* groupList, int64_t M, int64_t N,
+                      int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK, int rowIdxType,
+                      pgg_dtype dtype, void* workspace, size_t workspace_bytes,
+                      pgg_stream_t stream) {
+  Plan plan;
+  int rc = prepare(nullptr, nullptr, expandedRowIdx, groupList, false, M, N, K, G, L, batch, topK,
+                   rowIdxType, dtype, workspace, workspace_bytes, nullptr, &plan);
+  if (rc != PGG_OK) return rc;
+  return run_route_prep(plan, expandedRowIdx, groupList, workspace,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pgg_dx_grouped_gemm(const void* gradY, const void* weight, const int64_t* expandedRowIdx,
+                        const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                        int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                        void* workspace, size_t workspace_bytes, float* out,
+                        pgg_stream_t stream) {
+  Plan plan;
+  int rc = prepare(gradY, weight, expandedRowIdx, groupList, true, M, N, K, G, L, batch, topK,
+                   rowIdxType, dtype, workspace, workspace_bytes, out, &plan);
+  if (rc != PGG_OK) return rc;
+  return run_grouped_gemm(plan, gradY, weight, workspace, out,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pgg_dx_execute(const void* gradY, const void* weight, const int64_t* expandedRowIdx,
+                   const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                   int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype, void* workspace,
+                   size_t workspace_bytes, float* out, pgg_stream_t stream) {
+  Plan plan;
+  int rc = prepare(gradY, weight, expandedRowIdx, groupList, true, M, N, K, G, L, batch, topK,
+                   rowIdxType, dtype, workspace, workspace_bytes, out, &plan);
+  if (rc != PGG_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = run_route_prep(plan, expandedRowIdx, groupList, workspace, s);
+  if (rc != PGG_OK) return rc;
+  return run_grouped_gemm(plan, gradY, weight, workspace, out, s);
+}
+
+const char* pgg_status_string(int status) {
+  switch (status) {
+    case PGG_OK: return "ok";
+    case PGG_ERR_NULL: return "null pointer";
+    case PGG_ERR_SHAPE: return "shape outside the constraints";
+    case PGG_ERR_ATTR: return "attribute outside the constraints (batch, topK, rowIdxType)";
+    case PGG_ERR_DTYPE: return "unsupported dtype";
+    case PGG_ERR_WORKSPACE: return "workspace too small";
+    case PGG_ERR_CUDA: return "CUDA call failed";
+    case PGG_ERR_ALIGN: return "pointer or row stride not aligned";
+    case PGG_ERR_INDEX: return "expandedRowIdx entry out of range";
+    case PGG_ERR_GROUPSUM: return "groupList negative or sum != M";
+    case PGG_ERR_NOT_PERM: return "expandedRowIdx is not a permutation";
+    case PGG_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+  }
+}
+
+void pgg_debug_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+}
+
+void pgg_debug_set_ticket_bias(uint32_t bias) { g_ticket_bias.store(bias); }
+
+void pgg_debug_force_variant(int variant) { g_force_variant.store(variant); }
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Internal definitions shared by the host planner and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pgg.h"
+
+namespace pgg {
+
+// Output columns (problem K) per tile. They are the 128 accumulator lanes of
+// one tensor-memory tile.
+constexpr int kKBlock = 128;
+// Bytes of one operand row inside a pipeline stage: one 128-byte swizzle atom
+// along the reduction dimension (64 half-precision or 32 fp32 elements).
+constexpr int kRowBytes = 128;
+// Rows of d_y fetched by one tensor-memory-access copy.
+constexpr int kDyBoxRows = 32;
+
+// Status codes written by the kernels (same values as pgg_status).
+constexpr uint32_t kStIndex = 16, kStGroupSum = 17, kStNotPerm = 18, kStTimeout = 19;
+
+// Start of the workspace. The status word comes first (documented in pgg.h).
+struct alignas(16) WsHeader {
+  uint32_t status;        // first device-detected error, 0 = ok
+  uint32_t sched_next;    // dynamic tile counter of the grouped-GEMM kernel
+  uint32_t n_row_blocks;  // number of non-empty row blocks
+  uint32_t timeout_site;  // where a bounded wait ran out (diagnostic)
+  uint32_t pad[12];
+};
+static_assert(sizeof(WsHeader) == 64, "header size");
+
+struct Layout {
+  size_t hdr, off, rbstart, rblist, inv, rowinfo, tickets, total;
+  int64_t n_tickets;  // batch * k_blocks, rounded up to a multiple of 4
+};
+
+struct Plan {
+  int variant;         // 0 wide row blocks, 1 narrow row blocks
+  int dtype;           // pgg_dtype
+  int rows_per_block;  // MMA N extent
+  int stages;
+  int threads;
+  int smem_bytes;
+  int k_blocks;
+  int band_k_blocks;
+  int64_t max_row_blocks;
+  int64_t M, N, K, G, batch, topK;
+  int row_idx_type;
+  int nk;  // reduction steps: ceil(N / elements per 128-byte row)
+  Layout layout;
+};
+
+// Per-row record written by the routing kernels: token and rank of the
+// expanded row among that token's rows (by increasing expanded index).
+struct RowInfo {
+  int32_t token;
+  int32_t rank;
+};
+
+struct GemmArgs {
+  const int4* rblist;     // {expert, first row, rows, 0} per row block
+  const RowInfo* rowinfo; // [M]
+  uint32_t* tickets;      // [batch * k_blocks]
+  WsHeader* hdr;
+  float* out;             // [batch, K]
+  int64_t K;
+  int64_t batch;
+  int32_t k_blocks;
+  int32_t band_k_blocks;
+  int32_t nk;
+  uint32_t ticket_bias;
+  uint64_t wait_limit_ns;
+};
+
+}  // namespace pgg

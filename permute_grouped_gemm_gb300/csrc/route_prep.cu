@@ -1,0 +1,226 @@
+// Routing preprocess for the fused d_x backward ("MoeInitRoutingGroupedMatmulGrad
+// design", sections 2.4.1 and 2.5.3: per-expert prefix tables, the flattened
+// list of blocks over all non-empty experts, and the inverse of the routing
+// index for rowIdxType 1).
+//
+// Three small launches, in stream order:
+//   route_scan     (1 CTA)  exclusive scan of groupList -> off[G+1]; row-block
+//                           counts and their scan -> rbstart[G+1]; the row-block
+//                           list {expert, first row, rows}; header reset; the
+//                           sum / sign check of groupList.
+//   route_scatter  (grid)   range check of expandedRowIdx and its inverse
+//                           inv[idx[q]] = q; zeroes the scatter-add tickets.
+//   route_rank     (grid)   per token b: its topK expanded rows, the check that
+//                           the index is a permutation, and each row's rank
+//                           among the token's rows (increasing expanded index).
+//
+// The index is read as the constraint table and note 1 of section "输入输出"
+// state: rowIdxType 0 maps expanded row -> original position, rowIdxType 1
+// maps original position -> expanded row; original position = b * topK + j.
+
+#include <cstdint>
+
+#include "pgg_internal.h"
+
+namespace pgg {
+
+namespace {
+
+// Exclusive scan of one int64 per thread over the block (blockDim.x <= 1024).
+__device__ int64_t block_exclusive_scan(int64_t v, int64_t* total, int64_t* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += y;
+    }
+    if (lane < nwarps) s_warp[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int64_t before = warp > 0 ? s_warp[warp - 1] : 0;
+  *total = s_warp[nwarps - 1];
+  __syncthreads();  // s_warp is reused by the next call
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int64_t* __restrict__ group_list,
+                                                          int64_t G, int64_t M,
+                                                          int rows_per_block, WsHeader* hdr,
+                                                          int64_t* __restrict__ off,
+                                                          int32_t* __restrict__ rbstart,
+                                                          int4* __restrict__ rblist) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int64_t s_rows, s_blocks;
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_rows = 0;
+    s_blocks = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  for (int64_t base = 0; base < G; base += blockDim.x) {
+    const int64_t g = base + tid;
+    int64_t c = 0;
+    if (g < G) {
+      c = group_list[g];
+      if (c < 0 || c > M) {
+        s_bad = 1;
+        c = 0;
+      }
+    }
+    const int64_t nb = (c + rows_per_block - 1) / rows_per_block;
+    int64_t tot_c, tot_b;
+    const int64_t ex_c = block_exclusive_scan(c, &tot_c, s_warp);
+    const int64_t ex_b = block_exclusive_scan(nb, &tot_b, s_warp);
+    if (g < G) {
+      off[g] = s_rows + ex_c;
+      rbstart[g] = static_cast<int32_t>(s_blocks + ex_b);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      s_rows += tot_c;
+      s_blocks += tot_b;
+    }
+    __syncthreads();
+  }
+  const bool ok = !s_bad && s_rows == M;
+  const int64_t n_rb = ok ? s_blocks : 0;
+  if (tid == 0) {
+    off[G] = s_rows;
+    rbstart[G] = static_cast<int32_t>(s_blocks);
+    hdr->status = ok ? 0u : kStGroupSum;
+    hdr->sched_next = 0;
+    hdr->n_row_blocks = static_cast<uint32_t>(n_rb);
+    hdr->timeout_site = 0;
+  }
+  __syncthreads();
+  for (int64_t e = tid; e < n_rb; e += blockDim.x) {
+    // largest g with rbstart[g] <= e; it has rbstart[g + 1] > e, so it is non-empty
+    int64_t lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (rbstart[mid] <= e)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int64_t j = e - rbstart[lo];
+    const int64_t row0 = off[lo] + j * rows_per_block;
+    const int64_t rem = off[lo + 1] - row0;
+    const int64_t rows = rem < rows_per_block ? rem : rows_per_block;
+    rblist[e] = make_int4(static_cast<int>(lo), static_cast<int>(row0), static_cast<int>(rows), 0);
+  }
+}
+
+__global__ void route_scatter_kernel(const int64_t* __restrict__ idx, int64_t M,
+                                     int32_t* __restrict__ inv, WsHeader* hdr,
+                                     uint4* __restrict__ tickets4, int64_t n_tickets4) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  bool bad = false;
+  for (int64_t q = t0; q < M; q += stride) {
+    const int64_t v = idx[q];
+    if (v < 0 || v >= M)
+      bad = true;
+    else
+      inv[v] = static_cast<int32_t>(q);
+  }
+  if (bad) atomicCAS(&hdr->status, 0u, kStIndex);
+  for (int64_t t = t0; t < n_tickets4; t += stride) tickets4[t] = make_uint4(0, 0, 0, 0);
+}
+
+// Expanded row of original position p, or -1 if the index does not describe a
+// permutation at p. Values in inv may be left over from earlier calls; a stale
+// value can only pass the check if this call wrote it (see pgg_route_rank).
+__device__ __forceinline__ int64_t row_of_position(const int64_t* idx, const int32_t* inv,
+                                                   int64_t p, int64_t M, int row_idx_type) {
+  if (row_idx_type == 0) {
+    // inv[p] = q with idx[q] == p, if some q was scattered to p
+    const int64_t q = inv[p];
+    if (q < 0 || q >= M || idx[q] != p) return -1;
+    return q;
+  }
+  const int64_t i = idx[p];
+  if (i < 0 || i >= M || inv[i] != p) return -1;
+  return i;
+}
+
+// A stale inv[p] (not written by this call) equal to q passes the type-0 check
+// only if idx[q] == p, but then the scatter of this call wrote inv[p]: so every
+// accepted p has a preimage, and M positions with preimages among M rows make
+// the index a permutation. For type 1 inv[idx[p]] was written by this call by
+// some p' with idx[p'] == idx[p]; it equals p for every p only if idx is
+// injective.
+__global__ void route_rank_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                                  int64_t batch, int64_t top_k, int64_t M, int row_idx_type,
+                                  RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < batch;
+       b += stride) {
+    const int64_t p0 = b * top_k;
+    for (int64_t j = 0; j < top_k; ++j) {
+      const int64_t i = row_of_position(idx, inv, p0 + j, M, row_idx_type);
+      if (i < 0) {
+        bad = true;
+        continue;
+      }
+      int32_t rank = 0;
+      for (int64_t j2 = 0; j2 < top_k; ++j2) {
+        const int64_t i2 = row_of_position(idx, inv, p0 + j2, M, row_idx_type);
+        if (i2 >= 0 && i2 < i) ++rank;
+      }
+      RowInfo r;
+      r.token = static_cast<int32_t>(b);
+      r.rank = rank;
+      rowinfo[i] = r;
+    }
+  }
+  if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
+}
+
+}  // namespace
+
+cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
+                              void* workspace, int num_sms, cudaStream_t stream) {
+  char* ws = static_cast<char*>(workspace);
+  const Layout& L = plan.layout;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
+  int64_t* off = reinterpret_cast<int64_t*>(ws + L.off);
+  int32_t* rbstart = reinterpret_cast<int32_t*>(ws + L.rbstart);
+  int4* rblist = reinterpret_cast<int4*>(ws + L.rblist);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  RowInfo* rowinfo = reinterpret_cast<RowInfo*>(ws + L.rowinfo);
+  uint4* tickets4 = reinterpret_cast<uint4*>(ws + L.tickets);
+
+  route_scan_kernel<<<1, 1024, 0, stream>>>(group_list, plan.G, plan.M, plan.rows_per_block, hdr,
+                                            off, rbstart, rblist);
+  const int64_t work = plan.M > plan.layout.n_tickets / 4 ? plan.M : plan.layout.n_tickets / 4;
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, plan.M, inv, hdr,
+                                                                     tickets4,
+                                                                     plan.layout.n_tickets / 4);
+  int64_t rblocks = (plan.batch + 127) / 128;
+  if (rblocks > cap) rblocks = cap;
+  if (rblocks < 1) rblocks = 1;
+  route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
+      idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace pgg

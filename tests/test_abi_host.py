@@ -1,0 +1,120 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import permute_grouped_gemm_gb300 as pgg
+from permute_grouped_gemm_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    return pgg.load()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pgg_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "pgg_dx_execute" in names and "pgg_dx_workspace_size" in names
+    raw = ctypes.CDLL(pbuild.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+# large-config sizes (pages' scale): M = 108000, G = 60, K = 7168, N = 2048
+LARGE = dict(M=108000, N=2048, K=7168, G=60, L=108000, batch=13500, topK=8)
+
+
+def ws(**o):
+    a = dict(LARGE, rowIdxType=0, dtype=pgg.PGG_BF16)
+    a.update(o)
+    return pgg.pgg_dx_workspace_size(a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"],
+                                     a["topK"], a["rowIdxType"], a["dtype"])
+
+
+def code_of(**o):
+    with pytest.raises(pgg.PggError) as e:
+        ws(**o)
+    return pgg.STATUS[e.value.code]
+
+
+def test_workspace_is_small_and_independent_of_n(lib):
+    w = ws()
+    assert w <= 16 * 2**20
+    assert ws(N=4096) == w            # no dependence on N
+    assert ws(M=2048, L=2048, batch=256, G=256) < 256 * 1024  # skinny
+    # grows with M (index tables) but never holds an [M, K] array
+    assert w < LARGE["M"] * LARGE["K"] // 64
+
+
+def test_host_errors(lib):
+    assert code_of(L=107999) == "PGG_ERR_SHAPE"           # L != M
+    assert code_of(batch=13499) == "PGG_ERR_SHAPE"        # M != batch * topK
+    assert code_of(topK=0) == "PGG_ERR_ATTR"
+    assert code_of(batch=0) == "PGG_ERR_ATTR"
+    assert code_of(rowIdxType=2) == "PGG_ERR_ATTR"
+    assert code_of(dtype=3) == "PGG_ERR_DTYPE"
+    assert code_of(N=2047) == "PGG_ERR_ALIGN"             # row stride not 16-byte multiple
+    assert code_of(N=6, dtype=pgg.PGG_F32) == "PGG_ERR_ALIGN"
+    assert code_of(M=2**31, L=2**31, batch=2**28) == "PGG_ERR_SHAPE"
+    assert code_of(K=0) == "PGG_ERR_SHAPE"
+    assert code_of(G=0) == "PGG_ERR_SHAPE"
+
+
+def test_execute_rejects_before_any_cuda_call(lib):
+    # null pointers and a short workspace are reported without a GPU
+    a = LARGE
+    rc = pgg.pgg_dx_execute(0, 0, 0, 0, a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"],
+                            a["topK"], 0, pgg.PGG_BF16, 0, 0, 0, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_NULL"
+    fake = 1 << 20  # aligned non-null addresses: never dereferenced on these paths
+    need = ws()
+    rc = pgg.pgg_dx_execute(fake, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+                            a["batch"], a["topK"], 0, pgg.PGG_BF16, fake, need - 1, fake, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_WORKSPACE"
+    rc = pgg.pgg_dx_execute(fake + 8, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+                            a["batch"], a["topK"], 0, pgg.PGG_BF16, fake, need, fake, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_ALIGN"
+    rc = pgg.pgg_dx_execute(fake, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+                            a["batch"], a["topK"], 0, pgg.PGG_BF16, fake + 64, need, fake, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_ALIGN"
+    rc = pgg.pgg_dx_route_prep(0, fake, a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"],
+                               a["topK"], 0, pgg.PGG_BF16, fake, need, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_NULL"
+
+
+def test_plan_variants(lib):
+    big = pgg.pgg_dx_plan(108000, 2048, 7168, 60, 108000, 13500, 8, 0, pgg.PGG_BF16)
+    skinny = pgg.pgg_dx_plan(2048, 2048, 7168, 256, 2048, 256, 8, 0, pgg.PGG_BF16)
+    assert big["variant"] == 0 and big["rows_per_block"] == 256 and big["k_blocks"] == 56
+    assert skinny["variant"] == 1 and skinny["rows_per_block"] == 32
+    for p in (big, skinny):
+        assert p["smem_bytes"] <= 227 * 1024
+        assert p["k_per_block"] == 128
+    pgg.pgg_debug_force_variant(1)
+    try:
+        assert pgg.pgg_dx_plan(108000, 2048, 7168, 60, 108000, 13500, 8, 0,
+                               pgg.PGG_BF16)["variant"] == 1
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+
+
+def test_status_strings(lib):
+    for code, name in pgg.STATUS.items():
+        assert pgg.pgg_status_string(code) != "unknown status", name

@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerance for every dtype: max |GPU - oracle| <= 1e-4 * max |oracle| over the
+compared rows. The GPU result must also be bitwise identical from run to run.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_case, make_inputs
+from workloads.moe import with_row_idx_type
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from permute_grouped_gemm_gb300 import build as pbuild
+    pbuild.build()
+    oracle.build()
+    pgg.load()
+    yield
+    pgg.pgg_debug_force_variant(-1)
+    pgg.pgg_debug_set_ticket_bias(0)
+    pgg.pgg_debug_set_wait_limit_ns(0)
+
+
+def run(inp, **kw):
+    out, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                     inp.batch, inp.top_k, inp.row_idx_type, **kw)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+def ref_rows(inp, tokens=None):
+    return oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                     inp.batch, inp.top_k, inp.row_idx_type, tokens=tokens)
+
+
+def assert_close(got, ref, what=""):
+    scale = np.abs(ref).max()
+    err = np.abs(got - ref).max()
+    assert err <= TOL * scale, f"{what}: max|diff| {err:.3e} > {TOL} * {scale:.3e}"
+
+
+def check(inp, tokens=None, what=""):
+    out, ws = run(inp)
+    assert pgg.status(ws) == 0, pgg.STATUS.get(pgg.status(ws))
+    got = out.double().cpu().numpy()
+    if tokens is not None:
+        got = got[np.asarray(tokens)]
+    assert_close(got, ref_rows(inp, tokens), what)
+    return out
+
+
+# The page's white-box list (section 4.2.1), shapes whose row stride the
+# tensor-memory-access unit accepts. N=1 and N=286 are covered by the
+# alignment test below.
+WHITE_BOX = {
+    "one_token_one_expert": dict(batch=1, K=128, N=256, top_k=1, G=1),
+    "one_token_multi_expert": dict(batch=1, K=128, N=256, top_k=3, G=3),
+    "multi_token_one_expert": dict(batch=128, K=128, N=256, top_k=1, G=1),
+    "multi_token_multi_expert": dict(batch=128, K=128, N=256, top_k=3, G=10),
+    "empty_expert": dict(batch=10, K=128, N=256, top_k=2, G=4, empty=(1,)),
+    "tail_k178_n280": dict(batch=10, K=178, N=280, top_k=3, G=4),
+    "k_is_1": dict(batch=128, K=1, N=256, top_k=3, G=4),
+}
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("row_idx_type", [0, 1])
+@pytest.mark.parametrize("case", sorted(WHITE_BOX))
+def test_white_box(case, dtype, row_idx_type):
+    inp = make_case(dtype=dtype, row_idx_type=row_idx_type, seed=3, device="cuda",
+                    **WHITE_BOX[case])
+    if case == "empty_expert":
+        assert int(inp.group_list[1]) == 0
+    check(inp, what=case)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_large_m_white_box(dtype):
+    # "大 token 数": batch = 108 * 1024, topK = 2, G = 60, K = 128, N = 256
+    inp = make_case(batch=108 * 1024, top_k=2, G=60, K=128, N=256, dtype=dtype, seed=4,
+                    device="cuda")
+    toks = np.random.default_rng(0).choice(inp.batch, 256, replace=False)
+    check(inp, tokens=toks, what="large M")
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_multi_tile_ragged(dtype, variant):
+    # several k blocks with a ragged tail, a ragged reduction tail, groups of
+    # 0 .. several hundred rows
+    pgg.pgg_debug_force_variant(variant)
+    try:
+        inp = make_case(batch=300, top_k=4, G=7, K=400, N=328 if dtype != "fp32" else 332,
+                        dtype=dtype, routing="zipf", zipf_zero=2, seed=5, device="cuda")
+        assert (inp.group_list == 0).sum() == 2
+        check(inp, what=f"variant {variant}")
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_same_expert_twice_for_a_token(dtype):
+    # degenerate routing: rows of one token inside one tile must still be
+    # added in order (no deadlock, correct sum)
+    for variant in (0, 1):
+        pgg.pgg_debug_force_variant(variant)
+        try:
+            inp = make_case(batch=200, top_k=4, G=3, K=256, N=128, dtype=dtype,
+                            routing="replacement", seed=6, device="cuda")
+            check(inp, what=f"replacement variant {variant}")
+        finally:
+            pgg.pgg_debug_force_variant(-1)
+
+
+def test_bitwise_repeatable():
+    inp = make_case(batch=2048, top_k=8, G=16, K=512, N=256, dtype="bf16", seed=7,
+                    device="cuda")
+    first, ws = run(inp)
+    for _ in range(4):
+        again, _ = run(inp, workspace=ws)
+        assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+
+
+def test_gather_and_scatter_forms_agree_bitwise():
+    inp0 = make_case(batch=500, top_k=6, G=12, K=256, N=192, dtype="fp16", seed=8,
+                     device="cuda")
+    inp1 = with_row_idx_type(inp0, 1)
+    a, _ = run(inp0)
+    b, _ = run(inp1)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_device_detected_errors_zero_the_output():
+    base = make_case(batch=64, top_k=2, G=4, K=128, N=64, dtype="bf16", seed=9, device="cuda")
+    cases = {}
+    idx = base.expanded_row_idx.clone()
+    idx[5] = base.batch * base.top_k  # out of range
+    cases["PGG_ERR_INDEX"] = (idx, base.group_list)
+    idx = base.expanded_row_idx.clone()
+    idx[5] = idx[6]
+    cases["PGG_ERR_NOT_PERM"] = (idx, base.group_list)
+    gl = base.group_list.clone()
+    gl[0] += 1
+    cases["PGG_ERR_GROUPSUM"] = (base.expanded_row_idx, gl)
+    gl = base.group_list.clone()
+    gl[1] += gl[0] + 1
+    gl[0] = -1
+    cases["PGG_ERR_GROUPSUM_NEG"] = (base.expanded_row_idx, gl)
+    for name, (idx, gl) in cases.items():
+        out = torch.full((64, 128), 7.0, device="cuda")
+        _, ws = pgg.dx(base.grad_y, base.weight, idx, gl, 64, 2, 0, out=out)
+        torch.cuda.synchronize()
+        assert pgg.STATUS[pgg.status(ws)] == name.replace("_NEG", ""), name
+        assert torch.count_nonzero(out) == 0
+    # the context is still usable
+    check(base, what="after errors")
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    inp = make_case(batch=256, top_k=4, G=8, K=256, N=128, dtype="bf16", seed=10,
+                    device="cuda")
+    pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    pgg.pgg_debug_set_ticket_bias(1000)          # no ticket ever reaches rank + 1000
+    try:
+        _, ws = run(inp)
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
+    finally:
+        pgg.pgg_debug_set_ticket_bias(0)
+        pgg.pgg_debug_set_wait_limit_ns(0)
+    check(inp, what="after timeout")
+
+
+def test_no_writes_outside_out_and_workspace():
+    inp = make_case(batch=100, top_k=3, G=5, K=200, N=96, dtype="bf16", seed=11, device="cuda")
+    need = pgg.workspace_bytes(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                               inp.batch, inp.top_k, 0)
+    guard = 4096
+    ws_buf = torch.full((need + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    out_buf = torch.full((100 * 200 + 2 * 1024,), -3.0, device="cuda")
+    ws = ws_buf[guard:guard + need]
+    out = out_buf[1024:1024 + 100 * 200].view(100, 200)
+    _, _ = run(inp, out=out, workspace=ws)
+    assert pgg.status(ws) == 0
+    assert (ws_buf[:guard] == 0xA5).all() and (ws_buf[guard + need:] == 0xA5).all()
+    assert (out_buf[:1024] == -3.0).all() and (out_buf[1024 + 100 * 200:] == -3.0).all()
+    assert_close(out.double().cpu().numpy(), ref_rows(inp))
+
+
+def test_unaligned_row_stride_is_rejected():
+    for N in (1, 286):
+        inp = make_case(batch=128, top_k=3, G=4, K=128, N=N, dtype="bf16", seed=12,
+                        device="cuda")
+        with pytest.raises(pgg.PggError) as e:
+            run(inp)
+        assert pgg.STATUS[e.value.code] == "PGG_ERR_ALIGN"
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def test_workload_tiny_fp32_full():
+    w = WORKLOADS["tiny-fp32"]
+    inp = make_inputs(w, device="cuda")
+    out = check(inp, what=w.name)
+    again, _ = run(inp)
+    assert torch.equal(out.view(torch.int32), again.view(torch.int32))
+
+
+@pytest.mark.parametrize("name", ["uniform-bf16", "skewed-fp16", "large-bf16", "skinny-bf16"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda")
+    out, ws = run(inp)
+    assert pgg.status(ws) == 0
+    rng = np.random.default_rng(1)
+    toks = np.sort(rng.choice(w.batch, min(w.batch, 24), replace=False))
+    got = out.double().cpu().numpy()[toks]
+    assert_close(got, ref_rows(inp, toks), name)
+    again, _ = run(inp, workspace=ws)
+    assert torch.equal(out.view(torch.int32), again.view(torch.int32))
+    # every row was written: no row left at its initial content
+    assert torch.isfinite(out).all()
