@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MoE permute + grouped-matmul backward (d_x).
+
+One step = one pass of the whole path on one batch: the routing preprocess
+(groupList scan, row-block list, inverse index, ranks) and the persistent
+grouped GEMM with the fused ordered scatter-add into FP32 d_x. Inputs are
+seeded synthetic tensors already resident in HBM; L2 is flushed (256 MiB
+write) between steps, outside the per-step CUDA events.
+
+Metric: fused d_x TFLOP/s = 2*M*N*K / step time, with the roofline fraction
+of the grouped-GEMM kernel and the workspace bytes.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the path needs no exchange); value sums the work of
+all ranks over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "uniform-bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace bytes"
+KERNEL_SOURCES = ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu",
+                  "permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh",
+                  "permute_grouped_gemm_gb300/csrc/pgg_internal.h",
+                  "permute_grouped_gemm_gb300/csrc/pgg_api.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it
+    was taken on the current kernel source (matching hash), else None."""
+    path = os.path.join(ROOT, "profiles", f"gmm_dx_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("|").strip()
+        for key in ("kernel_source_hash", "dram_bytes_per_launch"):
+            if line.startswith(key + ":"):
+                vals[key] = line.split(":", 1)[1].strip().split()[0]
+    if vals.get("kernel_source_hash") != kernel_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def algorithmic(inp):
+    """(flops, bytes) of one step: 2*M*N*K, and d_y once + weight of non-empty
+    experts once + d_x written once + the two index arrays."""
+    w = inp.workload
+    es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+    nonempty = int((inp.group_list > 0).sum())
+    flops = 2 * w.M * w.N * w.K
+    nbytes = (w.M * w.N * es + nonempty * w.K * w.N * es + w.batch * w.K * 4
+              + w.M * 8 + w.G * 8)
+    return flops, nbytes
+
+
+def cpu_baseline(inp, target_s: float):
+    """The oracle (as it stands) on a bounded sample of the workload's tokens."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    w = inp.workload
+    host = inp.to("cpu")
+    rng = np.random.default_rng(0)
+    per_tok = 2 * w.top_k * w.N * w.K
+    cores = oracle.host_cores()
+    n = max(1, min(w.batch, cores))
+    toks = np.sort(rng.choice(w.batch, n, replace=False))
+    t0 = time.perf_counter()
+    oracle.dx(host.grad_y, host.weight, host.expanded_row_idx, host.group_list, w.batch,
+              w.top_k, w.row_idx_type, tokens=toks)
+    dt = time.perf_counter() - t0
+    if dt < target_s / 4 and n < w.batch:
+        n = int(min(w.batch, max(n, n * target_s / max(dt, 1e-3))))
+        toks = np.sort(rng.choice(w.batch, n, replace=False))
+        t0 = time.perf_counter()
+        oracle.dx(host.grad_y, host.weight, host.expanded_row_idx, host.group_list, w.batch,
+                  w.top_k, w.row_idx_type, tokens=toks)
+        dt = time.perf_counter() - t0
+    return {"value": per_tok * n / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, n),
+            "kind": "oracle",
+            "sample": f"{n} of {w.batch} tokens (all topK rows each), fp64 C++ loops, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle timed on the host cores: each step a bounded token sample."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from workloads import WORKLOADS, make_inputs
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, device="cpu")
+    cores = oracle.host_cores()
+    per_tok = 2 * w.top_k * w.N * w.K
+    # size each step to ~ (a few minutes) / (steps + warmup)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rng = np.random.default_rng(0)
+    n = max(1, min(w.batch, cores))
+    t0 = time.perf_counter()
+    oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, w.batch, w.top_k,
+              w.row_idx_type, tokens=np.arange(n))
+    probe = time.perf_counter() - t0
+    n = int(max(1, min(w.batch, n * budget / max(probe, 1e-3))))
+    times = []
+    for s in range(args.warmup + args.steps):
+        toks = np.sort(rng.choice(w.batch, n, replace=False))
+        t0 = time.perf_counter()
+        oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, w.batch,
+                  w.top_k, w.row_idx_type, tokens=toks)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = per_tok * n / dt / 1e12
+    sample = f"{n} of {w.batch} tokens per step (all topK rows each), fp64 C++ loops"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(cores, n),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import permute_grouped_gemm_gb300 as pgg
+    from permute_grouped_gemm_gb300 import build as pbuild
+    from workloads import WORKLOADS, make_inputs
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pbuild.build()
+    pgg.load()
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, device=dev)
+    dt_code = pgg.dtype_code(inp.grad_y.dtype)
+    M, N, K, G = w.M, w.N, w.K, w.G
+    sizes = (M, N, K, G, M, w.batch, w.top_k)
+    ws_bytes = pgg.pgg_dx_workspace_size(*sizes, w.row_idx_type, dt_code)
+    plan = pgg.pgg_dx_plan(*sizes, w.row_idx_type, dt_code)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(w.batch, K, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ptrs = (inp.grad_y.data_ptr(), inp.weight.data_ptr(), inp.expanded_row_idx.data_ptr(),
+            inp.group_list.data_ptr())
+
+    def route_prep():
+        rc = pgg.pgg_dx_route_prep(ptrs[2], ptrs[3], *sizes, w.row_idx_type, dt_code,
+                                   ws.data_ptr(), ws_bytes, sp)
+        if rc:
+            raise pgg.PggError(rc, "route_prep")
+
+    def gemm():
+        rc = pgg.pgg_dx_grouped_gemm(*ptrs, *sizes, w.row_idx_type, dt_code, ws.data_ptr(),
+                                     ws_bytes, out.data_ptr(), sp)
+        if rc:
+            raise pgg.PggError(rc, "grouped_gemm")
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        route_prep()
+        gemm()
+    torch.cuda.synchronize()
+    if pgg.status(ws) != 0:
+        raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
+    alloc_delta = torch.cuda.max_memory_allocated(dev) - base_alloc
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            route_prep()
+            ev[s][1].record(stream)
+            gemm()
+            ev[s][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    gemm_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    prep_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    if pgg.status(ws) != 0:
+        raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
+    mean_step = statistics.mean(step_ms)
+    mean_gemm = statistics.mean(gemm_ms)
+    if dist:
+        t = torch.tensor([mean_step, mean_gemm], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_step, mean_gemm = float(t[0]), float(t[1])
+
+    flops, nbytes = algorithmic(inp)
+    value = world * flops / (mean_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm:
+        bound, achieved = "tensor", flops / (mean_gemm * 1e-3) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        if w.dtype == "fp32":
+            # 3 tf32 products per fp32 product; tf32 dense rate is half of bf16
+            peak = peaks["bf16_tflops"] / 2 / 3
+    else:
+        bound, achieved = "hbm", nbytes / (mean_gemm * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    traffic = recorded_traffic(w.name)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(inp, pgg, dt_code, sizes, w, ws, ws_bytes, dev, stream, flops, world,
+                          dist)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded; routing and value recipe in DESIGN.md)",
+        "config": {**w.describe(), "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "plan": plan},
+        "workspace_bytes": ws_bytes,
+        "torch_alloc_delta_bytes": int(alloc_delta),
+        "phases_ms": {"route_prep": statistics.mean(prep_ms), "grouped_gemm": mean_gemm},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'profiling recipe fallback'})",
+                     "kernel": "gmm_dx_kernel", "algorithmic_flops": flops,
+                     "algorithmic_bytes": nbytes},
+        "clocks": clk.summary(),
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_region": t_wall,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def measure_e2e(inp, pgg, dt_code, sizes, w, ws, ws_bytes, dev, stream, flops, world, dist):
+    """Same metric through the public call with host buffers: every step copies
+    the inputs from pinned host memory, runs pgg_dx_execute and copies d_x back."""
+    import torch
+    h_dy = inp.grad_y.cpu().pin_memory()
+    h_w = inp.weight.cpu().pin_memory()
+    h_idx = inp.expanded_row_idx.cpu().pin_memory()
+    h_gl = inp.group_list.cpu().pin_memory()
+    h_out = torch.empty(w.batch, w.K, dtype=torch.float32).pin_memory()
+    d_dy = torch.empty_like(inp.grad_y)
+    d_w = torch.empty_like(inp.weight)
+    d_idx = torch.empty_like(inp.expanded_row_idx)
+    d_gl = torch.empty_like(inp.group_list)
+    d_out = torch.empty(w.batch, w.K, dtype=torch.float32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_dy, h_w, h_idx, h_gl))
+    d2h = h_out.numel() * 4
+    steps = 5
+
+    def step():
+        d_dy.copy_(h_dy, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        d_gl.copy_(h_gl, non_blocking=True)
+        rc = pgg.pgg_dx_execute(d_dy.data_ptr(), d_w.data_ptr(), d_idx.data_ptr(),
+                                d_gl.data_ptr(), *sizes, w.row_idx_type, dt_code, ws.data_ptr(),
+                                ws_bytes, d_out.data_ptr(), stream.cuda_stream)
+        if rc:
+            raise pgg.PggError(rc, "pgg_dx_execute")
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    if not torch.equal(h_out, d_out.cpu()):
+        raise RuntimeError("e2e readback mismatch")
+    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -171,10 +171,14 @@ const char* pgg_status_string(int status);
  *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
  * pgg_debug_force_variant: -1 = automatic (default), 0 or 1 = force the
  *   variant reported by pgg_dx_plan.
+ * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
+ *   automatic). The result does not depend on it, bit for bit: only the time
+ *   order of the tiles changes, never the order of the additions.
  */
 void pgg_debug_set_wait_limit_ns(uint64_t ns);
 void pgg_debug_set_ticket_bias(uint32_t bias);
 void pgg_debug_force_variant(int variant);
+void pgg_debug_set_band_k_blocks(int k_blocks);
 
 #ifdef __cplusplus
 }

@@ -10,8 +10,11 @@
 // expert and 128 consecutive output columns k. The MMA is issued with the
 // weight slice as operand A (M = 128 rows of k) and the d_y rows as operand B
 // (N = rows, rounded up to 16), both K-major along n, so that the accumulator
-// in tensor memory holds lane = k, column = expanded row. The epilogue then
-// writes each expanded row's 128 values of k as coalesced 128-byte segments.
+// in tensor memory holds lane = k, column = expanded row. The epilogue moves
+// each expanded row's 128 values of k into a shared-memory staging row and
+// hands the 512-byte segment of d_x to the tensor-memory-access unit as one
+// bulk store or bulk fp32 reduce-add (the addition happens in L2), so the
+// scatter-add costs the SM a handful of instructions per row.
 //
 // Warp roles (one CTA per SM, persistent):
 //   warp 0       tile scheduler + TMA producer (one lane)
@@ -68,6 +71,12 @@ struct DtTraits<PGG_F32> {
 
 constexpr int kQueue = 4;
 
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
 template <int DT, int ROWS, int STAGES>
 struct Cfg {
   static constexpr bool kSplit = DtTraits<DT>::kSplit;
@@ -76,7 +85,7 @@ struct Cfg {
   static constexpr int kBBytes = ROWS * kRowBytes;
   static constexpr int kStageBytes = (kABytes + kBBytes) * (kSplit ? 2 : 1);
   static constexpr int kAccCols = ROWS < 32 ? 32 : ROWS;
-  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);  // allocation unit
   static constexpr int kWords = (ROWS + 31) / 32;
   static constexpr int kEpiWarps = 4;
   static constexpr int kXformWarps = kSplit ? 4 : 0;
@@ -86,8 +95,13 @@ struct Cfg {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
+// Epilogue staging for the bulk path: rows x 128 fp32 (one 512-byte d_x row
+// segment per expanded row), two buffers of kChunk rows.
+constexpr int kChunk = 16;
+
 template <int ROWS, int STAGES>
 struct Ctl {
+  float stg[2][kChunk][kKBlock];
   uint64_t full[STAGES];   // TMA bytes landed
   uint64_t empty[STAGES];  // MMAs reading the stage completed
   uint64_t ready[STAGES];  // fp32 split done
@@ -128,6 +142,14 @@ __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint3
   if (atomicCAS(&hdr->status, 0u, code) == 0u) hdr->timeout_site = site;
 }
 
+// Index of the smallest d_y box (32 << j rows, at most ROWS) that covers R rows.
+template <int ROWS>
+__device__ __forceinline__ int dy_box(int R) {
+  int j = 0;
+  while ((kDyMinRows << j) < R && (kDyMinRows << j) < ROWS) ++j;
+  return j;
+}
+
 // Tile number -> (row block, k block). Bands of `band` k blocks; inside a band
 // row-block-major, k block fastest.
 __device__ __forceinline__ void decode_tile(uint32_t t, uint32_t n_rb, uint32_t kbs, uint32_t band,
@@ -142,7 +164,7 @@ __device__ __forceinline__ void decode_tile(uint32_t t, uint32_t n_rb, uint32_t 
 }
 
 template <int DT, int ROWS, int STAGES>
-__device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const CUtensorMap* tm_dy,
+__device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy_maps,
                          const CUtensorMap* tm_w, const GemmArgs& args, uint32_t total) {
   using C = Cfg<DT, ROWS, STAGES>;
   const uint64_t lim = args.wait_limit_ns;
@@ -150,17 +172,21 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const CUtensorMa
   int stage = 0, qs = 0;
   uint32_t phase = 0, qph = 0, outstanding = 0, last_parity = 0;
   const uint32_t n_rb = args.hdr->n_row_blocks;
+  const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
+  const uint32_t band = static_cast<uint32_t>(args.band_k_blocks);
+  auto entry = [&](uint32_t t) {
+    if (t >= total) return make_int4(-1, 0, 0, 0);
+    uint32_t rb, kb;
+    decode_tile(t, n_rb, kbs, band, &rb, &kb);
+    const int4 r = args.rblist[rb];
+    return make_int4(r.x, r.y, r.z, static_cast<int>(kb));
+  };
+  // The next tile is claimed and its row block read while the current one
+  // streams, so no tile starts with a scheduler round trip.
+  int4 e = entry(atomicAdd(&args.hdr->sched_next, 1u));
   bool failed = false;
   while (!failed) {
-    const uint32_t t = atomicAdd(&args.hdr->sched_next, 1u);
-    int4 e = make_int4(-1, 0, 0, 0);
-    if (t < total) {
-      uint32_t rb, kb;
-      decode_tile(t, n_rb, static_cast<uint32_t>(args.k_blocks),
-                  static_cast<uint32_t>(args.band_k_blocks), &rb, &kb);
-      const int4 r = args.rblist[rb];
-      e = make_int4(r.x, r.y, r.z, static_cast<int>(kb));
-    }
+    const uint32_t t_next = e.x >= 0 ? atomicAdd(&args.hdr->sched_next, 1u) : total;
     if (!ptx::mbar_wait(&ctl->qempty[qs], qph ^ 1u, lim, abort)) {
       failed = true;
       break;
@@ -172,8 +198,11 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const CUtensorMa
       qph ^= 1u;
     }
     if (e.x < 0) break;
-    const int nb = (e.z + kDyBoxRows - 1) / kDyBoxRows;
-    const uint32_t tx = C::kABytes + static_cast<uint32_t>(nb) * kDyBoxRows * kRowBytes;
+    const int bj = dy_box<ROWS>(e.z);
+    const CUtensorMap* tm_dy = &dy_maps->box[bj];
+    const uint32_t tx = C::kABytes + static_cast<uint32_t>(kDyMinRows << bj) * kRowBytes;
+    int4 e_next = make_int4(-1, 0, 0, 0);
+    bool have_next = false;
     for (int ks = 0; ks < args.nk; ++ks) {
       if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
         failed = true;
@@ -183,16 +212,22 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const CUtensorMa
       ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
       const int32_t n0 = ks * C::kElemsPerRow;
       ptx::tma_load_3d(sa, tm_w, &ctl->full[stage], n0, e.w * kKBlock, e.x);
-      for (int c = 0; c < nb; ++c)
-        ptx::tma_load_2d(sa + C::kABytes + c * kDyBoxRows * kRowBytes, tm_dy, &ctl->full[stage], n0,
-                         e.y + c * kDyBoxRows);
+      ptx::tma_load_2d(sa + C::kABytes, tm_dy, &ctl->full[stage], n0, e.y);
       outstanding |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
+      if (ks == 1 || ks + 1 == args.nk) {
+        if (!have_next) {
+          e_next = entry(t_next);
+          have_next = true;
+        }
+      }
     }
+    if (!have_next) e_next = entry(t_next);
+    e = e_next;
   }
   if (failed) {
     ctl->abort = 1;
@@ -301,8 +336,7 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
       qph ^= 1u;
     }
     if (e.x < 0) break;
-    const int nb = (e.z + kDyBoxRows - 1) / kDyBoxRows;
-    const int n_b4 = nb * kDyBoxRows * kRowBytes / 16;
+    const int n_b4 = (kDyMinRows << dy_box<ROWS>(e.z)) * kRowBytes / 16;
     bool stop = false;
     for (int ks = 0; ks < args.nk && !stop; ++ks) {
       ok = ptx::mbar_wait(&ctl->full[stage], phase, lim, abort);
@@ -340,6 +374,118 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
   }
 }
 
+// Rows of the tile whose ticket says they may be added now. Thread et looks
+// after rows et and et + 128; a warp ballot forms each 32-row mask word.
+template <int ROWS, int STAGES>
+__device__ __forceinline__ void ready_rows(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args, int R,
+                                           uint32_t kb, bool gave_up) {
+  constexpr int kWords = (ROWS + 31) / 32;
+  const int et = threadIdx.x - 64, ew = et >> 5, lane = threadIdx.x & 31;
+  const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
+  bool go[2] = {false, false};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = et + 128 * h;
+    if (r < R && ((ctl->pend[r >> 5] >> (r & 31)) & 1u)) {
+      const RowInfo m = ctl->meta[r];
+      go[h] = m.rank == 0 || gave_up;
+      if (!go[h]) {
+        const uint32_t have =
+            ptx::ld_acquire_gpu(args.tickets + static_cast<int64_t>(m.token) * kbs + kb);
+        go[h] = have >= static_cast<uint32_t>(m.rank) + args.ticket_bias;
+      }
+    }
+  }
+  const uint32_t w0 = __ballot_sync(0xffffffffu, go[0]);
+  const uint32_t w1 = __ballot_sync(0xffffffffu, go[1]);
+  if (lane == 0) {
+    if (ew < kWords) ctl->rdy[ew] = w0;
+    if (ew + 4 < kWords) ctl->rdy[ew + 4] = w1;
+  }
+}
+
+// Writes the ready rows through the tensor-memory-access unit: each warp moves
+// its 32 k values of kChunk rows from tensor memory into a staging row
+// [row][128 k] in shared memory; one thread per row then issues a bulk copy
+// (rank 0) or bulk fp32 reduce-add (rank > 0) of the row's segment of d_x.
+// Needs K % 4 == 0 (16-byte aligned segments).
+template <int ROWS, int STAGES>
+__device__ __forceinline__ void write_rows_bulk(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
+                                                uint32_t t_lane, int R, uint32_t kb, int quarter) {
+  const int et = threadIdx.x - 64, ew = et >> 5, lane = threadIdx.x & 31;
+  const int64_t K = args.K;
+  const int64_t k0 = static_cast<int64_t>(kb) * kKBlock;
+  const uint32_t bytes = static_cast<uint32_t>((K - k0 < kKBlock ? K - k0 : kKBlock) * 4);
+  const int nchunks = (R + kChunk - 1) / kChunk;
+  bool fenced = false;
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    // the warp that issued chunk c - 2 from this buffer waits for its reads
+    if (c >= 2 && ew == ((c - 2) & 3)) ptx::bulk_wait_read_all();
+    uint32_t v[kChunk];
+    ptx::tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(c * kChunk), v);
+    ptx::tmem_ld_wait();
+    ptx::named_bar_sync(1, 128);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) ctl->stg[buf][j][32 * quarter + lane] = __uint_as_float(v[j]);
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(1, 128);
+    if (ew == (c & 3) && lane < kChunk) {
+      const int r = c * kChunk + lane;
+      if (r < R && ((ctl->rdy[r >> 5] >> (r & 31)) & 1u)) {
+        const RowInfo m = ctl->meta[r];
+        float* dst = args.out + static_cast<int64_t>(m.token) * K + k0;
+        if (!fenced) {
+          ptx::fence_proxy_async_global();
+          fenced = true;
+        }
+        if (m.rank == 0)
+          ptx::bulk_store(dst, &ctl->stg[buf][lane][0], bytes);
+        else
+          ptx::bulk_reduce_add_f32(dst, &ctl->stg[buf][lane][0], bytes);
+      }
+      ptx::bulk_commit();
+    }
+  }
+  // every issued row is complete (performed in global memory) before its
+  // ticket is published
+  ptx::bulk_wait_all();
+  ptx::fence_proxy_async_global();
+}
+
+// Scalar path for K % 4 != 0: lane = k, one 128-byte store or reduction per
+// row and warp.
+template <int ROWS, int STAGES>
+__device__ __forceinline__ void write_rows_scalar(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
+                                                  uint32_t t_lane, int R, uint32_t kb,
+                                                  int quarter) {
+  const int lane = threadIdx.x & 31;
+  const int64_t K = args.K;
+  const int64_t k = static_cast<int64_t>(kb) * kKBlock + 32 * quarter + lane;
+  const bool k_ok = k < K;
+  const int nchunks = (R + 31) / 32;
+  for (int c = 0; c < nchunks; ++c) {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c * 32), v);
+    ptx::tmem_ld_wait();
+    const uint32_t word = ctl->rdy[c];
+    if (k_ok && word) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (word & (1u << j)) {
+          const RowInfo m = ctl->meta[c * 32 + j];
+          float* p = args.out + static_cast<int64_t>(m.token) * K + k;
+          const float x = __uint_as_float(v[j]);
+          if (m.rank == 0)
+            *p = x;
+          else
+            ptx::red_add_f32_gpu(p, x);
+        }
+      }
+    }
+  }
+}
+
 template <int DT, int ROWS, int STAGES>
 __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmArgs& args) {
   using C = Cfg<DT, ROWS, STAGES>;
@@ -348,7 +494,6 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
   const int et = threadIdx.x - 64;  // 0..127
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;     // tensor-memory lanes this warp may read
-  const int64_t K = args.K;
   const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
   int qs = 0, acc = 0;
   uint32_t qph = 0, aph = 0;
@@ -356,7 +501,13 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
   while (true) {
     bool ok = ptx::mbar_wait(&ctl->qfull[qs], qph, lim, abort);
     const int4 e = ctl->q[qs];
-    if (bar_any(1, 128, !ok || ctl->abort)) break;
+    if (bar_any(1, 128, !ok || ctl->abort)) {
+      if (!ok) {
+        ctl->abort = 1;
+        if (et == 0) raise_status(args.hdr, kStTimeout, 4);
+      }
+      break;
+    }
     if (et == 0) ptx::mbar_arrive(&ctl->qempty[qs]);
     if (++qs == kQueue) {
       qs = 0;
@@ -367,36 +518,25 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     const uint32_t kb = static_cast<uint32_t>(e.w);
     for (int r = et; r < R; r += 128) ctl->meta[r] = args.rowinfo[row0 + r];
     if (et < C::kWords) {
-      const int lo = et * 32;
-      const int n = R - lo;
+      const int n = R - et * 32;
       ctl->pend[et] = n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
     }
     ok = ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
-    if (bar_any(1, 128, !ok || ctl->abort)) break;
+    if (bar_any(1, 128, !ok || ctl->abort)) {
+      if (!ok) {
+        ctl->abort = 1;
+        if (et == 0) raise_status(args.hdr, kStTimeout, 5);
+      }
+      break;
+    }
     ptx::tc_fence_after_sync();
 
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
                             static_cast<uint32_t>(acc * C::kAccCols);
-    const int64_t k = static_cast<int64_t>(kb) * kKBlock + 32 * quarter + lane;
-    const bool k_ok = k < K;
     uint64_t t_wait0 = 0;
     while (true) {
       // 1. which pending rows may go now
-      if (et < C::kWords) ctl->rdy[et] = 0u;
-      ptx::named_bar_sync(1, 128);
-      for (int r = et; r < R; r += 128) {
-        const uint32_t bit = 1u << (r & 31);
-        if (ctl->pend[r >> 5] & bit) {
-          const RowInfo m = ctl->meta[r];
-          bool go = m.rank == 0 || gave_up;
-          if (!go) {
-            const uint32_t have =
-                ptx::ld_acquire_gpu(args.tickets + static_cast<int64_t>(m.token) * kbs + kb);
-            go = have >= static_cast<uint32_t>(m.rank) + args.ticket_bias;
-          }
-          if (go) atomicOr(&ctl->rdy[r >> 5], bit);
-        }
-      }
+      ready_rows(ctl, args, R, kb, gave_up);
       ptx::named_bar_sync(1, 128);
       bool any = false;
 #pragma unroll
@@ -413,28 +553,11 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
         }
         continue;
       }
-      // 2. write the ready rows: lane = k, one 128-byte segment per row and warp
-      const int nchunks = (R + 31) / 32;
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c * 32), v);
-        ptx::tmem_ld_wait();
-        const uint32_t word = ctl->rdy[c];
-        if (k_ok && word) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (word & (1u << j)) {
-              const RowInfo m = ctl->meta[c * 32 + j];
-              float* p = args.out + static_cast<int64_t>(m.token) * K + k;
-              const float x = __uint_as_float(v[j]);
-              if (m.rank == 0)
-                *p = x;
-              else
-                ptx::red_add_f32_gpu(p, x);
-            }
-          }
-        }
-      }
+      // 2. write the ready rows
+      if (args.bulk)
+        write_rows_bulk(ctl, args, t_lane, R, kb, quarter);
+      else
+        write_rows_scalar(ctl, args, t_lane, R, kb, quarter);
       ptx::named_bar_sync(1, 128);
       // 3. publish: the rows' additions happen-before the ticket bumps
       bool mine = false;
@@ -463,7 +586,7 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
 
 template <int DT, int ROWS, int STAGES>
 __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
-    gmm_dx_kernel(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_w,
+    gmm_dx_kernel(const __grid_constant__ DyMaps dy_maps, const __grid_constant__ CUtensorMap tm_w,
                   const GemmArgs args) {
   using C = Cfg<DT, ROWS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -502,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tm_dy);
+    for (int j = 0; j < kDyMaps; ++j) ptx::tma_prefetch_desc(&dy_maps.box[j]);
     ptx::tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
@@ -515,7 +638,7 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer<DT, ROWS, STAGES>(smem, ctl, &tm_dy, &tm_w, args, total);
+    if (lane == 0) producer<DT, ROWS, STAGES>(smem, ctl, &dy_maps, &tm_w, args, total);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<DT, ROWS, STAGES>(smem, ctl, tmem_base, args);
   } else if (warp < 2 + C::kEpiWarps) {
@@ -533,7 +656,7 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
 }
 
 template <int DT, int ROWS, int STAGES>
-cudaError_t launch_t(const CUtensorMap& tdy, const CUtensorMap& tw, const GemmArgs& args, int grid,
+cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& args, int grid,
                      cudaStream_t stream) {
   using C = Cfg<DT, ROWS, STAGES>;
   constexpr int smem = smem_bytes<DT, ROWS, STAGES>();
@@ -569,7 +692,7 @@ bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads,
   return false;
 }
 
-cudaError_t launch_grouped_gemm(int dtype, int variant, const CUtensorMap& tdy, const CUtensorMap& tw,
+cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy, const CUtensorMap& tw,
                                 const GemmArgs& args, int grid, cudaStream_t stream) {
 #define PGG_LAUNCH(DT, V, R, S) \
   if (dtype == DT && variant == V) return launch_t<DT, R, S>(tdy, tw, args, grid, stream);

@@ -18,7 +18,7 @@ namespace pgg {
 
 cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
                               void* workspace, int num_sms, cudaStream_t stream);
-cudaError_t launch_grouped_gemm(int dtype, int variant, const CUtensorMap& tdy,
+cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy,
                                 const CUtensorMap& tw, const GemmArgs& args, int grid,
                                 cudaStream_t stream);
 bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem);
@@ -29,6 +29,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 std::atomic<uint32_t> g_ticket_bias{0};
 std::atomic<int> g_force_variant{-1};
+std::atomic<int> g_band_k_blocks{0};
 
 constexpr int64_t kInt32Max = 2147483647;
 
@@ -66,7 +67,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   p->topK = topK;
   p->row_idx_type = rowIdxType;
   p->k_blocks = static_cast<int>((K + kKBlock - 1) / kKBlock);
-  p->band_k_blocks = p->k_blocks;
+  const int band = g_band_k_blocks.load();
+  p->band_k_blocks = (band > 0 && band < p->k_blocks) ? band : p->k_blocks;
   const int elems_per_row = kRowBytes / elem_size(dtype);
   p->nk = static_cast<int>((N + elems_per_row - 1) / elems_per_row);
   p->max_row_blocks = (M + p->rows_per_block - 1) / p->rows_per_block + G;
@@ -137,20 +139,20 @@ CUtensorMapDataType tmap_type(int dtype) {
   return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 }
 
-// d_y [M, N] as a 2-D map; boxes of 32 rows x one 128-byte row segment.
-// weight [G, K, N] as a 3-D map; boxes of 1 expert x 128 k x one segment.
-// Rows or columns outside the tensor read as zero.
-int encode_maps(const Plan& p, const void* dy, const void* w, CUtensorMap* tdy, CUtensorMap* tw) {
+// d_y [M, N] as 2-D maps with boxes of 32, 64, 128 and 256 rows x one
+// 128-byte row segment. weight [G, K, N] as a 3-D map; boxes of 1 expert x
+// 128 k x one segment. Rows or columns outside the tensor read as zero.
+int encode_maps(const Plan& p, const void* dy, const void* w, DyMaps* tdy, CUtensorMap* tw) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PGG_ERR_CUDA;
   const cuuint64_t es = static_cast<cuuint64_t>(elem_size(p.dtype));
   const cuuint32_t box_n = static_cast<cuuint32_t>(kRowBytes / es);
-  {
+  for (int j = 0; j < kDyMaps; ++j) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * es};
-    cuuint32_t box[2] = {box_n, static_cast<cuuint32_t>(kDyBoxRows)};
+    cuuint32_t box[2] = {box_n, static_cast<cuuint32_t>(kDyMinRows << j)};
     cuuint32_t estr[2] = {1, 1};
-    if (enc(tdy, tmap_type(p.dtype), 2, const_cast<void*>(dy), dims, strides, box, estr,
+    if (enc(&tdy->box[j], tmap_type(p.dtype), 2, const_cast<void*>(dy), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PGG_ERR_CUDA;
@@ -202,7 +204,8 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
                      cudaStream_t stream) {
   DeviceInfo di;
   if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
-  CUtensorMap tdy, tw;
+  DyMaps tdy;
+  CUtensorMap tw;
   int rc = encode_maps(plan, gradY, weight, &tdy, &tw);
   if (rc != PGG_OK) return rc;
   char* w = static_cast<char*>(ws);
@@ -218,6 +221,7 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   a.band_k_blocks = plan.band_k_blocks;
   a.nk = plan.nk;
   a.ticket_bias = g_ticket_bias.load();
+  a.bulk = (plan.K % 4 == 0) ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   const int64_t max_tiles = plan.max_row_blocks * plan.k_blocks;
   const int grid = static_cast<int>(max_tiles < di.num_sms ? max_tiles : di.num_sms);
@@ -330,5 +334,7 @@ void pgg_debug_set_wait_limit_ns(uint64_t ns) {
 void pgg_debug_set_ticket_bias(uint32_t bias) { g_ticket_bias.store(bias); }
 
 void pgg_debug_force_variant(int variant) { g_force_variant.store(variant); }
+
+void pgg_debug_set_band_k_blocks(int k_blocks) { g_band_k_blocks.store(k_blocks); }
 
 }  // extern "C"

@@ -17,8 +17,15 @@ constexpr int kKBlock = 128;
 // Bytes of one operand row inside a pipeline stage: one 128-byte swizzle atom
 // along the reduction dimension (64 half-precision or 32 fp32 elements).
 constexpr int kRowBytes = 128;
-// Rows of d_y fetched by one tensor-memory-access copy.
-constexpr int kDyBoxRows = 32;
+// d_y is read through four tensor maps whose boxes are 32, 64, 128 and 256
+// rows high; each tile takes one copy with the smallest box that covers its
+// rows (the number of copies, not their size, limits the copy engine here).
+constexpr int kDyMaps = 4;
+constexpr int kDyMinRows = 32;
+
+struct alignas(64) DyMaps {
+  CUtensorMap box[kDyMaps];  // box[j]: 32 << j rows x one 128-byte row segment
+};
 
 // Status codes written by the kernels (same values as pgg_status).
 constexpr uint32_t kStIndex = 16, kStGroupSum = 17, kStNotPerm = 18, kStTimeout = 19;
@@ -73,6 +80,7 @@ struct GemmArgs {
   int32_t band_k_blocks;
   int32_t nk;
   uint32_t ticket_bias;
+  int32_t bulk;  // 1: epilogue rows go through bulk copies / bulk reductions (K % 4 == 0)
   uint64_t wait_limit_ns;
 };
 

@@ -28,6 +28,7 @@ def built():
     pgg.load()
     yield
     pgg.pgg_debug_force_variant(-1)
+    pgg.pgg_debug_set_band_k_blocks(0)
     pgg.pgg_debug_set_ticket_bias(0)
     pgg.pgg_debug_set_wait_limit_ns(0)
 
@@ -130,6 +131,20 @@ def test_bitwise_repeatable():
     for _ in range(4):
         again, _ = run(inp, workspace=ws)
         assert torch.equal(again.view(torch.int32), first.view(torch.int32))
+
+
+def test_tile_order_does_not_change_a_bit():
+    inp = make_case(batch=1024, top_k=8, G=12, K=1024, N=256, dtype="bf16", seed=13,
+                    device="cuda")
+    base, ws = run(inp)
+    try:
+        for band in (1, 3, 5):
+            pgg.pgg_debug_set_band_k_blocks(band)
+            again, _ = run(inp, workspace=ws)
+            assert torch.equal(again.view(torch.int32), base.view(torch.int32)), band
+    finally:
+        pgg.pgg_debug_set_band_k_blocks(0)
+    assert_close(base.double().cpu().numpy(), ref_rows(inp))
 
 
 def test_gather_and_scatter_forms_agree_bitwise():
