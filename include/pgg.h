@@ -180,6 +180,41 @@ void pgg_debug_set_ticket_bias(uint32_t bias);
 void pgg_debug_force_variant(int variant);
 void pgg_debug_set_band_k_blocks(int k_blocks);
 
+/*
+ * pgg_dx_execute for callers that cannot allocate device memory. (The pages
+ * have no counterpart of this call; it is a service of this library.)
+ *
+ * Who needs it: code that has no allocator at hand when the gradient is due
+ * -- a plugin inside a framework that owns all device memory, a serving or
+ * real-time runtime that reserved HBM up front and forbids cudaMalloc later,
+ * plain C code without an allocator handle. Such a caller passes the same
+ * inputs and `out` as to pgg_dx_execute, but no workspace: the call uses a
+ * fixed 8 MiB scratch array that the library's CUDA module reserves on every
+ * device that loads the library, held until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   status  optional device pointer (may be NULL); after the work on `stream`
+ *           has finished it holds the device-detected status word that
+ *           pgg_dx_execute would have left at the start of its workspace.
+ *
+ * Returns PGG_ERR_WORKSPACE when pgg_dx_workspace_size for these sizes exceeds
+ * 8 MiB (8388608 bytes; e.g. M = 108000, K = 7168 needs 4.3 MB), and
+ * otherwise what pgg_dx_execute returns.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture on the device. Every call on a device shares the one
+ * array, and each call re-initialises what it needs, so leftover contents from
+ * the previous call do no harm -- but two calls whose work overlaps on the GPU
+ * (for example on two streams without ordering between them) race on the
+ * array and give wrong results. Order such calls on one stream.
+ */
+int pgg_dx_execute_static_scratch(const void* gradY, const void* weight,
+                                  const int64_t* expandedRowIdx, const int64_t* groupList,
+                                  int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                                  int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                                  float* out, uint32_t* status, pgg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,8 +62,10 @@ def load(path: str | None = None):
             lib.pgg_dx_execute.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, vp, sz, vp, vp]
             lib.pgg_dx_grouped_gemm.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, vp, sz, vp, vp]
             lib.pgg_dx_route_prep.argtypes = [vp, vp, *_SIZES, i32, i32, vp, sz, vp]
+            lib.pgg_dx_execute_static_scratch.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, vp,
+                                                          vp, vp]
             for f in ("pgg_dx_workspace_size", "pgg_dx_plan", "pgg_dx_execute",
-                      "pgg_dx_grouped_gemm", "pgg_dx_route_prep"):
+                      "pgg_dx_grouped_gemm", "pgg_dx_route_prep", "pgg_dx_execute_static_scratch"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.pgg_status_string.argtypes = [ctypes.c_int]
             lib.pgg_status_string.restype = ctypes.c_char_p
@@ -115,6 +117,17 @@ def pgg_dx_grouped_gemm(gradY, weight, expandedRowIdx, groupList, M, N, K, G, L,
     return load().pgg_dx_grouped_gemm(gradY, weight, expandedRowIdx, groupList, M, N, K, G, L,
                                       batch, topK, rowIdxType, dtype, workspace, workspace_bytes,
                                       out, stream)
+
+
+def pgg_dx_execute_static_scratch(gradY, weight, expandedRowIdx, groupList, M, N, K, G, L, batch,
+                                  topK, rowIdxType, dtype, out, status, stream) -> int:
+    """pgg_dx_execute without a workspace argument, for callers that cannot
+    allocate device memory: the library's fixed 8 MiB device scratch is used.
+    `status` is an optional device address (0 = none) that receives the
+    device-detected status word. Returns the pgg_status code."""
+    return load().pgg_dx_execute_static_scratch(gradY, weight, expandedRowIdx, groupList, M, N, K,
+                                                G, L, batch, topK, rowIdxType, dtype, out,
+                                                status or None, stream)
 
 
 def pgg_status_string(code: int) -> str:

@@ -338,3 +338,68 @@ void pgg_debug_force_variant(int variant) { g_force_variant.store(variant); }
 void pgg_debug_set_band_k_blocks(int k_blocks) { g_band_k_blocks.store(k_blocks); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.
+//
+// Some callers of this library have no way to obtain scratch memory at the
+// moment they need the gradient: a plugin running inside a framework that owns
+// every device allocation and exposes no allocator to it, a serving or
+// real-time runtime that reserves all of HBM up front and forbids cudaMalloc
+// afterwards (a late allocation could fail or stall), or plain C code with no
+// allocator handle at all. pgg_dx_execute_static_scratch serves them: it
+// takes the same inputs and output as pgg_dx_execute but no workspace, and
+// uses instead the fixed scratch array below, which the CUDA module reserves
+// on every device that loads this library and keeps until the process exits.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+
+// The device-side scratch. In host code this name is only a stand-in for the
+// symbol, not a device address: its address is looked up per device below.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the first call on a device does this; it should come before any
+// stream capture on that device).
+int static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PGG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PGG_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return PGG_OK;
+}
+
+}  // namespace
+
+extern "C" int pgg_dx_execute_static_scratch(const void* gradY, const void* weight,
+                                             const int64_t* expandedRowIdx,
+                                             const int64_t* groupList, int64_t M, int64_t N,
+                                             int64_t K, int64_t G, int64_t L, int64_t batch,
+                                             int64_t topK, int rowIdxType, pgg_dtype dtype,
+                                             float* out, uint32_t* status, pgg_stream_t stream) {
+  size_t need = 0;
+  int rc = pgg_dx_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype, &need);
+  if (rc != PGG_OK) return rc;
+  if (need > kStaticScratchBytes) return PGG_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  rc = static_scratch_address(&scratch);
+  if (rc != PGG_OK) return rc;
+  rc = pgg_dx_execute(gradY, weight, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                      rowIdxType, dtype, scratch, kStaticScratchBytes, out, stream);
+  if (rc != PGG_OK || !status) return rc;
+  // the status word is the first uint32 of the scratch
+  return cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
