@@ -144,9 +144,10 @@ int pgg_dx_grouped_gemm(const void* gradY, const void* weight, const int64_t* ex
 
 /* How pgg_dx_execute will run a problem of these sizes (host only, no CUDA call). */
 typedef struct {
-  int32_t variant;          /* 0 = wide row blocks (tensor-bound), 1 = narrow row blocks (streaming) */
+  int32_t variant;          /* 0 = wide row blocks on CTA pairs (tensor-bound), 1 = narrow row
+                               blocks (weight streaming), 2 = wide row blocks on single CTAs */
   int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent */
-  int32_t k_per_block;      /* output columns per tile: the MMA M extent (128) */
+  int32_t k_per_block;      /* output columns per CTA and tile (128; a CTA pair covers 256) */
   int32_t stages;           /* shared-memory pipeline depth */
   int32_t k_blocks;         /* ceil(K / k_per_block) */
   int32_t band_k_blocks;    /* k-blocks per band of the tile order */
@@ -154,6 +155,7 @@ typedef struct {
   size_t workspace_bytes;   /* as pgg_dx_workspace_size */
   int32_t threads;          /* threads per CTA of the grouped-GEMM kernel */
   int32_t smem_bytes;       /* dynamic shared memory per CTA */
+  int32_t cta_pair;         /* 1: clusters of two CTAs share each tile (tcgen05 cta_group::2) */
 } pgg_plan_info;
 
 int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
@@ -169,8 +171,8 @@ const char* pgg_status_string(int status);
  * pgg_debug_set_ticket_bias: added to the ticket count each ordered
  *   scatter-add waits for; a positive bias makes every wait of a row with
  *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
- * pgg_debug_force_variant: -1 = automatic (default), 0 or 1 = force the
- *   variant reported by pgg_dx_plan.
+ * pgg_debug_force_variant: -1 = automatic (default), 0, 1 or 2 = force the
+ *   variant reported by pgg_dx_plan (2 exists for the 16-bit dtypes only).
  * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
  *   automatic). The result does not depend on it, bit for bit: only the time
  *   order of the tiles changes, never the order of the additions.

@@ -37,6 +37,7 @@ class PlanInfo(ctypes.Structure):
         ("k_blocks", ctypes.c_int32), ("band_k_blocks", ctypes.c_int32),
         ("max_row_blocks", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t),
         ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+        ("cta_pair", ctypes.c_int32),
     ]
 
     def as_dict(self):

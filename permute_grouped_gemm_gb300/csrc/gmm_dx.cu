@@ -12,9 +12,8 @@
 // (N = rows, rounded up to 16), both K-major along n, so that the accumulator
 // in tensor memory holds lane = k, column = expanded row. The epilogue moves
 // each expanded row's 128 values of k into a shared-memory staging row and
-// hands the 512-byte segment of d_x to the tensor-memory-access unit as one
-// bulk store or bulk fp32 reduce-add (the addition happens in L2), so the
-// scatter-add costs the SM a handful of instructions per row.
+// writes the 512-byte segment of d_x with one vector store (the row's first
+// contribution) or one vector fp32 reduction performed at L2 (later ones).
 //
 // Warp roles (one CTA per SM, persistent):
 //   warp 0       tile scheduler + TMA producer (one lane)
@@ -22,6 +21,17 @@
 //   warps 2..5   epilogue: TMEM -> registers -> ordered scatter-add into d_x
 //   warps 6..9   fp32 inputs only: split each staged fp32 tile into tf32
 //                high and low parts for the 3-product tf32 MMA
+//
+// CTA pairs (the tensor-bound 16-bit variant): two CTAs of a cluster share
+// one tile of 256 k x up to 256 rows. Each holds half of the weight slice
+// (its 128 k) and half of the rows in its own shared memory; the even CTA
+// issues tcgen05.mma.cta_group::2, which reads both halves and leaves each
+// CTA's 128 accumulator lanes in that CTA's tensor memory. Per SM this halves
+// the d_y bytes staged per MMA, so the shared-memory port (written by TMA,
+// read by the tensor core) carries a third less traffic per flop than a
+// single-CTA 128 x 256 tile. The even CTA claims tiles and forwards them to its
+// peer; the peer's copies complete on the even CTA's barriers; MMA
+// completions are multicast to both CTAs.
 //
 // Tiles are handed out by an atomic counter in increasing order of a fixed
 // global numbering: bands of k blocks, then row blocks (expert-major, row
@@ -77,12 +87,14 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int DT, int ROWS, int STAGES>
+template <int DT, int ROWS, int STAGES, bool PAIR = false>
 struct Cfg {
   static constexpr bool kSplit = DtTraits<DT>::kSplit;
   static constexpr int kElemsPerRow = kRowBytes / DtTraits<DT>::kElem;
   static constexpr int kABytes = kKBlock * kRowBytes;
-  static constexpr int kBBytes = ROWS * kRowBytes;
+  // rows of d_y this CTA stages per k step (a pair splits the tile's rows)
+  static constexpr int kBRows = PAIR ? ROWS / 2 : ROWS;
+  static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStageBytes = (kABytes + kBBytes) * (kSplit ? 2 : 1);
   static constexpr int kAccCols = ROWS < 32 ? 32 : ROWS;
   static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);  // allocation unit
@@ -90,27 +102,41 @@ struct Cfg {
   static constexpr int kEpiWarps = 4;
   static constexpr int kXformWarps = kSplit ? 4 : 0;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kXformWarps);
+  static constexpr int kMmaM = PAIR ? 2 * kKBlock : kKBlock;
+  static constexpr int kNAlign = PAIR ? 32 : 16;  // MMA N granularity
+  // consumers of a tile-queue slot: MMA + epilogue (+ fp32 split), and in a
+  // pair the peer's producer and epilogue as well
+  static constexpr uint32_t kQEmpty = PAIR ? 4 : (kSplit ? 3 : 2);
+  static constexpr uint32_t kTEmpty = PAIR ? 2 * kEpiWarps : kEpiWarps;
   static_assert(ROWS % 32 == 0 && ROWS <= 256, "rows per block");
-  static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "tmem columns");
+  static_assert(!PAIR || (!kSplit && ROWS % 64 == 0), "pairs: 16-bit inputs, rows % 64 == 0");
+  static_assert(kTmemCols <= 512, "tmem columns");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
-// Epilogue staging for the bulk path: rows x 128 fp32 (one 512-byte d_x row
+// MMA N extent for a tile of R rows.
+template <class C>
+__device__ __forceinline__ int mma_n(int R) {
+  const int n = (R + C::kNAlign - 1) / C::kNAlign * C::kNAlign;
+  return n < C::kNAlign ? C::kNAlign : n;
+}
+
+// Epilogue staging for the vector path: rows x 128 fp32 (one 512-byte d_x row
 // segment per expanded row), two buffers of kChunk rows.
 constexpr int kChunk = 16;
 
 template <int ROWS, int STAGES>
 struct Ctl {
   float stg[2][kChunk][kKBlock];
-  uint64_t full[STAGES];   // TMA bytes landed
+  uint64_t full[STAGES];   // TMA bytes landed (pairs: both CTAs' bytes, even CTA's barrier)
   uint64_t empty[STAGES];  // MMAs reading the stage completed
   uint64_t ready[STAGES];  // fp32 split done
   uint64_t tfull[2];       // accumulator complete
-  uint64_t tempty[2];      // accumulator drained by the epilogue
+  uint64_t tempty[2];      // accumulator drained by the epilogue(s)
   uint64_t qfull[kQueue];
   uint64_t qempty[kQueue];
   uint64_t drain;
-  int4 q[kQueue];  // {expert (-1 = stop), first row, rows, k block}
+  int4 q[kQueue];  // {expert (-1 = stop), first row, rows, k unit}
   uint32_t tmem_base;
   int abort;
   uint32_t pend[(ROWS + 31) / 32];
@@ -118,9 +144,10 @@ struct Ctl {
   RowInfo meta[ROWS];
 };
 
-template <int DT, int ROWS, int STAGES>
+template <int DT, int ROWS, int STAGES, bool PAIR>
 constexpr int smem_bytes() {
-  return 1024 + STAGES * Cfg<DT, ROWS, STAGES>::kStageBytes + static_cast<int>(sizeof(Ctl<ROWS, STAGES>));
+  return 1024 + STAGES * Cfg<DT, ROWS, STAGES, PAIR>::kStageBytes +
+         static_cast<int>(sizeof(Ctl<ROWS, STAGES>));
 }
 
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
@@ -142,11 +169,11 @@ __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint3
   if (atomicCAS(&hdr->status, 0u, code) == 0u) hdr->timeout_site = site;
 }
 
-// Index of the smallest d_y box (32 << j rows, at most ROWS) that covers R rows.
-template <int ROWS>
+// Index of the smallest d_y box (16 << j rows, at most CAP) that covers R rows.
+template <int CAP>
 __device__ __forceinline__ int dy_box(int R) {
   int j = 0;
-  while ((kDyMinRows << j) < R && (kDyMinRows << j) < ROWS) ++j;
+  while ((kDyMinRows << j) < R && (kDyMinRows << j) < CAP) ++j;
   return j;
 }
 
@@ -163,87 +190,125 @@ __device__ __forceinline__ void decode_tile(uint32_t t, uint32_t n_rb, uint32_t 
   *kb = kb_lo + rem % w;
 }
 
-template <int DT, int ROWS, int STAGES>
+template <int DT, int ROWS, int STAGES, bool PAIR>
 __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy_maps,
-                         const CUtensorMap* tm_w, const GemmArgs& args, uint32_t total) {
-  using C = Cfg<DT, ROWS, STAGES>;
+                         const CUtensorMap* tm_w, const GemmArgs& args, uint32_t total,
+                         uint32_t rank) {
+  using C = Cfg<DT, ROWS, STAGES, PAIR>;
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
+  const bool leader = rank == 0;
   int stage = 0, qs = 0;
   uint32_t phase = 0, qph = 0, outstanding = 0, last_parity = 0;
   const uint32_t n_rb = args.hdr->n_row_blocks;
-  const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
-  const uint32_t band = static_cast<uint32_t>(args.band_k_blocks);
+  const uint32_t units = static_cast<uint32_t>(args.k_units);
+  const uint32_t band = static_cast<uint32_t>(args.band_units);
   auto entry = [&](uint32_t t) {
     if (t >= total) return make_int4(-1, 0, 0, 0);
-    uint32_t rb, kb;
-    decode_tile(t, n_rb, kbs, band, &rb, &kb);
+    uint32_t rb, ku;
+    decode_tile(t, n_rb, units, band, &rb, &ku);
     const int4 r = args.rblist[rb];
-    return make_int4(r.x, r.y, r.z, static_cast<int>(kb));
+    return make_int4(r.x, r.y, r.z, static_cast<int>(ku));
   };
   // The next tile is claimed and its row block read while the current one
   // streams, so no tile starts with a scheduler round trip.
-  int4 e = entry(atomicAdd(&args.hdr->sched_next, 1u));
+  int4 e = make_int4(-1, 0, 0, 0);
+  if (leader) e = entry(atomicAdd(&args.hdr->sched_next, 1u));
   bool failed = false;
   while (!failed) {
-    const uint32_t t_next = e.x >= 0 ? atomicAdd(&args.hdr->sched_next, 1u) : total;
-    if (!ptx::mbar_wait(&ctl->qempty[qs], qph ^ 1u, lim, abort)) {
-      failed = true;
-      break;
+    uint32_t t_next = total;
+    if (leader) {
+      if (e.x >= 0) t_next = atomicAdd(&args.hdr->sched_next, 1u);
+      if (!ptx::mbar_wait(&ctl->qempty[qs], qph ^ 1u, lim, abort)) {
+        failed = true;
+        break;
+      }
+      ctl->q[qs] = e;
+      ptx::mbar_arrive(&ctl->qfull[qs]);
+      if constexpr (PAIR) {
+        ptx::st_cluster_v4(ptx::mapa(&ctl->q[qs], 1), e);
+        ptx::mbar_arrive_remote(ptx::mapa(&ctl->qfull[qs], 1));
+      }
+    } else {
+      if (!ptx::mbar_wait_cluster(&ctl->qfull[qs], qph, lim, abort)) {
+        failed = true;
+        break;
+      }
+      e = ctl->q[qs];
+      ptx::mbar_arrive_remote(ptx::mapa(&ctl->qempty[qs], 0));
     }
-    ctl->q[qs] = e;
-    ptx::mbar_arrive(&ctl->qfull[qs]);
     if (++qs == kQueue) {
       qs = 0;
       qph ^= 1u;
     }
     if (e.x < 0) break;
-    const int bj = dy_box<ROWS>(e.z);
+    const int nm = mma_n<C>(e.z);
+    const int b_rows = PAIR ? nm / 2 : e.z;  // rows of d_y this CTA stages
+    const int bj = dy_box<C::kBRows>(b_rows);
+    const uint32_t box_bytes = static_cast<uint32_t>(kDyMinRows << bj) * kRowBytes;
+    const uint32_t tx = PAIR ? 2 * (C::kABytes + box_bytes) : C::kABytes + box_bytes;
     const CUtensorMap* tm_dy = &dy_maps->box[bj];
-    const uint32_t tx = C::kABytes + static_cast<uint32_t>(kDyMinRows << bj) * kRowBytes;
+    const int kb = PAIR ? 2 * e.w + static_cast<int>(rank) : e.w;
+    const int brow = e.y + (PAIR ? static_cast<int>(rank) * (nm / 2) : 0);
     int4 e_next = make_int4(-1, 0, 0, 0);
     bool have_next = false;
     for (int ks = 0; ks < args.nk; ++ks) {
-      if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
+      const bool ok = PAIR ? ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)
+                           : ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort);
+      if (!ok) {
         failed = true;
         break;
       }
       uint8_t* sa = smem + stage * C::kStageBytes;
-      ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
       const int32_t n0 = ks * C::kElemsPerRow;
-      ptx::tma_load_3d(sa, tm_w, &ctl->full[stage], n0, e.w * kKBlock, e.x);
-      ptx::tma_load_2d(sa + C::kABytes, tm_dy, &ctl->full[stage], n0, e.y);
+      if constexpr (PAIR) {
+        const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
+        if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+        ptx::tma_load_3d_pair(sa, tm_w, fb, n0, kb * kKBlock, e.x);
+        ptx::tma_load_2d_pair(sa + C::kABytes, tm_dy, fb, n0, brow);
+      } else {
+        ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
+        ptx::tma_load_3d(sa, tm_w, &ctl->full[stage], n0, kb * kKBlock, e.x);
+        ptx::tma_load_2d(sa + C::kABytes, tm_dy, &ctl->full[stage], n0, brow);
+      }
       outstanding |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
-      if (ks == 1 || ks + 1 == args.nk) {
-        if (!have_next) {
-          e_next = entry(t_next);
-          have_next = true;
-        }
+      if (leader && !have_next && (ks == 1 || ks + 1 == args.nk)) {
+        e_next = entry(t_next);
+        have_next = true;
       }
     }
-    if (!have_next) e_next = entry(t_next);
-    e = e_next;
+    if (leader) {
+      if (!have_next) e_next = entry(t_next);
+      e = e_next;
+    }
   }
   if (failed) {
     ctl->abort = 1;
     raise_status(args.hdr, kStTimeout, 2);
   }
   // Never leave while a copy into this CTA's shared memory may be in flight.
+  // A pair's odd CTA cannot see its copies complete (they signal the even
+  // CTA's barrier); the even CTA's MMA consuming the stage implies it.
   int no_abort = 0;
-  for (int s = 0; s < STAGES; ++s)
-    if (outstanding & (1u << s))
-      ptx::mbar_wait(&ctl->full[s], (last_parity >> s) & 1u, lim, &no_abort);
+  for (int s = 0; s < STAGES; ++s) {
+    if (!(outstanding & (1u << s))) continue;
+    const uint32_t par = (last_parity >> s) & 1u;
+    if (!PAIR || leader)
+      ptx::mbar_wait(&ctl->full[s], par, lim, &no_abort);
+    else
+      ptx::mbar_wait_cluster(&ctl->empty[s], par, lim, &no_abort);
+  }
 }
 
-template <int DT, int ROWS, int STAGES>
+template <int DT, int ROWS, int STAGES, bool PAIR>
 __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base,
                            const GemmArgs& args) {
-  using C = Cfg<DT, ROWS, STAGES>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR>;
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   int stage = 0, qs = 0, acc = 0;
@@ -261,10 +326,11 @@ __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_
       qph ^= 1u;
     }
     if (e.x < 0) break;
-    uint32_t n_mma = (static_cast<uint32_t>(e.z) + 15u) & ~15u;
-    if (n_mma < 16u) n_mma = 16u;
-    const uint32_t idesc = ptx::idesc_make(DtTraits<DT>::kFmt, kKBlock, n_mma);
-    if (!ptx::mbar_wait(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
+    const uint32_t idesc =
+        ptx::idesc_make(DtTraits<DT>::kFmt, C::kMmaM, static_cast<uint32_t>(mma_n<C>(e.z)));
+    const bool ok_t = PAIR ? ptx::mbar_wait_cluster(&ctl->tempty[acc], aph ^ 1u, lim, abort)
+                           : ptx::mbar_wait(&ctl->tempty[acc], aph ^ 1u, lim, abort);
+    if (!ok_t) {
       failed = true;
       break;
     }
@@ -272,7 +338,9 @@ __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
     for (int ks = 0; ks < args.nk; ++ks) {
       uint64_t* bar = C::kSplit ? &ctl->ready[stage] : &ctl->full[stage];
-      if (!ptx::mbar_wait(bar, phase, lim, abort)) {
+      const bool ok = PAIR ? ptx::mbar_wait_cluster(bar, phase, lim, abort)
+                           : ptx::mbar_wait(bar, phase, lim, abort);
+      if (!ok) {
         failed = true;
         break;
       }
@@ -284,7 +352,9 @@ __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_
       for (int kk = 0; kk < kRowBytes / 32; ++kk) {
         const uint64_t koff = static_cast<uint64_t>((kk * 32) >> 4);
         const uint32_t accum = (ks | kk) != 0 ? 1u : 0u;
-        if constexpr (!C::kSplit) {
+        if constexpr (PAIR) {
+          ptx::mma_f16_pair(d_tmem, a_hi + koff, b_hi + koff, idesc, accum);
+        } else if constexpr (!C::kSplit) {
           ptx::mma_f16(d_tmem, a_hi + koff, b_hi + koff, idesc, accum);
         } else {
           const uint64_t a_lo = ptx::sdesc_sw128(sa + C::kABytes + C::kBBytes);
@@ -295,14 +365,20 @@ __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_
         }
       }
       issued = true;
-      ptx::mma_commit(&ctl->empty[stage]);
+      if constexpr (PAIR)
+        ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
+      else
+        ptx::mma_commit(&ctl->empty[stage]);
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (failed) break;
-    ptx::mma_commit(&ctl->tfull[acc]);
+    if constexpr (PAIR)
+      ptx::mma_commit_pair(&ctl->tfull[acc], 0x3);
+    else
+      ptx::mma_commit(&ctl->tfull[acc]);
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
@@ -313,7 +389,10 @@ __device__ void mma_issuer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, uint32_t tmem_
   if (issued) {
     // Tensor memory is released only after every issued MMA has completed.
     int no_abort = 0;
-    ptx::mma_commit(&ctl->drain);
+    if constexpr (PAIR)
+      ptx::mma_commit_pair(&ctl->drain, 0x1);
+    else
+      ptx::mma_commit(&ctl->drain);
     ptx::mbar_wait(&ctl->drain, 0u, lim, &no_abort);
   }
 }
@@ -404,53 +483,47 @@ __device__ __forceinline__ void ready_rows(Ctl<ROWS, STAGES>* ctl, const GemmArg
   }
 }
 
-// Writes the ready rows through the tensor-memory-access unit: each warp moves
-// its 32 k values of kChunk rows from tensor memory into a staging row
-// [row][128 k] in shared memory; one thread per row then issues a bulk copy
-// (rank 0) or bulk fp32 reduce-add (rank > 0) of the row's segment of d_x.
-// Needs K % 4 == 0 (16-byte aligned segments).
+// Writes the ready rows: each warp moves its 32 k values of kChunk rows from
+// tensor memory into staging rows [row][128 k] in shared memory; then each
+// warp sends whole 512-byte row segments, one st.global.v4 (rank 0) or
+// red.global.add.v4.f32 (rank > 0) warp instruction per row. The writes stay
+// on the load/store path: handing them to the tensor-memory-access unit as
+// bulk copies queued them in front of the main loop's operand loads and
+// starved the tensor cores. Needs K % 4 == 0 (16-byte aligned segments).
 template <int ROWS, int STAGES>
-__device__ __forceinline__ void write_rows_bulk(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
-                                                uint32_t t_lane, int R, uint32_t kb, int quarter) {
+__device__ __forceinline__ void write_rows_vec(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
+                                               uint32_t t_lane, int R, uint32_t kb, int quarter) {
   const int et = threadIdx.x - 64, ew = et >> 5, lane = threadIdx.x & 31;
   const int64_t K = args.K;
   const int64_t k0 = static_cast<int64_t>(kb) * kKBlock;
-  const uint32_t bytes = static_cast<uint32_t>((K - k0 < kKBlock ? K - k0 : kKBlock) * 4);
+  const int n4 = static_cast<int>((K - k0 < kKBlock ? K - k0 : kKBlock) / 4);
   const int nchunks = (R + kChunk - 1) / kChunk;
-  bool fenced = false;
+  constexpr int kRowsPerWarp = kChunk / 4;
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
-    // the warp that issued chunk c - 2 from this buffer waits for its reads
-    if (c >= 2 && ew == ((c - 2) & 3)) ptx::bulk_wait_read_all();
     uint32_t v[kChunk];
     ptx::tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(c * kChunk), v);
     ptx::tmem_ld_wait();
-    ptx::named_bar_sync(1, 128);
+    // (chunk c - 2 used this buffer; every warp finished reading it before the
+    // barrier of chunk c - 1)
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) ctl->stg[buf][j][32 * quarter + lane] = __uint_as_float(v[j]);
-    ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(1, 128);
-    if (ew == (c & 3) && lane < kChunk) {
-      const int r = c * kChunk + lane;
-      if (r < R && ((ctl->rdy[r >> 5] >> (r & 31)) & 1u)) {
+#pragma unroll
+    for (int jj = 0; jj < kRowsPerWarp; ++jj) {
+      const int j = ew * kRowsPerWarp + jj;
+      const int r = c * kChunk + j;
+      if (r < R && ((ctl->rdy[r >> 5] >> (r & 31)) & 1u) && lane < n4) {
         const RowInfo m = ctl->meta[r];
-        float* dst = args.out + static_cast<int64_t>(m.token) * K + k0;
-        if (!fenced) {
-          ptx::fence_proxy_async_global();
-          fenced = true;
-        }
+        const float4 x = *reinterpret_cast<const float4*>(&ctl->stg[buf][j][4 * lane]);
+        float* dst = args.out + static_cast<int64_t>(m.token) * K + k0 + 4 * lane;
         if (m.rank == 0)
-          ptx::bulk_store(dst, &ctl->stg[buf][lane][0], bytes);
+          *reinterpret_cast<float4*>(dst) = x;
         else
-          ptx::bulk_reduce_add_f32(dst, &ctl->stg[buf][lane][0], bytes);
+          ptx::red_add_v4_f32_gpu(dst, x);
       }
-      ptx::bulk_commit();
     }
   }
-  // every issued row is complete (performed in global memory) before its
-  // ticket is published
-  ptx::bulk_wait_all();
-  ptx::fence_proxy_async_global();
 }
 
 // Scalar path for K % 4 != 0: lane = k, one 128-byte store or reduction per
@@ -486,20 +559,23 @@ __device__ __forceinline__ void write_rows_scalar(Ctl<ROWS, STAGES>* ctl, const 
   }
 }
 
-template <int DT, int ROWS, int STAGES>
-__device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmArgs& args) {
-  using C = Cfg<DT, ROWS, STAGES>;
+template <int DT, int ROWS, int STAGES, bool PAIR>
+__device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmArgs& args,
+                         uint32_t rank) {
+  using C = Cfg<DT, ROWS, STAGES, PAIR>;
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int et = threadIdx.x - 64;  // 0..127
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;     // tensor-memory lanes this warp may read
   const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
+  const bool remote = PAIR && rank != 0;  // queue and accumulator barriers live in the even CTA
   int qs = 0, acc = 0;
   uint32_t qph = 0, aph = 0;
   bool gave_up = false;
   while (true) {
-    bool ok = ptx::mbar_wait(&ctl->qfull[qs], qph, lim, abort);
+    bool ok = remote ? ptx::mbar_wait_cluster(&ctl->qfull[qs], qph, lim, abort)
+                     : ptx::mbar_wait(&ctl->qfull[qs], qph, lim, abort);
     const int4 e = ctl->q[qs];
     if (bar_any(1, 128, !ok || ctl->abort)) {
       if (!ok) {
@@ -508,20 +584,27 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
       }
       break;
     }
-    if (et == 0) ptx::mbar_arrive(&ctl->qempty[qs]);
+    if (et == 0) {
+      if (remote)
+        ptx::mbar_arrive_remote(ptx::mapa(&ctl->qempty[qs], 0));
+      else
+        ptx::mbar_arrive(&ctl->qempty[qs]);
+    }
     if (++qs == kQueue) {
       qs = 0;
       qph ^= 1u;
     }
     if (e.x < 0) break;
     const int R = e.z, row0 = e.y;
-    const uint32_t kb = static_cast<uint32_t>(e.w);
+    const uint32_t kb = PAIR ? 2u * static_cast<uint32_t>(e.w) + rank : static_cast<uint32_t>(e.w);
+    const bool kb_ok = kb < kbs;  // a pair's odd half may lie beyond K
     for (int r = et; r < R; r += 128) ctl->meta[r] = args.rowinfo[row0 + r];
     if (et < C::kWords) {
-      const int n = R - et * 32;
+      const int n = kb_ok ? R - et * 32 : 0;
       ctl->pend[et] = n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
     }
-    ok = ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
+    ok = PAIR ? ptx::mbar_wait_cluster(&ctl->tfull[acc], aph, lim, abort)
+              : ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
     if (bar_any(1, 128, !ok || ctl->abort)) {
       if (!ok) {
         ctl->abort = 1;
@@ -534,7 +617,7 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
                             static_cast<uint32_t>(acc * C::kAccCols);
     uint64_t t_wait0 = 0;
-    while (true) {
+    while (kb_ok) {
       // 1. which pending rows may go now
       ready_rows(ctl, args, R, kb, gave_up);
       ptx::named_bar_sync(1, 128);
@@ -554,8 +637,8 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
         continue;
       }
       // 2. write the ready rows
-      if (args.bulk)
-        write_rows_bulk(ctl, args, t_lane, R, kb, quarter);
+      if (args.vec_rows)
+        write_rows_vec(ctl, args, t_lane, R, kb, quarter);
       else
         write_rows_scalar(ctl, args, t_lane, R, kb, quarter);
       ptx::named_bar_sync(1, 128);
@@ -578,24 +661,31 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ctl->tempty[acc]);
+    if (lane == 0) {
+      if (remote)
+        ptx::mbar_arrive_remote(ptx::mapa(&ctl->tempty[acc], 0));
+      else
+        ptx::mbar_arrive(&ctl->tempty[acc]);
+    }
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
 }
 
-template <int DT, int ROWS, int STAGES>
-__global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
+template <int DT, int ROWS, int STAGES, bool PAIR>
+__global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
     gmm_dx_kernel(const __grid_constant__ DyMaps dy_maps, const __grid_constant__ CUtensorMap tm_w,
                   const GemmArgs args) {
-  using C = Cfg<DT, ROWS, STAGES>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   auto* ctl = reinterpret_cast<Ctl<ROWS, STAGES>*>(smem + STAGES * C::kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
 
-  // Routing validation failed: the result is defined as zeros.
+  // Routing validation failed: the result is defined as zeros. (Both CTAs of
+  // a pair see the same status and leave before any cluster operation.)
   const uint32_t st = args.hdr->status;
   if (st == kStIndex || st == kStGroupSum || st == kStNotPerm) {
     const int64_t n = args.batch * args.K;
@@ -604,7 +694,7 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
       args.out[q] = 0.0f;
     return;
   }
-  const uint32_t total = args.hdr->n_row_blocks * static_cast<uint32_t>(args.k_blocks);
+  const uint32_t total = args.hdr->n_row_blocks * static_cast<uint32_t>(args.k_units);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -614,11 +704,11 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl->tfull[a], 1);
-      ptx::mbar_init(&ctl->tempty[a], C::kEpiWarps);
+      ptx::mbar_init(&ctl->tempty[a], C::kTEmpty);
     }
     for (int q = 0; q < kQueue; ++q) {
       ptx::mbar_init(&ctl->qfull[q], 1);
-      ptx::mbar_init(&ctl->qempty[q], C::kSplit ? 3 : 2);
+      ptx::mbar_init(&ctl->qempty[q], C::kQEmpty);
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -629,63 +719,99 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES>::kThreads, 1)
     ptx::tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, C::kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(&ctl->tmem_base, C::kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();  // the peer's barriers are initialised
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer<DT, ROWS, STAGES>(smem, ctl, &dy_maps, &tm_w, args, total);
+    if (lane == 0) producer<DT, ROWS, STAGES, PAIR>(smem, ctl, &dy_maps, &tm_w, args, total, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<DT, ROWS, STAGES>(smem, ctl, tmem_base, args);
+    if (lane == 0 && rank == 0) mma_issuer<DT, ROWS, STAGES, PAIR>(smem, ctl, tmem_base, args);
   } else if (warp < 2 + C::kEpiWarps) {
-    epilogue<DT, ROWS, STAGES>(ctl, tmem_base, args);
-  } else {
+    epilogue<DT, ROWS, STAGES, PAIR>(ctl, tmem_base, args, rank);
+  } else if constexpr (C::kSplit) {
     transformer<DT, ROWS, STAGES>(smem, ctl, args);
   }
 
   ptx::tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();  // no CTA leaves while its peer may still use it
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-template <int DT, int ROWS, int STAGES>
-cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& args, int grid,
+template <int DT, int ROWS, int STAGES, bool PAIR>
+cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& args, int max_ctas,
                      cudaStream_t stream) {
-  using C = Cfg<DT, ROWS, STAGES>;
-  constexpr int smem = smem_bytes<DT, ROWS, STAGES>();
-  auto kern = gmm_dx_kernel<DT, ROWS, STAGES>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR>;
+  constexpr int smem = smem_bytes<DT, ROWS, STAGES, PAIR>();
+  auto kern = gmm_dx_kernel<DT, ROWS, STAGES, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::kThreads, smem, stream>>>(tdy, tw, args);
-  return cudaGetLastError();
+  if constexpr (!PAIR) {
+    kern<<<max_ctas, C::kThreads, smem, stream>>>(tdy, tw, args);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * ((max_ctas + 1) / 2), 1, 1);
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    const int want = (max_ctas + 1) / 2;
+    cfg.gridDim = dim3(2 * (clusters < want ? clusters : want), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, tdy, tw, args);
+  }
 }
 
-// (dtype, variant) -> (rows per block, stages)
-#define PGG_VARIANTS(X)      \
-  X(PGG_BF16, 0, 256, 4)     \
-  X(PGG_BF16, 1, 32, 10)     \
-  X(PGG_F16, 0, 256, 4)      \
-  X(PGG_F16, 1, 32, 10)      \
-  X(PGG_F32, 0, 128, 3)      \
-  X(PGG_F32, 1, 32, 4)
+// (dtype, variant) -> (rows per block, stages, CTA pair)
+#define PGG_VARIANTS(X)          \
+  X(PGG_BF16, 0, 256, 6, true)   \
+  X(PGG_BF16, 1, 32, 10, false)  \
+  X(PGG_BF16, 2, 256, 4, false)  \
+  X(PGG_F16, 0, 256, 6, true)    \
+  X(PGG_F16, 1, 32, 10, false)   \
+  X(PGG_F16, 2, 256, 4, false)   \
+  X(PGG_F32, 0, 128, 3, false)   \
+  X(PGG_F32, 1, 32, 4, false)
 
 }  // namespace
 
-bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem) {
-#define PGG_CFG(DT, V, R, S)                          \
-  if (dtype == DT && variant == V) {                  \
-    *rows = R;                                        \
-    *stages = S;                                      \
-    *threads = Cfg<DT, R, S>::kThreads;               \
-    *smem = smem_bytes<DT, R, S>();                   \
-    return true;                                      \
+bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem,
+                   int* pair) {
+#define PGG_CFG(DT, V, R, S, P)                 \
+  if (dtype == DT && variant == V) {            \
+    *rows = R;                                  \
+    *stages = S;                                \
+    *threads = Cfg<DT, R, S, P>::kThreads;      \
+    *smem = smem_bytes<DT, R, S, P>();          \
+    *pair = P ? 1 : 0;                          \
+    return true;                                \
   }
   PGG_VARIANTS(PGG_CFG)
 #undef PGG_CFG
@@ -693,9 +819,9 @@ bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads,
 }
 
 cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy, const CUtensorMap& tw,
-                                const GemmArgs& args, int grid, cudaStream_t stream) {
-#define PGG_LAUNCH(DT, V, R, S) \
-  if (dtype == DT && variant == V) return launch_t<DT, R, S>(tdy, tw, args, grid, stream);
+                                const GemmArgs& args, int max_ctas, cudaStream_t stream) {
+#define PGG_LAUNCH(DT, V, R, S, P) \
+  if (dtype == DT && variant == V) return launch_t<DT, R, S, P>(tdy, tw, args, max_ctas, stream);
   PGG_VARIANTS(PGG_LAUNCH)
 #undef PGG_LAUNCH
   return cudaErrorInvalidValue;

@@ -19,9 +19,10 @@ namespace pgg {
 cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
                               void* workspace, int num_sms, cudaStream_t stream);
 cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy,
-                                const CUtensorMap& tw, const GemmArgs& args, int grid,
+                                const CUtensorMap& tw, const GemmArgs& args, int max_ctas,
                                 cudaStream_t stream);
-bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem);
+bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem,
+                   int* pair);
 
 namespace {
 
@@ -55,9 +56,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   std::memset(p, 0, sizeof(*p));
   p->dtype = dtype;
   int variant = g_force_variant.load();
-  if (variant != 0 && variant != 1) variant = (M / G < 64) ? 1 : 0;
+  if (variant < 0) variant = (M / G < 64) ? 1 : 0;
   p->variant = variant;
-  if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes))
+  if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes,
+                     &p->pair))
     return PGG_ERR_DTYPE;
   p->M = M;
   p->N = N;
@@ -72,7 +74,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   const int elems_per_row = kRowBytes / elem_size(dtype);
   p->nk = static_cast<int>((N + elems_per_row - 1) / elems_per_row);
   p->max_row_blocks = (M + p->rows_per_block - 1) / p->rows_per_block + G;
-  if (p->max_row_blocks * p->k_blocks > kInt32Max) return PGG_ERR_SHAPE;
+  p->k_units = p->pair ? (p->k_blocks + 1) / 2 : p->k_blocks;
+  p->band_units = p->pair ? (p->band_k_blocks + 1) / 2 : p->band_k_blocks;
+  if (p->max_row_blocks * p->k_units > kInt32Max) return PGG_ERR_SHAPE;
 
   Layout& L = p->layout;
   size_t a = 0;
@@ -218,13 +222,14 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   a.K = plan.K;
   a.batch = plan.batch;
   a.k_blocks = plan.k_blocks;
-  a.band_k_blocks = plan.band_k_blocks;
+  a.k_units = plan.k_units;
+  a.band_units = plan.band_units;
   a.nk = plan.nk;
   a.ticket_bias = g_ticket_bias.load();
-  a.bulk = (plan.K % 4 == 0) ? 1 : 0;
+  a.vec_rows = (plan.K % 4 == 0) ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
-  const int64_t max_tiles = plan.max_row_blocks * plan.k_blocks;
-  const int grid = static_cast<int>(max_tiles < di.num_sms ? max_tiles : di.num_sms);
+  const int64_t max_ctas = plan.max_row_blocks * plan.k_units * (plan.pair ? 2 : 1);
+  const int grid = static_cast<int>(max_ctas < di.num_sms ? max_ctas : di.num_sms);
   return launch_grouped_gemm(plan.dtype, plan.variant, tdy, tw, a, grid, stream) == cudaSuccess
              ? PGG_OK
              : PGG_ERR_CUDA;
@@ -267,6 +272,7 @@ int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   info->workspace_bytes = p.layout.total;
   info->threads = p.threads;
   info->smem_bytes = p.smem_bytes;
+  info->cta_pair = p.pair;
   return PGG_OK;
 }
 

@@ -17,14 +17,15 @@ constexpr int kKBlock = 128;
 // Bytes of one operand row inside a pipeline stage: one 128-byte swizzle atom
 // along the reduction dimension (64 half-precision or 32 fp32 elements).
 constexpr int kRowBytes = 128;
-// d_y is read through four tensor maps whose boxes are 32, 64, 128 and 256
-// rows high; each tile takes one copy with the smallest box that covers its
-// rows (the number of copies, not their size, limits the copy engine here).
-constexpr int kDyMaps = 4;
-constexpr int kDyMinRows = 32;
+// d_y is read through five tensor maps whose boxes are 16, 32, 64, 128 and
+// 256 rows high; each tile takes one copy per k step with the smallest box
+// that covers its rows (the number of copies, not their size, limits the copy
+// engine here).
+constexpr int kDyMaps = 5;
+constexpr int kDyMinRows = 16;
 
-struct alignas(64) DyMaps {
-  CUtensorMap box[kDyMaps];  // box[j]: 32 << j rows x one 128-byte row segment
+struct DyMaps {
+  CUtensorMap box[kDyMaps];  // box[j]: 16 << j rows x one 128-byte row segment
 };
 
 // Status codes written by the kernels (same values as pgg_status).
@@ -46,7 +47,8 @@ struct Layout {
 };
 
 struct Plan {
-  int variant;         // 0 wide row blocks, 1 narrow row blocks
+  int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single CTAs
+  int pair;            // 1: CTA-pair tiles of 256 k
   int dtype;           // pgg_dtype
   int rows_per_block;  // MMA N extent
   int stages;
@@ -54,6 +56,8 @@ struct Plan {
   int smem_bytes;
   int k_blocks;
   int band_k_blocks;
+  int k_units;     // k_blocks, or k-block pairs for CTA-pair tiles
+  int band_units;
   int64_t max_row_blocks;
   int64_t M, N, K, G, batch, topK;
   int row_idx_type;
@@ -76,11 +80,13 @@ struct GemmArgs {
   float* out;             // [batch, K]
   int64_t K;
   int64_t batch;
-  int32_t k_blocks;
-  int32_t band_k_blocks;
+  int32_t k_blocks;    // ceil(K / 128): ticket columns
+  int32_t k_units;     // k blocks per row block in the tile order (pairs: k-block pairs)
+  int32_t band_units;  // k units per band of the tile order
   int32_t nk;
   uint32_t ticket_bias;
-  int32_t bulk;  // 1: epilogue rows go through bulk copies / bulk reductions (K % 4 == 0)
+  int32_t vec_rows;  // 1: epilogue writes 512-byte row segments with v4 stores / reductions
+                     // (needs K % 4 == 0); 0: one 128-byte scalar store / reduction per warp
   uint64_t wait_limit_ns;
 };
 
