@@ -10,10 +10,11 @@
 // expert and 128 consecutive output columns k. The MMA is issued with the
 // weight slice as operand A (M = 128 rows of k) and the d_y rows as operand B
 // (N = rows, rounded up to 16), both K-major along n, so that the accumulator
-// in tensor memory holds lane = k, column = expanded row. The epilogue moves
-// each expanded row's 128 values of k into a shared-memory staging row and
-// writes the 512-byte segment of d_x with one vector store (the row's first
-// contribution) or one vector fp32 reduction performed at L2 (later ones).
+// in tensor memory holds lane = k, column = expanded row. The epilogue
+// transposes 4 x 4 blocks in registers so that each lane holds four
+// consecutive k of one row, and writes each row's 512-byte segment of d_x as
+// 128-byte vector stores (the row's first contribution) or vector fp32
+// reductions performed at L2 (later ones).
 //
 // Warp roles (one CTA per SM, persistent):
 //   warp 0       tile scheduler + TMA producer (one lane)
@@ -99,7 +100,12 @@ struct Cfg {
   static constexpr int kAccCols = ROWS < 32 ? 32 : ROWS;
   static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);  // allocation unit
   static constexpr int kWords = (ROWS + 31) / 32;
-  static constexpr int kEpiWarps = 4;
+  // Epilogue warp groups of four warps (one per tensor-memory lane quarter).
+  // Group g drains accumulator buffer g, so with two groups each tile's
+  // epilogue has two MMA tile-times to finish. The fp32 variant keeps one
+  // group (its extra warps split operands).
+  static constexpr int kEpiGroups = kSplit ? 1 : 2;
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kXformWarps = kSplit ? 4 : 0;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kXformWarps);
   static constexpr int kMmaM = PAIR ? 2 * kKBlock : kKBlock;
@@ -107,7 +113,7 @@ struct Cfg {
   // consumers of a tile-queue slot: MMA + epilogue (+ fp32 split), and in a
   // pair the peer's producer and epilogue as well
   static constexpr uint32_t kQEmpty = PAIR ? 4 : (kSplit ? 3 : 2);
-  static constexpr uint32_t kTEmpty = PAIR ? 2 * kEpiWarps : kEpiWarps;
+  static constexpr uint32_t kTEmpty = PAIR ? 8 : 4;  // one group's warps (of both CTAs)
   static_assert(ROWS % 32 == 0 && ROWS <= 256, "rows per block");
   static_assert(!PAIR || (!kSplit && ROWS % 64 == 0), "pairs: 16-bit inputs, rows % 64 == 0");
   static_assert(kTmemCols <= 512, "tmem columns");
@@ -121,13 +127,19 @@ __device__ __forceinline__ int mma_n(int R) {
   return n < C::kNAlign ? C::kNAlign : n;
 }
 
-// Epilogue staging for the vector path: rows x 128 fp32 (one 512-byte d_x row
-// segment per expanded row), two buffers of kChunk rows.
+// Rows per tensor-memory load in the epilogue.
 constexpr int kChunk = 16;
+
+// Per-tile state of one epilogue group.
+template <int ROWS>
+struct EpiState {
+  uint32_t pend[(ROWS + 31) / 32];  // rows still to be added
+  uint32_t rdy[(ROWS + 31) / 32];   // rows whose turn has come in this round
+  RowInfo meta[ROWS];
+};
 
 template <int ROWS, int STAGES>
 struct Ctl {
-  float stg[2][kChunk][kKBlock];
   uint64_t full[STAGES];   // TMA bytes landed (pairs: both CTAs' bytes, even CTA's barrier)
   uint64_t empty[STAGES];  // MMAs reading the stage completed
   uint64_t ready[STAGES];  // fp32 split done
@@ -139,9 +151,7 @@ struct Ctl {
   int4 q[kQueue];  // {expert (-1 = stop), first row, rows, k unit}
   uint32_t tmem_base;
   int abort;
-  uint32_t pend[(ROWS + 31) / 32];
-  uint32_t rdy[(ROWS + 31) / 32];
-  RowInfo meta[ROWS];
+  EpiState<ROWS> epi[2];  // one per epilogue group
 };
 
 template <int DT, int ROWS, int STAGES, bool PAIR>
@@ -215,6 +225,7 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
   int4 e = make_int4(-1, 0, 0, 0);
   if (leader) e = entry(atomicAdd(&args.hdr->sched_next, 1u));
   bool failed = false;
+  int stops = 0;
   while (!failed) {
     uint32_t t_next = total;
     if (leader) {
@@ -241,7 +252,11 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
       qs = 0;
       qph ^= 1u;
     }
-    if (e.x < 0) break;
+    if (e.x < 0) {
+      // one stop entry per epilogue group (each group reads every other entry)
+      if (leader && ++stops < C::kEpiGroups) continue;
+      break;
+    }
     const int nm = mma_n<C>(e.z);
     const int b_rows = PAIR ? nm / 2 : e.z;  // rows of d_y this CTA stages
     const int bj = dy_box<C::kBRows>(b_rows);
@@ -408,7 +423,7 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
   while (true) {
     bool ok = ptx::mbar_wait(&ctl->qfull[qs], qph, lim, abort);
     const int4 e = ctl->q[qs];
-    if (bar_any(2, 128, !ok || ctl->abort)) break;
+    if (bar_any(3, 128, !ok || ctl->abort)) break;
     if (tt == 0) ptx::mbar_arrive(&ctl->qempty[qs]);
     if (++qs == kQueue) {
       qs = 0;
@@ -419,7 +434,7 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
     bool stop = false;
     for (int ks = 0; ks < args.nk && !stop; ++ks) {
       ok = ptx::mbar_wait(&ctl->full[stage], phase, lim, abort);
-      if (bar_any(2, 128, !ok || ctl->abort)) {
+      if (bar_any(3, 128, !ok || ctl->abort)) {
         stop = true;
         break;
       }
@@ -442,7 +457,7 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
       for (int i = tt; i < C::kABytes / 16; i += 128) split(a, a_lo, i);
       for (int i = tt; i < n_b4; i += 128) split(b, b_lo, i);
       ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(2, 128);
+      ptx::named_bar_sync(3, 128);
       if (tt == 0) ptx::mbar_arrive(&ctl->ready[stage]);
       if (++stage == STAGES) {
         stage = 0;
@@ -455,18 +470,18 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
 
 // Rows of the tile whose ticket says they may be added now. Thread et looks
 // after rows et and et + 128; a warp ballot forms each 32-row mask word.
-template <int ROWS, int STAGES>
-__device__ __forceinline__ void ready_rows(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args, int R,
+template <int ROWS>
+__device__ __forceinline__ void ready_rows(EpiState<ROWS>* es, const GemmArgs& args, int R,
                                            uint32_t kb, bool gave_up) {
   constexpr int kWords = (ROWS + 31) / 32;
-  const int et = threadIdx.x - 64, ew = et >> 5, lane = threadIdx.x & 31;
+  const int et = (threadIdx.x - 64) & 127, ew = et >> 5, lane = threadIdx.x & 31;
   const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
   bool go[2] = {false, false};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = et + 128 * h;
-    if (r < R && ((ctl->pend[r >> 5] >> (r & 31)) & 1u)) {
-      const RowInfo m = ctl->meta[r];
+    if (r < R && ((es->pend[r >> 5] >> (r & 31)) & 1u)) {
+      const RowInfo m = es->meta[r];
       go[h] = m.rank == 0 || gave_up;
       if (!go[h]) {
         const uint32_t have =
@@ -478,45 +493,64 @@ __device__ __forceinline__ void ready_rows(Ctl<ROWS, STAGES>* ctl, const GemmArg
   const uint32_t w0 = __ballot_sync(0xffffffffu, go[0]);
   const uint32_t w1 = __ballot_sync(0xffffffffu, go[1]);
   if (lane == 0) {
-    if (ew < kWords) ctl->rdy[ew] = w0;
-    if (ew + 4 < kWords) ctl->rdy[ew + 4] = w1;
+    if (ew < kWords) es->rdy[ew] = w0;
+    if (ew + 4 < kWords) es->rdy[ew + 4] = w1;
   }
 }
 
-// Writes the ready rows: each warp moves its 32 k values of kChunk rows from
-// tensor memory into staging rows [row][128 k] in shared memory; then each
-// warp sends whole 512-byte row segments, one st.global.v4 (rank 0) or
-// red.global.add.v4.f32 (rank > 0) warp instruction per row. The writes stay
-// on the load/store path: handing them to the tensor-memory-access unit as
-// bulk copies queued them in front of the main loop's operand loads and
-// starved the tensor cores. Needs K % 4 == 0 (16-byte aligned segments).
-template <int ROWS, int STAGES>
-__device__ __forceinline__ void write_rows_vec(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
+// Writes the ready rows without leaving registers. A tensor-memory load gives
+// lane l of warp q the value of k = 32q + l for kChunk rows. Two xor-shuffle
+// stages transpose every 4 x 4 block (lane bits 0-1 <-> row bits 0-1), after
+// which lane l holds k = 32q + 4(l/4) .. +3 of row 4s + (l % 4). The eight lanes
+// sharing a row then cover its 128 contiguous bytes of this warp's quarter, and
+// one v4 store (rank 0) or v4 fp32 reduction at L2 (rank > 0) per lane writes
+// four rows per warp instruction. Needs K % 4 == 0.
+template <int ROWS>
+__device__ __forceinline__ void write_rows_vec(const EpiState<ROWS>* es, const GemmArgs& args,
                                                uint32_t t_lane, int R, uint32_t kb, int quarter) {
-  const int et = threadIdx.x - 64, ew = et >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int64_t K = args.K;
-  const int64_t k0 = static_cast<int64_t>(kb) * kKBlock;
-  const int n4 = static_cast<int>((K - k0 < kKBlock ? K - k0 : kKBlock) / 4);
+  const int64_t k = static_cast<int64_t>(kb) * kKBlock + 32 * quarter + 4 * (lane >> 2);
+  const bool k_ok = k < K;  // K % 4 == 0: a lane's four k are all in or all out
+  const bool up = (lane & 2) != 0, odd = (lane & 1) != 0;
   const int nchunks = (R + kChunk - 1) / kChunk;
-  constexpr int kRowsPerWarp = kChunk / 4;
   for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
+    const int r_lo = c * kChunk;
+    const uint32_t word = es->rdy[r_lo >> 5] >> (r_lo & 31);  // bits of this chunk's rows
+    if ((word & ((1u << kChunk) - 1u)) == 0u) continue;        // warp-uniform
     uint32_t v[kChunk];
-    ptx::tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(c * kChunk), v);
+    ptx::tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(r_lo), v);
     ptx::tmem_ld_wait();
-    // (chunk c - 2 used this buffer; every warp finished reading it before the
-    // barrier of chunk c - 1)
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) ctl->stg[buf][j][32 * quarter + lane] = __uint_as_float(v[j]);
-    ptx::named_bar_sync(1, 128);
-#pragma unroll
-    for (int jj = 0; jj < kRowsPerWarp; ++jj) {
-      const int j = ew * kRowsPerWarp + jj;
-      const int r = c * kChunk + j;
-      if (r < R && ((ctl->rdy[r >> 5] >> (r & 31)) & 1u) && lane < n4) {
-        const RowInfo m = ctl->meta[r];
-        const float4 x = *reinterpret_cast<const float4*>(&ctl->stg[buf][j][4 * lane]);
-        float* dst = args.out + static_cast<int64_t>(m.token) * K + k0 + 4 * lane;
+    for (int g = 0; g < kChunk / 4; ++g) {
+      uint32_t r0 = v[4 * g], r1 = v[4 * g + 1], r2 = v[4 * g + 2], r3 = v[4 * g + 3];
+      // exchange across lane bit 1 <-> row bit 1
+      uint32_t t0 = __shfl_xor_sync(0xffffffffu, up ? r0 : r2, 2);
+      uint32_t t1 = __shfl_xor_sync(0xffffffffu, up ? r1 : r3, 2);
+      if (up) {
+        r0 = t0;
+        r1 = t1;
+      } else {
+        r2 = t0;
+        r3 = t1;
+      }
+      // exchange across lane bit 0 <-> row bit 0
+      t0 = __shfl_xor_sync(0xffffffffu, odd ? r0 : r1, 1);
+      t1 = __shfl_xor_sync(0xffffffffu, odd ? r2 : r3, 1);
+      if (odd) {
+        r0 = t0;
+        r2 = t1;
+      } else {
+        r1 = t0;
+        r3 = t1;
+      }
+      const int j = 4 * g + (lane & 3);
+      const int r = r_lo + j;
+      if (r < R && ((word >> j) & 1u) && k_ok) {
+        const RowInfo m = es->meta[r];
+        float* dst = args.out + static_cast<int64_t>(m.token) * K + k;
+        const float4 x = make_float4(__uint_as_float(r0), __uint_as_float(r1), __uint_as_float(r2),
+                                     __uint_as_float(r3));
         if (m.rank == 0)
           *reinterpret_cast<float4*>(dst) = x;
         else
@@ -528,8 +562,8 @@ __device__ __forceinline__ void write_rows_vec(Ctl<ROWS, STAGES>* ctl, const Gem
 
 // Scalar path for K % 4 != 0: lane = k, one 128-byte store or reduction per
 // row and warp.
-template <int ROWS, int STAGES>
-__device__ __forceinline__ void write_rows_scalar(Ctl<ROWS, STAGES>* ctl, const GemmArgs& args,
+template <int ROWS>
+__device__ __forceinline__ void write_rows_scalar(const EpiState<ROWS>* es, const GemmArgs& args,
                                                   uint32_t t_lane, int R, uint32_t kb,
                                                   int quarter) {
   const int lane = threadIdx.x & 31;
@@ -541,12 +575,12 @@ __device__ __forceinline__ void write_rows_scalar(Ctl<ROWS, STAGES>* ctl, const 
     uint32_t v[32];
     ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c * 32), v);
     ptx::tmem_ld_wait();
-    const uint32_t word = ctl->rdy[c];
+    const uint32_t word = es->rdy[c];
     if (k_ok && word) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (word & (1u << j)) {
-          const RowInfo m = ctl->meta[c * 32 + j];
+          const RowInfo m = es->meta[c * 32 + j];
           float* p = args.out + static_cast<int64_t>(m.token) * K + k;
           const float x = __uint_as_float(v[j]);
           if (m.rank == 0)
@@ -565,19 +599,26 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
   using C = Cfg<DT, ROWS, STAGES, PAIR>;
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
-  const int et = threadIdx.x - 64;  // 0..127
+  const int et = (threadIdx.x - 64) & 127;  // thread within the group
+  const int grp = (threadIdx.x - 64) >> 7;   // epilogue group: drains accumulator buffer grp
+  const uint32_t bar = 1u + static_cast<uint32_t>(grp);
+  EpiState<ROWS>* es = &ctl->epi[grp];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;     // tensor-memory lanes this warp may read
   const uint32_t kbs = static_cast<uint32_t>(args.k_blocks);
   const bool remote = PAIR && rank != 0;  // queue and accumulator barriers live in the even CTA
-  int qs = 0, acc = 0;
-  uint32_t qph = 0, aph = 0;
   bool gave_up = false;
-  while (true) {
+  // The group takes every kEpiGroups-th tile of the queue, starting at its index.
+  for (uint32_t n = 0;; ++n) {
+    const uint32_t i = n * C::kEpiGroups + static_cast<uint32_t>(grp);
+    const int qs = static_cast<int>(i % kQueue);
+    const uint32_t qph = (i / kQueue) & 1u;
+    const int acc = static_cast<int>(i & 1u);
+    const uint32_t aph = (i >> 1) & 1u;
     bool ok = remote ? ptx::mbar_wait_cluster(&ctl->qfull[qs], qph, lim, abort)
                      : ptx::mbar_wait(&ctl->qfull[qs], qph, lim, abort);
     const int4 e = ctl->q[qs];
-    if (bar_any(1, 128, !ok || ctl->abort)) {
+    if (bar_any(bar, 128, !ok || ctl->abort)) {
       if (!ok) {
         ctl->abort = 1;
         if (et == 0) raise_status(args.hdr, kStTimeout, 4);
@@ -590,22 +631,18 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
       else
         ptx::mbar_arrive(&ctl->qempty[qs]);
     }
-    if (++qs == kQueue) {
-      qs = 0;
-      qph ^= 1u;
-    }
     if (e.x < 0) break;
     const int R = e.z, row0 = e.y;
     const uint32_t kb = PAIR ? 2u * static_cast<uint32_t>(e.w) + rank : static_cast<uint32_t>(e.w);
     const bool kb_ok = kb < kbs;  // a pair's odd half may lie beyond K
-    for (int r = et; r < R; r += 128) ctl->meta[r] = args.rowinfo[row0 + r];
+    for (int r = et; r < R; r += 128) es->meta[r] = args.rowinfo[row0 + r];
     if (et < C::kWords) {
-      const int n = kb_ok ? R - et * 32 : 0;
-      ctl->pend[et] = n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
+      const int nr = kb_ok ? R - et * 32 : 0;
+      es->pend[et] = nr >= 32 ? 0xFFFFFFFFu : (nr <= 0 ? 0u : ((1u << nr) - 1u));
     }
     ok = PAIR ? ptx::mbar_wait_cluster(&ctl->tfull[acc], aph, lim, abort)
               : ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
-    if (bar_any(1, 128, !ok || ctl->abort)) {
+    if (bar_any(bar, 128, !ok || ctl->abort)) {
       if (!ok) {
         ctl->abort = 1;
         if (et == 0) raise_status(args.hdr, kStTimeout, 5);
@@ -619,16 +656,16 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     uint64_t t_wait0 = 0;
     while (kb_ok) {
       // 1. which pending rows may go now
-      ready_rows(ctl, args, R, kb, gave_up);
-      ptx::named_bar_sync(1, 128);
+      ready_rows(es, args, R, kb, gave_up);
+      ptx::named_bar_sync(bar, 128);
       bool any = false;
 #pragma unroll
-      for (int w = 0; w < C::kWords; ++w) any |= ctl->rdy[w] != 0u;
+      for (int w = 0; w < C::kWords; ++w) any |= es->rdy[w] != 0u;
       if (!any) {
         if (t_wait0 == 0) t_wait0 = ptx::globaltimer();
         const bool expired = (ptx::globaltimer() - t_wait0 > lim) ||
                              *reinterpret_cast<volatile uint32_t*>(&args.hdr->status) == kStTimeout;
-        if (bar_any(1, 128, expired)) {
+        if (bar_any(bar, 128, expired)) {
           gave_up = true;
           if (et == 0) raise_status(args.hdr, kStTimeout, 1);
         } else {
@@ -638,25 +675,25 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
       }
       // 2. write the ready rows
       if (args.vec_rows)
-        write_rows_vec(ctl, args, t_lane, R, kb, quarter);
+        write_rows_vec(es, args, t_lane, R, kb, quarter);
       else
-        write_rows_scalar(ctl, args, t_lane, R, kb, quarter);
-      ptx::named_bar_sync(1, 128);
+        write_rows_scalar(es, args, t_lane, R, kb, quarter);
+      ptx::named_bar_sync(bar, 128);
       // 3. publish: the rows' additions happen-before the ticket bumps
       bool mine = false;
-      for (int r = et; r < R; r += 128) mine |= (ctl->rdy[r >> 5] >> (r & 31)) & 1u;
+      for (int r = et; r < R; r += 128) mine |= (es->rdy[r >> 5] >> (r & 31)) & 1u;
       if (mine) {
         ptx::fence_acq_rel_gpu();
         for (int r = et; r < R; r += 128)
-          if ((ctl->rdy[r >> 5] >> (r & 31)) & 1u)
-            ptx::red_add_u32_gpu(args.tickets + static_cast<int64_t>(ctl->meta[r].token) * kbs + kb,
+          if ((es->rdy[r >> 5] >> (r & 31)) & 1u)
+            ptx::red_add_u32_gpu(args.tickets + static_cast<int64_t>(es->meta[r].token) * kbs + kb,
                                  1u);
       }
-      if (et < C::kWords) ctl->pend[et] &= ~ctl->rdy[et];
-      ptx::named_bar_sync(1, 128);
+      if (et < C::kWords) es->pend[et] &= ~es->rdy[et];
+      ptx::named_bar_sync(bar, 128);
       bool left = false;
 #pragma unroll
-      for (int w = 0; w < C::kWords; ++w) left |= ctl->pend[w] != 0u;
+      for (int w = 0; w < C::kWords; ++w) left |= es->pend[w] != 0u;
       if (!left) break;
     }
     ptx::tc_fence_before_sync();
@@ -667,8 +704,6 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
       else
         ptx::mbar_arrive(&ctl->tempty[acc]);
     }
-    acc ^= 1;
-    if (acc == 0) aph ^= 1u;
   }
 }
 
