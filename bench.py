@@ -36,10 +36,17 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "uniform-bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace bytes"
-KERNEL_SOURCES = ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu",
-                  "permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh",
-                  "permute_grouped_gemm_gb300/csrc/pgg_internal.h",
-                  "permute_grouped_gemm_gb300/csrc/pgg_api.cu"]
+_COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh",
+           "permute_grouped_gemm_gb300/csrc/pgg_internal.h",
+           "permute_grouped_gemm_gb300/csrc/pgg_api.cu"]
+# grouped-GEMM kernel -> the sources its ncu counters depend on
+KERNEL_SOURCES = {
+    "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", *_COMMON],
+    "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
+}
+SIMT_VARIANT = 3
+FP32_LANES_PER_SM = 128    # FP32 fused multiply-add lanes per SM
+NOMINAL_SM_MHZ = 2070.0    # maximum SM clock of the part
 
 
 def parse():
@@ -63,9 +70,9 @@ def dist_info():
     return rank, world, local
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = "gmm_dx_kernel") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -81,10 +88,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per grouped-GEMM launch from the committed ncu summary, if it
     was taken on the current kernel source (matching hash), else None."""
-    path = os.path.join(ROOT, "profiles", f"gmm_dx_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -95,7 +102,7 @@ def recorded_traffic(workload: str):
         for key in ("kernel_source_hash", "dram_bytes_per_launch"):
             if line.startswith(key + ":"):
                 vals[key] = line.split(":", 1)[1].strip().split()[0]
-    if vals.get("kernel_source_hash") != kernel_hash():
+    if vals.get("kernel_source_hash") != kernel_hash(kernel):
         return None
     try:
         return int(float(vals["dram_bytes_per_launch"]))
@@ -344,7 +351,16 @@ def run_ours(args):
     tc_key = "bf16_tflops_sustained" if capped and "bf16_tflops_sustained" in peaks else "bf16_tflops"
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    if t_tc >= t_hbm:
+    simt = plan["variant"] == SIMT_VARIANT
+    kernel = "gmm_dx_simt_kernel" if simt else "gmm_dx_kernel"
+    if simt:
+        # FP32 pipes: SMs x FP32 lanes x 2 flops x the maximum SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or NOMINAL_SM_MHZ
+        bound, achieved = "alu", flops / (mean_gemm * 1e-3) / 1e12
+        peak, unit = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, "TFLOP/s"
+        peak_src = f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {mhz:.0f} MHz"
+    elif t_tc >= t_hbm:
         bound, achieved = "tensor", flops / (mean_gemm * 1e-3) / 1e12
         peak, unit = peaks[tc_key], "TFLOP/s"
         peak_src = f"{peak_src} {tc_key}"
@@ -355,7 +371,7 @@ def run_ours(args):
         bound, achieved = "hbm", nbytes / (mean_gemm * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
         peak_src = f"{peak_src} hbm_gbs"
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(kernel, w.name)
 
     e2e = None
     if not args.no_e2e:
@@ -375,8 +391,8 @@ def run_ours(args):
         "phases_ms": {"route_prep": statistics.mean(prep_ms), "grouped_gemm": mean_gemm},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src.startswith('measured') else 'profiling recipe fallback'})",
-                     "kernel": "gmm_dx_kernel", "algorithmic_flops": flops,
+                     "peak_source": peak_src if simt else f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src.startswith('measured') else 'profiling recipe fallback'})",
+                     "kernel": kernel, "algorithmic_flops": flops,
                      "algorithmic_bytes": nbytes},
         "clocks": clocks,
         "gpu_launches": 4 * args.steps,

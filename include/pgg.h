@@ -41,10 +41,16 @@
  *     the workspace: 0 means success, otherwise one of PGG_ERR_INDEX ..
  *     PGG_ERR_TIMEOUT. Read it after the stream has finished. When routing
  *     validation fails, `out` is zero-filled instead of computed.
- *   - Alignment (a restriction of this library, from the tensor-memory-access
- *     unit): gradY and weight must be 16-byte aligned and N * sizeof(dtype)
- *     must be a multiple of 16 bytes; workspace must be 256-byte aligned; out
- *     must be 16-byte aligned. Otherwise PGG_ERR_ALIGN.
+ *   - Alignment: gradY and weight must be aligned to their element size,
+ *     out to 4 bytes, expandedRowIdx and groupList to 8 bytes, and the
+ *     workspace to 256 bytes; otherwise PGG_ERR_ALIGN. Any N and K are
+ *     accepted. When N * sizeof(dtype) is a multiple of 16 bytes and gradY
+ *     and weight are 16-byte aligned, the grouped GEMM runs on the tensor
+ *     cores (operands streamed by the tensor-memory-access unit, which needs
+ *     both); otherwise it runs on the FP32 pipes (plan variant 3), with the
+ *     same ordered scatter-add and the same determinism. For the same call
+ *     the two paths may differ in the last bits of the GEMM sums, never
+ *     from run to run.
  */
 #ifndef PGG_H
 #define PGG_H
@@ -145,7 +151,10 @@ int pgg_dx_grouped_gemm(const void* gradY, const void* weight, const int64_t* ex
 /* How pgg_dx_execute will run a problem of these sizes (host only, no CUDA call). */
 typedef struct {
   int32_t variant;          /* 0 = wide row blocks on CTA pairs (tensor-bound), 1 = narrow row
-                               blocks (weight streaming), 2 = wide row blocks on single CTAs */
+                               blocks (weight streaming), 2 = wide row blocks on single CTAs,
+                               3 = FP32-pipe kernel (rows of N * sizeof(dtype) bytes that are
+                               not a multiple of 16); pgg_dx_execute also takes variant 3 when
+                               gradY or weight is not 16-byte aligned */
   int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent */
   int32_t k_per_block;      /* output columns per CTA and tile (128; a CTA pair covers 256) */
   int32_t stages;           /* shared-memory pipeline depth */
@@ -171,8 +180,9 @@ const char* pgg_status_string(int status);
  * pgg_debug_set_ticket_bias: added to the ticket count each ordered
  *   scatter-add waits for; a positive bias makes every wait of a row with
  *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
- * pgg_debug_force_variant: -1 = automatic (default), 0, 1 or 2 = force the
- *   variant reported by pgg_dx_plan (2 exists for the 16-bit dtypes only).
+ * pgg_debug_force_variant: -1 = automatic (default), 0, 1, 2 or 3 = force the
+ *   variant reported by pgg_dx_plan (2 exists for the 16-bit dtypes only;
+ *   rows that are not a multiple of 16 bytes always take variant 3).
  * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
  *   automatic). The result does not depend on it, bit for bit: only the time
  *   order of the tiles changes, never the order of the additions.

@@ -23,6 +23,9 @@ cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy,
                                 cudaStream_t stream);
 bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem,
                    int* pair);
+void simt_config(int* rows, int* stages, int* threads, int* smem);
+cudaError_t launch_simt(int dtype, const SimtArgs& a, int64_t max_tiles, int num_sms,
+                        cudaStream_t stream);
 
 namespace {
 
@@ -33,6 +36,7 @@ std::atomic<int> g_force_variant{-1};
 std::atomic<int> g_band_k_blocks{0};
 
 constexpr int64_t kInt32Max = 2147483647;
+constexpr int kVariantSimt = 3;  // FP32-pipe kernel (gmm_dx_simt.cu)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -47,9 +51,12 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   if (M > kInt32Max || N > kInt32Max || K > kInt32Max || G > kInt32Max) return PGG_ERR_SHAPE;
   if (L != M) return PGG_ERR_SHAPE;
   if (batch > M || topK > M || batch * topK != M) return PGG_ERR_SHAPE;
-  if ((N * elem_size(dtype)) % 16 != 0) return PGG_ERR_ALIGN;
   return PGG_OK;
 }
+
+// Rows of d_y and weight that the tensor-memory-access unit can stream: their
+// byte length must be a multiple of 16.
+bool rows_streamable(int64_t N, int dtype) { return (N * elem_size(dtype)) % 16 == 0; }
 
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
               int rowIdxType, int dtype, Plan* p) {
@@ -57,10 +64,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   p->dtype = dtype;
   int variant = g_force_variant.load();
   if (variant < 0) variant = (M / G < 64) ? 1 : 0;
+  if (!rows_streamable(N, dtype)) variant = kVariantSimt;
   p->variant = variant;
-  if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes,
-                     &p->pair))
+  if (variant == kVariantSimt) {
+    simt_config(&p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes);
+  } else if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads,
+                            &p->smem_bytes, &p->pair)) {
     return PGG_ERR_DTYPE;
+  }
   p->M = M;
   p->N = N;
   p->K = K;
@@ -190,7 +201,8 @@ int prepare(const void* gradY, const void* weight, const int64_t* idx, const int
   rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, plan);
   if (rc != PGG_OK) return rc;
   if (!aligned(ws, 256) || !aligned(idx, 8) || !aligned(gl, 8)) return PGG_ERR_ALIGN;
-  if (need_values && (!aligned(gradY, 16) || !aligned(weight, 16) || !aligned(out, 16)))
+  const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
+  if (need_values && (!aligned(gradY, es) || !aligned(weight, es) || !aligned(out, 4)))
     return PGG_ERR_ALIGN;
   if (ws_bytes < plan->layout.total) return PGG_ERR_WORKSPACE;
   return PGG_OK;
@@ -204,10 +216,38 @@ int run_route_prep(const Plan& plan, const int64_t* idx, const int64_t* gl, void
                                                                                    : PGG_ERR_CUDA;
 }
 
+// The FP32-pipe kernel: any row length and element-aligned pointers. It runs
+// on the row blocks the routing step built, whatever their height.
+int run_simt(const Plan& plan, const void* gradY, const void* weight, void* ws, float* out,
+             const DeviceInfo& di, cudaStream_t stream) {
+  char* w = static_cast<char*>(ws);
+  SimtArgs a;
+  a.dy = gradY;
+  a.w = weight;
+  a.rblist = reinterpret_cast<const int4*>(w + plan.layout.rblist);
+  a.rowinfo = reinterpret_cast<const RowInfo*>(w + plan.layout.rowinfo);
+  a.tickets = reinterpret_cast<uint32_t*>(w + plan.layout.tickets);
+  a.hdr = reinterpret_cast<WsHeader*>(w + plan.layout.hdr);
+  a.out = out;
+  a.N = plan.N;
+  a.K = plan.K;
+  a.batch = plan.batch;
+  a.k_blocks = plan.k_blocks;
+  a.ticket_bias = g_ticket_bias.load();
+  a.vec_out = (plan.K % 4 == 0 && aligned(out, 16)) ? 1 : 0;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  return launch_simt(plan.dtype, a, plan.max_row_blocks * plan.k_blocks, di.num_sms, stream) ==
+                 cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
+
 int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, void* ws, float* out,
                      cudaStream_t stream) {
   DeviceInfo di;
   if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  if (plan.variant == kVariantSimt || !aligned(gradY, 16) || !aligned(weight, 16))
+    return run_simt(plan, gradY, weight, ws, out, di, stream);
   DyMaps tdy;
   CUtensorMap tw;
   int rc = encode_maps(plan, gradY, weight, &tdy, &tw);
@@ -226,7 +266,7 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   a.band_units = plan.band_units;
   a.nk = plan.nk;
   a.ticket_bias = g_ticket_bias.load();
-  a.vec_rows = (plan.K % 4 == 0) ? 1 : 0;
+  a.vec_rows = (plan.K % 4 == 0 && aligned(out, 16)) ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   const int64_t max_ctas = plan.max_row_blocks * plan.k_units * (plan.pair ? 2 : 1);
   const int grid = static_cast<int>(max_ctas < di.num_sms ? max_ctas : di.num_sms);

@@ -47,7 +47,8 @@ struct Layout {
 };
 
 struct Plan {
-  int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single CTAs
+  int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single
+                       // CTAs, 3 FP32-pipe kernel for rows the tensor-memory-access unit cannot stream
   int pair;            // 1: CTA-pair tiles of 256 k
   int dtype;           // pgg_dtype
   int rows_per_block;  // MMA N extent
@@ -87,6 +88,26 @@ struct GemmArgs {
   uint32_t ticket_bias;
   int32_t vec_rows;  // 1: epilogue writes 512-byte row segments with v4 stores / reductions
                      // (needs K % 4 == 0); 0: one 128-byte scalar store / reduction per warp
+  uint64_t wait_limit_ns;
+};
+
+// Arguments of the FP32-pipe kernel used when the operands cannot be streamed
+// by the tensor-memory-access unit (row bytes not a multiple of 16, or a
+// pointer not 16-byte aligned).
+struct SimtArgs {
+  const void* dy;         // [M, N] dtype
+  const void* w;          // [G, K, N] dtype
+  const int4* rblist;     // {expert, first row, rows, 0} per row block (any row count)
+  const RowInfo* rowinfo; // [M]
+  uint32_t* tickets;      // [batch * k_blocks]
+  WsHeader* hdr;
+  float* out;             // [batch, K]
+  int64_t N;
+  int64_t K;
+  int64_t batch;
+  int32_t k_blocks;
+  uint32_t ticket_bias;
+  int32_t vec_out;  // 1: K % 4 == 0 and out 16-byte aligned (16-byte stores / reductions)
   uint64_t wait_limit_ns;
 };
 

@@ -70,8 +70,6 @@ def test_host_errors(lib):
     assert code_of(batch=0) == "PGG_ERR_ATTR"
     assert code_of(rowIdxType=2) == "PGG_ERR_ATTR"
     assert code_of(dtype=3) == "PGG_ERR_DTYPE"
-    assert code_of(N=2047) == "PGG_ERR_ALIGN"             # row stride not 16-byte multiple
-    assert code_of(N=6, dtype=pgg.PGG_F32) == "PGG_ERR_ALIGN"
     assert code_of(M=2**31, L=2**31, batch=2**28) == "PGG_ERR_SHAPE"
     assert code_of(K=0) == "PGG_ERR_SHAPE"
     assert code_of(G=0) == "PGG_ERR_SHAPE"
@@ -88,8 +86,15 @@ def test_execute_rejects_before_any_cuda_call(lib):
     rc = pgg.pgg_dx_execute(fake, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
                             a["batch"], a["topK"], 0, pgg.PGG_BF16, fake, need - 1, fake, None)
     assert pgg.STATUS[rc] == "PGG_ERR_WORKSPACE"
-    rc = pgg.pgg_dx_execute(fake + 8, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+    # gradY and weight need element alignment, out 4 bytes, the workspace 256
+    rc = pgg.pgg_dx_execute(fake + 1, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
                             a["batch"], a["topK"], 0, pgg.PGG_BF16, fake, need, fake, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_ALIGN"
+    rc = pgg.pgg_dx_execute(fake, fake + 2, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+                            a["batch"], a["topK"], 0, pgg.PGG_F32, fake, need, fake, None)
+    assert pgg.STATUS[rc] == "PGG_ERR_ALIGN"
+    rc = pgg.pgg_dx_execute(fake, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
+                            a["batch"], a["topK"], 0, pgg.PGG_BF16, fake, need, fake + 2, None)
     assert pgg.STATUS[rc] == "PGG_ERR_ALIGN"
     rc = pgg.pgg_dx_execute(fake, fake, fake, fake, a["M"], a["N"], a["K"], a["G"], a["L"],
                             a["batch"], a["topK"], 0, pgg.PGG_BF16, fake + 64, need, fake, None)
@@ -118,3 +123,18 @@ def test_plan_variants(lib):
 def test_status_strings(lib):
     for code, name in pgg.STATUS.items():
         assert pgg.pgg_status_string(code) != "unknown status", name
+
+
+def test_rows_the_tma_cannot_stream_take_the_fp32_pipe_kernel(lib):
+    # row bytes N * sizeof(dtype) not a multiple of 16 (the page's N = 1 and
+    # N = 286 white-box cases) plan the FP32-pipe kernel instead of an error
+    for n, dt in ((1, pgg.PGG_BF16), (286, pgg.PGG_BF16), (2047, pgg.PGG_F16), (6, pgg.PGG_F32),
+                  (1, pgg.PGG_F32)):
+        p = pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)
+        assert p["variant"] == 3 and p["rows_per_block"] == 64 and p["threads"] == 128, (n, dt)
+        assert p["cta_pair"] == 0 and p["smem_bytes"] <= 48 * 1024
+    for n, dt in ((8, pgg.PGG_BF16), (4, pgg.PGG_F32), (280, pgg.PGG_F16)):
+        assert pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)["variant"] != 3, (n, dt)
+    # the workspace stays small at the pages' scale
+    assert ws(N=2047) <= 16 * 2**20
+    assert ws(N=2047) < LARGE["M"] * LARGE["K"] // 64

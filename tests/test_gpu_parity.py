@@ -61,16 +61,19 @@ def check(inp, tokens=None, what=""):
     return out
 
 
-# The page's white-box list (section 4.2.1), shapes whose row stride the
-# tensor-memory-access unit accepts. N=1 and N=286 are covered by the
-# alignment test below.
+# The page's white-box list (section 4.2.1). N = 1 and the tail case's
+# N = 286 have rows whose byte length is not a multiple of 16 and run on the
+# FP32-pipe kernel; "tail_k178_n280" keeps a ragged tail on the tensor cores.
 WHITE_BOX = {
     "one_token_one_expert": dict(batch=1, K=128, N=256, top_k=1, G=1),
     "one_token_multi_expert": dict(batch=1, K=128, N=256, top_k=3, G=3),
     "multi_token_one_expert": dict(batch=128, K=128, N=256, top_k=1, G=1),
     "multi_token_multi_expert": dict(batch=128, K=128, N=256, top_k=3, G=10),
     "empty_expert": dict(batch=10, K=128, N=256, top_k=2, G=4, empty=(1,)),
+    "tail_k178_n286": dict(batch=10, K=178, N=286, top_k=3, G=4),
     "tail_k178_n280": dict(batch=10, K=178, N=280, top_k=3, G=4),
+    "m_is_1": dict(batch=1, K=128, N=256, top_k=1, G=1),
+    "n_is_1": dict(batch=128, K=128, N=1, top_k=3, G=4),
     "k_is_1": dict(batch=128, K=1, N=256, top_k=3, G=4),
 }
 
@@ -95,7 +98,7 @@ def test_large_m_white_box(dtype):
     check(inp, tokens=toks, what="large M")
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 def test_multi_tile_ragged(dtype, variant):
     if dtype == "fp32" and variant == 2:
@@ -116,7 +119,7 @@ def test_multi_tile_ragged(dtype, variant):
 def test_same_expert_twice_for_a_token(dtype):
     # degenerate routing: rows of one token inside one tile must still be
     # added in order (no deadlock, correct sum)
-    for variant in ((0, 1, 2) if dtype != "fp32" else (0, 1)):
+    for variant in ((0, 1, 2, 3) if dtype != "fp32" else (0, 1, 3)):
         pgg.pgg_debug_force_variant(variant)
         try:
             inp = make_case(batch=200, top_k=4, G=3, K=384, N=128, dtype=dtype,
@@ -126,8 +129,9 @@ def test_same_expert_twice_for_a_token(dtype):
             pgg.pgg_debug_force_variant(-1)
 
 
-def test_bitwise_repeatable():
-    inp = make_case(batch=2048, top_k=8, G=16, K=512, N=256, dtype="bf16", seed=7,
+@pytest.mark.parametrize("n", [256, 250])
+def test_bitwise_repeatable(n):
+    inp = make_case(batch=2048, top_k=8, G=16, K=512, N=n, dtype="bf16", seed=7,
                     device="cuda")
     first, ws = run(inp)
     for _ in range(4):
@@ -157,7 +161,7 @@ def test_variants_agree():
     ref = ref_rows(inp)
     outs = []
     try:
-        for variant in (0, 1, 2):
+        for variant in (0, 1, 2, 3):
             pgg.pgg_debug_force_variant(variant)
             out, _ = run(inp)
             outs.append(out)
@@ -166,8 +170,9 @@ def test_variants_agree():
         pgg.pgg_debug_force_variant(-1)
 
 
-def test_gather_and_scatter_forms_agree_bitwise():
-    inp0 = make_case(batch=500, top_k=6, G=12, K=256, N=192, dtype="fp16", seed=8,
+@pytest.mark.parametrize("n", [192, 190])
+def test_gather_and_scatter_forms_agree_bitwise(n):
+    inp0 = make_case(batch=500, top_k=6, G=12, K=256, N=n, dtype="fp16", seed=8,
                      device="cuda")
     inp1 = with_row_idx_type(inp0, 1)
     a, _ = run(inp0)
@@ -175,8 +180,9 @@ def test_gather_and_scatter_forms_agree_bitwise():
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-def test_device_detected_errors_zero_the_output():
-    base = make_case(batch=64, top_k=2, G=4, K=128, N=64, dtype="bf16", seed=9, device="cuda")
+@pytest.mark.parametrize("n", [64, 63])
+def test_device_detected_errors_zero_the_output(n):
+    base = make_case(batch=64, top_k=2, G=4, K=128, N=n, dtype="bf16", seed=9, device="cuda")
     cases = {}
     idx = base.expanded_row_idx.clone()
     idx[5] = base.batch * base.top_k  # out of range
@@ -201,8 +207,9 @@ def test_device_detected_errors_zero_the_output():
     check(base, what="after errors")
 
 
-def test_bounded_wait_reports_timeout_and_recovers():
-    inp = make_case(batch=256, top_k=4, G=8, K=256, N=128, dtype="bf16", seed=10,
+@pytest.mark.parametrize("n", [128, 127])
+def test_bounded_wait_reports_timeout_and_recovers(n):
+    inp = make_case(batch=256, top_k=4, G=8, K=256, N=n, dtype="bf16", seed=10,
                     device="cuda")
     pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
     pgg.pgg_debug_set_ticket_bias(1000)          # no ticket ever reaches rank + 1000
@@ -231,13 +238,63 @@ def test_no_writes_outside_out_and_workspace():
     assert_close(out.double().cpu().numpy(), ref_rows(inp))
 
 
-def test_unaligned_row_stride_is_rejected():
-    for N in (1, 286):
-        inp = make_case(batch=128, top_k=3, G=4, K=128, N=N, dtype="bf16", seed=12,
-                        device="cuda")
-        with pytest.raises(pgg.PggError) as e:
-            run(inp)
-        assert pgg.STATUS[e.value.code] == "PGG_ERR_ALIGN"
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_unaligned_rows_many_tiles(dtype):
+    # rows of 2 * 1030 (or 4 * 1031) bytes: the FP32-pipe kernel over many row
+    # blocks, k blocks with a ragged tail, and a ragged reduction tail
+    n = 1031 if dtype == "fp32" else 1030
+    inp = make_case(batch=1000, top_k=4, G=9, K=300, N=n, dtype=dtype, routing="zipf",
+                    zipf_zero=2, seed=12, device="cuda")
+    assert pgg.pgg_dx_plan(*_sizes(inp), 0, pgg.dtype_code(inp.grad_y.dtype))["variant"] == 3
+    check(inp, what=f"unaligned rows {dtype}")
+
+
+def _sizes(inp):
+    M, N = inp.grad_y.shape
+    G, K, _ = inp.weight.shape
+    return M, N, K, G, M, inp.batch, inp.top_k
+
+
+def _shifted(t, elems):
+    # the same values in a contiguous tensor whose address is `elems` elements
+    # past an allocation boundary
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    v = buf[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_misaligned_pointers(dtype):
+    # gradY / weight not 16-byte aligned: the FP32-pipe kernel, whose result
+    # does not depend on the addresses; out not 16-byte aligned: scalar
+    # epilogue stores, bitwise equal to the vector ones
+    inp = make_case(batch=300, top_k=4, G=6, K=256, N=128, dtype=dtype, seed=15, device="cuda")
+    ref = ref_rows(inp)
+    try:
+        pgg.pgg_debug_force_variant(3)
+        simt, _ = run(inp)
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert_close(simt.double().cpu().numpy(), ref, "forced FP32-pipe kernel")
+    for shift_y, shift_w in ((1, 0), (0, 1), (3, 5)):
+        out, ws = pgg.dx(_shifted(inp.grad_y, shift_y), _shifted(inp.weight, shift_w),
+                         inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k, 0)
+        torch.cuda.synchronize()
+        assert pgg.status(ws) == 0
+        assert torch.equal(out.view(torch.int32), simt.view(torch.int32)), (shift_y, shift_w)
+    tc, _ = run(inp)
+    assert_close(tc.double().cpu().numpy(), ref, "tensor cores")
+    out_buf = torch.empty(300 * 256 + 1, dtype=torch.float32, device="cuda")
+    out = out_buf[1:].view(300, 256)
+    _, ws = run(inp, out=out)
+    assert pgg.status(ws) == 0
+    assert torch.equal(out.view(torch.int32), tc.view(torch.int32))
+    _, ws = pgg.dx(_shifted(inp.grad_y, 1), inp.weight, inp.expanded_row_idx, inp.group_list,
+                   inp.batch, inp.top_k, 0, out=out)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(out.view(torch.int32), simt.view(torch.int32))
 
 
 # ---------------------------------------------------------------- full-size workloads

@@ -70,7 +70,7 @@ class Workload:
         }
 
 
-# The five workloads the benchmarks and full-size parity tests run.
+# The workloads the benchmarks and full-size parity tests run.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -81,6 +81,8 @@ WORKLOADS = {
                  routing="zipf", zipf_s=1.2, zipf_zero=10, row_idx_type=1),
         Workload("large-bf16", batch=13500, top_k=8, G=60, K=7168, N=2048, dtype="bf16"),
         Workload("skinny-bf16", batch=256, top_k=8, G=256, K=7168, N=2048, dtype="bf16"),
+        # rows of 2044 bytes (not a multiple of 16): the FP32-pipe kernel
+        Workload("unaligned-bf16", batch=4096, top_k=8, G=16, K=2048, N=1022, dtype="bf16"),
     ]
 }
 
