@@ -132,7 +132,7 @@ def test_rows_the_tma_cannot_stream_take_the_fp32_pipe_kernel(lib):
                   (1, pgg.PGG_F32)):
         p = pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)
         assert p["variant"] == 3 and p["rows_per_block"] == 64 and p["threads"] == 128, (n, dt)
-        assert p["cta_pair"] == 0 and p["smem_bytes"] <= 48 * 1024
+        assert p["cta_pair"] == 0 and p["smem_bytes"] <= 227 * 1024 // 3  # 3 CTAs per SM
     for n, dt in ((8, pgg.PGG_BF16), (4, pgg.PGG_F32), (280, pgg.PGG_F16)):
         assert pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)["variant"] != 3, (n, dt)
     # the workspace stays small at the pages' scale
