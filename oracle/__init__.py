@@ -1,4 +1,4 @@
-"""Oracle for the fused MoE permute + grouped-matmul backward (d_x only).
+"""Oracle for the MoE permute + grouped-matmul backward: d_x and d_weight.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package. The product path
@@ -14,14 +14,22 @@ page "MoeInitRoutingGroupedMatmulGrad design" (section "数学定义和公式"):
 
 with batch(i) = original_pos(i) // topK (same section, Step 2) and
 expandedRowIdx read in gather (rowIdxType 0) or scatter (rowIdxType 1) form
-(section "输入输出", note 1).
+(section "输入输出", note 1); and the weight gradient of the separate operator
+the same page describes (section 1.2, "为何不计算 d_weight" item 3:
+expanded_x^T @ d_y per expert, expanded_x[i] = x[batch(i)] from the forward's
+MoeInitRouting of section 1.1):
 
-Pins (``tests/test_oracle_pins.py``): a pure-Python indicator-sum brute force,
+    d_weight[g, k, n] = sum_{i in expert g} x[batch(i), k] * d_y[i, n]
+
+Pins (``tests/test_oracle_pins.py``, ``tests/test_oracle_dw_pins.py``): a
+pure-Python indicator-sum brute force,
 the unfused two-step form written with numpy, ``torch.matmul`` for the
 one-expert identity-routing case, hand-derived closed forms, a hand-worked
 example in ``tests/golden/``, and invariants (column sums, expert relabelling,
-empty experts, gather vs scatter index, linearity). The dtype decoders are
-pinned against numpy / torch conversions of every 16-bit pattern.
+empty experts, gather vs scatter index, linearity), and for d_weight the
+adjoint identity sum(d_weight * weight) == sum(d_x * x), which ties the two
+functions to each other. The dtype decoders are pinned against numpy / torch
+conversions of every 16-bit pattern.
 """
 
 from __future__ import annotations
@@ -75,6 +83,9 @@ def load_library(path: str):
     lib.oracle_dx.restype = ctypes.c_int
     lib.oracle_decode.argtypes = [vp, ctypes.c_int, i64, dp]
     lib.oracle_decode.restype = ctypes.c_int
+    lib.oracle_dw.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64,
+                              i64, i64, ctypes.c_int, vp, vp, i64, dp, ctypes.c_int]
+    lib.oracle_dw.restype = ctypes.c_int
     return lib
 
 
@@ -161,6 +172,47 @@ def dx(grad_y, weight, expanded_row_idx, group_list, batch: int, top_k: int,
     if rc != 0:
         raise OracleError(rc)
     return out
+
+
+def dw(x, grad_y, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_type: int,
+       sel=None, nthreads: int = 0, lib=None) -> np.ndarray:
+    """fp64 d_weight. With ``sel`` None: array [G, K, N]; otherwise ``sel`` is a
+    pair (g, k) of int arrays and the result is [len(g), N], row s being
+    d_weight[g[s], k[s], :].
+
+    x: [batch, K] (the forward input, original token order), grad_y: [M, N],
+    same dtype; expanded_row_idx, group_list as for ``dx``. ``group_list`` also
+    fixes G.
+    """
+    lib = lib or _load()
+    xr, dt = _raw(x)
+    dy, dty = _raw(grad_y)
+    if dt != dty:
+        raise OracleError(4)
+    B, K = xr.shape
+    M, N = dy.shape
+    idx = _i64(expanded_row_idx)
+    gl = _i64(group_list)
+    G = gl.shape[0]
+    if B != batch or idx.shape != (M,):
+        raise OracleError(2)
+    if sel is None:
+        sg = sk = None
+        ns = G * K
+    else:
+        sg, sk = _i64(sel[0]), _i64(sel[1])
+        if sg.shape != sk.shape or sg.ndim != 1:
+            raise OracleError(2)
+        ns = sg.shape[0]
+    out = np.empty((ns, N), dtype=np.float64)
+    rc = lib.oracle_dw(xr.ctypes.data, dy.ctypes.data, dt, idx.ctypes.data, gl.ctypes.data,
+                       M, N, K, G, batch, top_k, row_idx_type,
+                       None if sg is None else sg.ctypes.data,
+                       None if sk is None else sk.ctypes.data, ns, out.ctypes.data,
+                       int(nthreads))
+    if rc != 0:
+        raise OracleError(rc)
+    return out.reshape(G, K, N) if sel is None else out
 
 
 def decode(raw_bits: np.ndarray, dtype_code: int, lib=None) -> np.ndarray:

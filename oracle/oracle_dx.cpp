@@ -1,4 +1,6 @@
-// Oracle for the fused MoE permute + grouped-matmul backward (input gradient only).
+// Oracle for the MoE permute + grouped-matmul backward: the input gradient d_x
+// (the fused operator) and the weight gradient d_weight (its separate
+// companion operator).
 //
 // TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, load or call
 // this file; only the tests, the smoke check and the benchmark's CPU-baseline
@@ -33,6 +35,20 @@
 // Input validation mirrors the constraint table (section "约束"): batch > 0,
 // topK > 0, rowIdxType in {0, 1}, M == batch * topK, every groupList entry
 // >= 0 and their sum == M, expandedRowIdx a permutation of [0, M).
+//
+// d_weight (same page, section 1.2 "为何不计算 d_weight" item 3: a separate
+// grouped matmul expanded_x^T @ d_y per expert; section 1.1: the forward's
+// MoeInitRouting lays the token rows out by expert as expanded_x, so row i of
+// expanded_x is row batch(i) of the forward input x):
+//
+//     d_weight[g, k, n] = sum over expanded rows i of expert g of
+//                         x[batch(i), k] * d_y[i, n]
+//
+// Steps, in this order: widen every input element to double; find the expert
+// of each expanded row by walking groupList and the original position of each
+// row from the index; for each requested (g, k), for the rows i of expert g in
+// increasing order, add x[batch(i), k] * d_y[i, n] into an accumulator row
+// over n. An expert with no rows has a zero gradient.
 
 #include <cmath>
 #include <cstdint>
@@ -104,6 +120,8 @@ struct Decoder {
 struct Routing {
   std::vector<int64_t> group_of_row;  // g(i) for every expanded row i
   std::vector<int64_t> row_of_pos;    // expanded row of original position p
+  std::vector<int64_t> pos_of_row;    // original position of expanded row i
+  std::vector<int64_t> first_row;     // first expanded row of expert g (G + 1 entries)
 };
 
 // Validates the inputs against the constraint table and builds g(i) and the
@@ -118,9 +136,13 @@ int build_routing(const int64_t* idx, const int64_t* group_list, int64_t M, int6
   if (total != M) return kErrGroupSum;
 
   r->group_of_row.assign(M, -1);
+  r->first_row.assign(G + 1, 0);
   int64_t i = 0;
-  for (int64_t g = 0; g < G; ++g)
+  for (int64_t g = 0; g < G; ++g) {
+    r->first_row[g] = i;
     for (int64_t c = 0; c < group_list[g]; ++c) r->group_of_row[i++] = g;
+  }
+  r->first_row[G] = i;
 
   for (int64_t q = 0; q < M; ++q)
     if (idx[q] < 0 || idx[q] >= M) return kErrIndex;
@@ -141,6 +163,8 @@ int build_routing(const int64_t* idx, const int64_t* group_list, int64_t M, int6
       r->row_of_pos[p] = idx[p];
     }
   }
+  r->pos_of_row.assign(M, -1);
+  for (int64_t p = 0; p < M; ++p) r->pos_of_row[r->row_of_pos[p]] = p;
   return kOk;
 }
 
@@ -175,6 +199,50 @@ void run_tokens(const Job& job, int64_t t_begin, int64_t t_end) {
     double* o = job.out + t * K;
     for (int64_t k = 0; k < K; ++k) o[k] = acc[k];
   }
+}
+
+struct DwJob {
+  const void* x;
+  const void* dy;
+  const Decoder* dec;
+  const Routing* routing;
+  const int64_t* sel_g;
+  const int64_t* sel_k;
+  int64_t nsel, N, K, topK;
+  double* out;
+};
+
+void run_dw_rows(const DwJob& job, int64_t s_begin, int64_t s_end) {
+  const int64_t N = job.N, K = job.K;
+  std::vector<double> acc(N);
+  for (int64_t s = s_begin; s < s_end; ++s) {
+    const int64_t g = job.sel_g ? job.sel_g[s] : s / K;
+    const int64_t k = job.sel_k ? job.sel_k[s] : s % K;
+    for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+    for (int64_t i = job.routing->first_row[g]; i < job.routing->first_row[g + 1]; ++i) {
+      const int64_t b = job.routing->pos_of_row[i] / job.topK;
+      const double xv = job.dec->at(job.x, b * K + k);
+      for (int64_t n = 0; n < N; ++n) acc[n] += xv * job.dec->at(job.dy, i * N + n);
+    }
+    double* o = job.out + s * N;
+    for (int64_t n = 0; n < N; ++n) o[n] = acc[n];
+  }
+}
+
+template <class JobT, class Fn>
+void run_pool(const JobT& job, int64_t count, int nthreads, Fn fn) {
+  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
+  if (nthreads <= 0) nthreads = 1;
+  if (nthreads > count) nthreads = static_cast<int>(count > 0 ? count : 1);
+  std::vector<std::thread> pool;
+  const int64_t per = (count + nthreads - 1) / nthreads;
+  for (int th = 0; th < nthreads; ++th) {
+    const int64_t lo = th * per;
+    const int64_t hi = lo + per < count ? lo + per : count;
+    if (lo >= hi) break;
+    pool.emplace_back(fn, std::cref(job), lo, hi);
+  }
+  for (auto& t : pool) t.join();
 }
 
 }  // namespace
@@ -213,19 +281,34 @@ int oracle_dx(const void* dy, const void* w, int dtype, const int64_t* expanded_
 
   Decoder dec(dtype);
   Job job{dy, w, &dec, &routing, tokens, ntokens, N, K, topK, out};
-  if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
-  if (nthreads <= 0) nthreads = 1;
-  if (nthreads > ntokens) nthreads = static_cast<int>(ntokens > 0 ? ntokens : 1);
+  run_pool(job, ntokens, nthreads, run_tokens);
+  return kOk;
+}
 
-  std::vector<std::thread> pool;
-  const int64_t per = (ntokens + nthreads - 1) / nthreads;
-  for (int th = 0; th < nthreads; ++th) {
-    const int64_t lo = th * per;
-    const int64_t hi = lo + per < ntokens ? lo + per : ntokens;
-    if (lo >= hi) break;
-    pool.emplace_back(run_tokens, std::cref(job), lo, hi);
-  }
-  for (auto& t : pool) t.join();
+// d_weight rows dW[sel_g[s], sel_k[s], 0..N-1] for s < nsel (all G*K rows in
+// (g, k) order when sel_g == sel_k == NULL, then nsel must equal G * K). out
+// is [nsel, N] double. x is [batch, K], dy is [M, N], both in the given dtype.
+int oracle_dw(const void* x, const void* dy, int dtype, const int64_t* expanded_row_idx,
+              const int64_t* group_list, int64_t M, int64_t N, int64_t K, int64_t G,
+              int64_t batch, int64_t topK, int row_idx_type, const int64_t* sel_g,
+              const int64_t* sel_k, int64_t nsel, double* out, int nthreads) {
+  if (!x || !dy || !expanded_row_idx || !group_list || !out) return kErrNull;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return kErrDtype;
+  if (batch <= 0 || topK <= 0 || (row_idx_type != 0 && row_idx_type != 1)) return kErrAttr;
+  if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return kErrShape;
+  if (M != batch * topK) return kErrShape;
+  if ((sel_g == nullptr) != (sel_k == nullptr)) return kErrNull;
+  if (!sel_g && nsel != G * K) return kErrShape;
+  for (int64_t s = 0; sel_g && s < nsel; ++s)
+    if (sel_g[s] < 0 || sel_g[s] >= G || sel_k[s] < 0 || sel_k[s] >= K) return kErrShape;
+
+  Routing routing;
+  const int rc = build_routing(expanded_row_idx, group_list, M, G, row_idx_type, &routing);
+  if (rc != kOk) return rc;
+
+  Decoder dec(dtype);
+  DwJob job{x, dy, &dec, &routing, sel_g, sel_k, nsel, N, K, topK, out};
+  run_pool(job, nsel, nthreads, run_dw_rows);
   return kOk;
 }
 

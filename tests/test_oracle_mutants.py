@@ -1,7 +1,8 @@
 """Plausible mistakes planted in copies of the oracle source are caught.
 
 Each mutant is the oracle's C++ source with one edit (a dropped term, a wrong
-index, a transposed operand, swapped index forms, a wrong exponent bias),
+index, a transposed operand, swapped index forms, a wrong exponent bias, in
+the input gradient or the weight gradient),
 compiled to a temporary library on the CPU. The check fails if any mutant
 passes every pin below, i.e. if the pins could not tell it from the real
 oracle. Every mutant keeps all memory accesses in bounds.
@@ -33,6 +34,15 @@ MUTANTS = {
     "group_off_by_one": ("r->group_of_row[i++] = g;", "r->group_of_row[i++] = (g + 1) % G;"),
     "fp16_exponent_bias": ("e - 25", "e - 24"),
     "bf16_wrong_half": ("static_cast<uint32_t>(h) << 16;", "static_cast<uint32_t>(h) << 15;"),
+    # weight gradient
+    "dw_drop_last_row": ("i < job.routing->first_row[g + 1]; ++i)",
+                         "i + 1 < job.routing->first_row[g + 1]; ++i)"),
+    "dw_rows_from_start": ("for (int64_t i = job.routing->first_row[g];",
+                           "for (int64_t i = 0;"),
+    "dw_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;",
+                                     "const int64_t b = i / job.topK;"),
+    "dw_k_n_swapped_in_x": ("job.dec->at(job.x, b * K + k)",
+                            "job.dec->at(job.x, b * K + (K - 1 - k))"),
 }
 
 
@@ -50,6 +60,8 @@ def build_mutant(tmp_path, name):
 
 def pins_pass(lib) -> bool:
     from test_oracle_pins import brute_force, unfused_numpy, rel_err
+    from test_oracle_dw_pins import brute_force_dw
+    from workloads.moe import forward_input
     # decoders against numpy / torch
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     ref16 = bits.view(np.float16).astype(np.float64)
@@ -76,6 +88,15 @@ def pins_pass(lib) -> bool:
             if rel_err(got, brute_force(inp)) > 1e-12:
                 return False
             if rel_err(got, unfused_numpy(inp)[0]) > 1e-12:
+                return False
+            # weight gradient against its brute force
+            x = forward_input(inp)
+            try:
+                gw = oracle.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch,
+                               inp.top_k, rit, lib=lib)
+            except oracle.OracleError:
+                return False
+            if rel_err(gw, brute_force_dw(inp, x)) > 1e-12:
                 return False
     return True
 

@@ -12,6 +12,7 @@ from .moe import (  # noqa: F401
     Workload,
     make_inputs,
     make_case,
+    forward_input,
     route_experts,
     expanded_order,
 )

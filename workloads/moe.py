@@ -21,7 +21,9 @@ Recipe (the same for every workload, seed 0 unless stated):
 3. Values. d_y ~ N(0, 1) with shape [M, N] in expanded order and
    weight ~ N(0, w_std^2) with shape [G, K, N], drawn in fp32 and rounded to
    the workload dtype (round to nearest even). The weight is drawn one
-   expert at a time so that the fp32 staging stays small.
+   expert at a time so that the fp32 staging stays small. For the weight
+   gradient, the forward input x ~ N(0, 1) with shape [batch, K] (seed + 2,
+   ``forward_input``).
 
 The pages' shapes: M ~ 108K expanded tokens, K = 7168, G = 60, N = 2048
 ("MoeInitRoutingGroupedMatmulGrad design", section 1.2 and the d_weight
@@ -176,6 +178,18 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     idx = gather if w.row_idx_type == 0 else scatter
     dy, weight = _values(w, device, w.seed)
     return Inputs(w, dy, weight, idx.to(device), group_list.to(device), experts, gather)
+
+
+def forward_input(inp: Inputs, device=None) -> torch.Tensor:
+    """The forward input x [batch, K] that goes with ``inp`` (the operand of the
+    weight gradient): x ~ N(0, 1) drawn in fp32 on ``device`` (default: the
+    device of ``inp``) with seed + 2 and rounded to the workload dtype."""
+    w = inp.workload
+    device = inp.grad_y.device if device is None else device
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed + 2)
+    x = torch.randn(w.batch, w.K, generator=gen, device=device, dtype=torch.float32)
+    return x.to(DTYPES[w.dtype])
 
 
 def make_case(batch, top_k, G, K, N, dtype="bf16", routing="uniform", row_idx_type=0,
