@@ -227,6 +227,58 @@ int pgg_dx_execute_static_scratch(const void* gradY, const void* weight,
                                   int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
                                   float* out, uint32_t* status, pgg_stream_t stream);
 
+/*
+ * ---------------------------------------------------------------------------
+ * Weight gradient (the companion operator; page "MoeInitRoutingGroupedMatmulGrad
+ * design", section 1.2 "为何不计算 d_weight", item 3: a separate grouped matmul
+ * expanded_x^T @ d_y per expert; section 1.1: the forward's MoeInitRouting
+ * lays out the token rows by expert, expanded_x[i] = x[batch(i)]):
+ *
+ *     dweight[g, k, n] = sum_{expanded rows i of expert g} x[batch(i), k] * gradY[i, n]
+ *
+ *   x              device, [batch, K] of `dtype`: the forward input in original
+ *                  token order. expanded_x is never materialised: its rows are
+ *                  gathered from x by token. (A caller that kept expanded_x
+ *                  [M, K] instead passes it as x with batch = M, topK = 1 and
+ *                  expandedRowIdx = 0 .. M-1, groupList unchanged.)
+ *   gradY          device, [M, N] of `dtype`, expanded order
+ *   expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType, dtype:
+ *                  as for pgg_dx_execute
+ *   out_dtype      dtype of dweight: `dtype` (the page sizes d_weight in the
+ *                  input precision) or PGG_F32; else PGG_ERR_DTYPE. Accumulation
+ *                  is always FP32; a 16-bit output is rounded to nearest even.
+ *   workspace      at least pgg_dw_workspace_size bytes, 256-byte aligned;
+ *                  status word at offset 0 as for pgg_dx_execute
+ *   dweight        device, [G, K, N] of out_dtype, fully overwritten; an expert
+ *                  with no rows gets zeros; zero-filled when the routing
+ *                  validation fails
+ *
+ * Each element is produced by one tile with a fixed order of additions (the
+ * expert's rows in increasing order, in MMA blocks of 16), so the result is
+ * bitwise repeatable. Runs on the tensor cores when dtype is 16-bit, K and N
+ * are multiples of 8 and x, gradY, dweight are 16-byte aligned; otherwise on
+ * the FP32 pipes (also forced by pgg_debug_force_variant(3)). Alignment: x and
+ * gradY aligned to their element size, dweight to its element size.
+ */
+int pgg_dw_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                          int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                          size_t* workspace_bytes);
+
+int pgg_dw_execute(const void* x, const void* gradY, const int64_t* expandedRowIdx,
+                   const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                   int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                   pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* dweight,
+                   pgg_stream_t stream);
+
+/*
+ * How pgg_dw_execute runs these sizes with 16-byte aligned pointers: variant 0
+ * (tensor cores: k_per_block = 128 output rows, 256 output columns, 64
+ * reduction rows per stage) or 3 (FP32 pipes: 64 rows, 128 columns, 32 rows
+ * per step); k_blocks and band_k_blocks hold the k and n blocks per expert.
+ */
+int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
+
 #ifdef __cplusplus
 }
 #endif

@@ -12,6 +12,7 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401
     CODES, PGG_BF16, PGG_F16, PGG_F32, STATUS, PggError, load,
     pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
+    pgg_dw_execute, pgg_dw_plan, pgg_dw_workspace_size,
     pgg_dx_execute, pgg_dx_execute_static_scratch, pgg_dx_grouped_gemm, pgg_dx_plan,
     pgg_dx_route_prep,
     pgg_dx_workspace_size, pgg_status_string,
@@ -74,6 +75,42 @@ def dx(grad_y, weight, expanded_row_idx, group_list, batch: int, top_k: int,
                         stream.cuda_stream)
     if rc != 0:
         raise PggError(rc, "pgg_dx_execute")
+    return out, workspace
+
+
+def dw(x, grad_y, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_type: int,
+       G: int | None = None, out_dtype=None, out=None, workspace=None, stream=None):
+    """d_weight [G, K, N] (``out_dtype``: grad_y's dtype by default, or
+    torch.float32) from the forward input x [batch, K] and grad_y [M, N].
+    G defaults to len(group_list). Returns (out, workspace)."""
+    import torch
+    for t in (x, grad_y, expanded_row_idx, group_list):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if expanded_row_idx.dtype != torch.int64 or group_list.dtype != torch.int64:
+        raise ValueError("expandedRowIdx and groupList must be int64")
+    if x.dtype != grad_y.dtype:
+        raise PggError(CODES["PGG_ERR_DTYPE"], "dw")
+    M, N = grad_y.shape
+    _, K = x.shape
+    G = group_list.shape[0] if G is None else G
+    sizes = (M, N, K, G, expanded_row_idx.shape[0], batch, top_k)
+    dt = dtype_code(grad_y.dtype)
+    out_dtype = grad_y.dtype if out_dtype is None else out_dtype
+    odt = dtype_code(out_dtype)
+    need = pgg_dw_workspace_size(*sizes, row_idx_type, dt)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=grad_y.device)
+    if out is None:
+        out = torch.empty(G, K, N, dtype=out_dtype, device=grad_y.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(grad_y.device)
+    rc = pgg_dw_execute(x.data_ptr(), grad_y.data_ptr(), expanded_row_idx.data_ptr(),
+                        group_list.data_ptr(), *sizes, row_idx_type, dt, odt,
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        out.data_ptr(), stream.cuda_stream)
+    if rc != 0:
+        raise PggError(rc, "pgg_dw_execute")
     return out, workspace
 
 

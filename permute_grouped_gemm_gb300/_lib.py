@@ -65,8 +65,12 @@ def load(path: str | None = None):
             lib.pgg_dx_route_prep.argtypes = [vp, vp, *_SIZES, i32, i32, vp, sz, vp]
             lib.pgg_dx_execute_static_scratch.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, vp,
                                                           vp, vp]
+            lib.pgg_dw_workspace_size.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(sz)]
+            lib.pgg_dw_plan.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(PlanInfo)]
+            lib.pgg_dw_execute.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz, vp, vp]
             for f in ("pgg_dx_workspace_size", "pgg_dx_plan", "pgg_dx_execute",
-                      "pgg_dx_grouped_gemm", "pgg_dx_route_prep", "pgg_dx_execute_static_scratch"):
+                      "pgg_dx_grouped_gemm", "pgg_dx_route_prep", "pgg_dx_execute_static_scratch",
+                      "pgg_dw_workspace_size", "pgg_dw_plan", "pgg_dw_execute"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.pgg_status_string.argtypes = [ctypes.c_int]
             lib.pgg_status_string.restype = ctypes.c_char_p
@@ -129,6 +133,28 @@ def pgg_dx_execute_static_scratch(gradY, weight, expandedRowIdx, groupList, M, N
     return load().pgg_dx_execute_static_scratch(gradY, weight, expandedRowIdx, groupList, M, N, K,
                                                 G, L, batch, topK, rowIdxType, dtype, out,
                                                 status or None, stream)
+
+
+def pgg_dw_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pgg_dw_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype,
+                                        ctypes.byref(out)), "pgg_dw_workspace_size")
+    return out.value
+
+
+def pgg_dw_plan(M, N, K, G, L, batch, topK, rowIdxType, dtype) -> dict:
+    info = PlanInfo()
+    _check(load().pgg_dw_plan(M, N, K, G, L, batch, topK, rowIdxType, dtype,
+                              ctypes.byref(info)), "pgg_dw_plan")
+    return info.as_dict()
+
+
+def pgg_dw_execute(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType,
+                   dtype, out_dtype, workspace, workspace_bytes, dweight, stream) -> int:
+    """Raw call with integer device addresses; returns the pgg_status code."""
+    return load().pgg_dw_execute(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                                 rowIdxType, dtype, out_dtype, workspace, workspace_bytes,
+                                 dweight, stream)
 
 
 def pgg_status_string(code: int) -> str:

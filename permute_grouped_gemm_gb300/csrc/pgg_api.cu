@@ -26,6 +26,14 @@ bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads,
 void simt_config(int* rows, int* stages, int* threads, int* smem);
 cudaError_t launch_simt(int dtype, const SimtArgs& a, int64_t max_tiles, int num_sms,
                         cudaStream_t stream);
+int dw_smem_bytes();
+int dw_threads();
+void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
+cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int num_sms,
+                      cudaStream_t stream);
+void dw_simt_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
+int dw_simt_smem_bytes();
+cudaError_t launch_dw_simt(int dtype, const DwArgs& a, int vec, int num_sms, cudaStream_t stream);
 
 namespace {
 
@@ -275,6 +283,80 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
              : PGG_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- weight gradient
+
+// The tensor-core kernel takes 16-bit inputs whose x and d_y rows are whole
+// 16-byte units, with x, d_y and the output 16-byte aligned; everything else
+// runs on the FP32 pipes.
+bool dw_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void* dy,
+                    const void* out) {
+  if (g_force_variant.load() == kVariantSimt) return false;
+  if (dtype == PGG_F32) return false;
+  if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0) return false;
+  return aligned(x, 16) && aligned(dy, 16) && aligned(out, 16);
+}
+
+int check_dw(const void* x, const void* gradY, const int64_t* idx, const int64_t* gl,
+             int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+             int rowIdxType, int dtype, int out_dtype, void* ws, size_t ws_bytes,
+             const void* dweight, Plan* plan) {
+  if (!x || !gradY || !idx || !gl || !ws || !dweight) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  if (out_dtype != dtype && out_dtype != PGG_F32) return PGG_ERR_DTYPE;
+  if (G * K > kInt32Max / 4) return PGG_ERR_SHAPE;  // tile numbers stay below 2^31
+  rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, plan);
+  if (rc != PGG_OK) return rc;
+  const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
+  if (!aligned(ws, 256) || !aligned(idx, 8) || !aligned(gl, 8)) return PGG_ERR_ALIGN;
+  if (!aligned(x, es) || !aligned(gradY, es) ||
+      !aligned(dweight, static_cast<uintptr_t>(elem_size(out_dtype))))
+    return PGG_ERR_ALIGN;
+  if (ws_bytes < plan->layout.total) return PGG_ERR_WORKSPACE;
+  return PGG_OK;
+}
+
+int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* dweight,
+           int out_dtype, cudaStream_t stream) {
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  char* w = static_cast<char*>(ws);
+  DwArgs a;
+  a.x = x;
+  a.dy = gradY;
+  a.off = reinterpret_cast<const int64_t*>(w + plan.layout.off);
+  a.rowinfo = reinterpret_cast<const RowInfo*>(w + plan.layout.rowinfo);
+  a.hdr = reinterpret_cast<WsHeader*>(w + plan.layout.hdr);
+  a.out = dweight;
+  a.M = plan.M;
+  a.N = plan.N;
+  a.K = plan.K;
+  a.G = plan.G;
+  a.batch = plan.batch;
+  a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (dw_tensor_path(plan.dtype, plan.N, plan.K, x, gradY, dweight)) {
+    dw_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PGG_ERR_CUDA;
+    CUtensorMap tm;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(plan.N) * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&tm, tmap_type(plan.dtype), 2, const_cast<void*>(gradY), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PGG_ERR_CUDA;
+    return launch_dw(plan.dtype, tm, a, di.num_sms, stream) == cudaSuccess ? PGG_OK : PGG_ERR_CUDA;
+  }
+  dw_simt_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
+  const uintptr_t vec_align = out_dtype == PGG_F32 ? 16 : 8;
+  const int vec = (plan.N % 4 == 0 && aligned(dweight, vec_align)) ? 1 : 0;
+  return launch_dw_simt(plan.dtype, a, vec, di.num_sms, stream) == cudaSuccess ? PGG_OK
+                                                                                  : PGG_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pgg
 
@@ -353,6 +435,63 @@ int pgg_dx_execute(const void* gradY, const void* weight, const int64_t* expande
   rc = run_route_prep(plan, expandedRowIdx, groupList, workspace, s);
   if (rc != PGG_OK) return rc;
   return run_grouped_gemm(plan, gradY, weight, workspace, out, s);
+}
+
+int pgg_dw_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                          int64_t topK, int rowIdxType, pgg_dtype dtype, size_t* workspace_bytes) {
+  return pgg_dx_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype, workspace_bytes);
+}
+
+int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                int rowIdxType, pgg_dtype dtype, pgg_plan_info* info) {
+  if (!info) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  Plan p;
+  rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
+  if (rc != PGG_OK) return rc;
+  // 16-byte aligned pointers assumed: only the shape decides here
+  alignas(16) static const char probe[16] = {0};
+  const bool tc = dw_tensor_path(dtype, N, K, probe, probe, probe);
+  std::memset(info, 0, sizeof(*info));
+  int kb = 0, nb = 0;
+  if (tc) {
+    dw_tiles(K, N, &kb, &nb);
+    info->variant = 0;
+    info->rows_per_block = 64;
+    info->k_per_block = 128;
+    info->stages = 4;
+    info->threads = dw_threads();
+    info->smem_bytes = dw_smem_bytes();
+  } else {
+    dw_simt_tiles(K, N, &kb, &nb);
+    info->variant = kVariantSimt;
+    info->rows_per_block = 32;
+    info->k_per_block = 64;
+    info->stages = 2;
+    info->threads = 128;
+    info->smem_bytes = dw_simt_smem_bytes();
+  }
+  info->k_blocks = kb;
+  info->band_k_blocks = nb;
+  info->max_row_blocks = G;
+  info->workspace_bytes = p.layout.total;
+  return PGG_OK;
+}
+
+int pgg_dw_execute(const void* x, const void* gradY, const int64_t* expandedRowIdx,
+                   const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                   int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                   pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* dweight,
+                   pgg_stream_t stream) {
+  Plan plan;
+  int rc = check_dw(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType,
+                    dtype, out_dtype, workspace, workspace_bytes, dweight, &plan);
+  if (rc != PGG_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = run_route_prep(plan, expandedRowIdx, groupList, workspace, s);
+  if (rc != PGG_OK) return rc;
+  return run_dw(plan, x, gradY, workspace, dweight, out_dtype, s);
 }
 
 const char* pgg_status_string(int status) {

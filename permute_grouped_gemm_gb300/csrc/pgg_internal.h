@@ -111,4 +111,19 @@ struct SimtArgs {
   uint64_t wait_limit_ns;
 };
 
+// Arguments of the weight-gradient kernels (gmm_dw.cu, gmm_dw_simt.cu).
+struct DwArgs {
+  const void* x;           // [batch, K] dtype: the forward input, original token order
+  const void* dy;          // [M, N] dtype, expanded order
+  const int64_t* off;      // [G + 1] first expanded row of each expert (routing step)
+  const RowInfo* rowinfo;  // [M] token of each expanded row (routing step)
+  WsHeader* hdr;
+  void* out;               // [G, K, N] in the output dtype
+  int64_t M, N, K, G, batch;
+  int32_t k_blocks;  // output rows (k) blocks per expert
+  int32_t n_blocks;  // output column (n) blocks per expert
+  int32_t out_f32;   // 1: out is fp32; 0: out has the input dtype
+  uint64_t wait_limit_ns;
+};
+
 }  // namespace pgg

@@ -212,6 +212,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile with the
+// 128-byte swizzle: panels of 64 (16-bit) elements along M or N, each stored as
+// rows of 128 bytes, one row per reduction index; 8-row groups are 1024 bytes
+// apart inside a panel (stride-dimension offset) and panels are `panel_bytes`
+// apart (leading-dimension offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t panel_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((panel_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32, dense, fp32 accumulator,
 // both operands K-major.
 //   bits 4-5 D format (1 = f32); bits 7-9 A format, 10-12 B format
@@ -219,6 +234,31 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 //   bits 17-22 N >> 3; bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_make(uint32_t ab_format, uint32_t m, uint32_t n) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Same with both operands MN-major (bits 15 and 16 set).
+__host__ __device__ constexpr uint32_t idesc_make_mn(uint32_t ab_format, uint32_t m, uint32_t n) {
+  return idesc_make(ab_format, m, n) | (1u << 15) | (1u << 16);
+}
+
+// ------------------------------------------------------------------ cp.async (16 bytes)
+
+// 16 bytes global -> shared; `src_bytes` (0 or 16) of them are read, the rest
+// are zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most N committed groups of this thread are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ------------------------------------------------------------------ scoped memory ops

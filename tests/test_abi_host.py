@@ -138,3 +138,28 @@ def test_rows_the_tma_cannot_stream_take_the_fp32_pipe_kernel(lib):
     # the workspace stays small at the pages' scale
     assert ws(N=2047) <= 16 * 2**20
     assert ws(N=2047) < LARGE["M"] * LARGE["K"] // 64
+
+
+def test_weight_gradient_plan_and_host_errors(lib):
+    a = LARGE
+    sizes = (a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"], a["topK"], 0)
+    p = pgg.pgg_dw_plan(*sizes, pgg.PGG_BF16)
+    assert p["variant"] == 0 and p["k_per_block"] == 128 and p["threads"] == 320
+    assert p["k_blocks"] == 56 and p["band_k_blocks"] == 8 and p["smem_bytes"] <= 227 * 1024
+    assert pgg.pgg_dw_plan(*sizes, pgg.PGG_F32)["variant"] == 3
+    assert pgg.pgg_dw_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
+                           pgg.PGG_BF16)["variant"] == 3
+    assert pgg.pgg_dw_workspace_size(*sizes, pgg.PGG_BF16) == ws()
+    fake = 1 << 20
+    need = ws()
+    args = (fake, fake, fake, fake, *sizes[:-1], 0, pgg.PGG_BF16)
+    assert pgg.STATUS[pgg.pgg_dw_execute(*args, pgg.PGG_F16, fake, need, fake, None)] == \
+        "PGG_ERR_DTYPE"
+    assert pgg.STATUS[pgg.pgg_dw_execute(*args, pgg.PGG_BF16, fake, need - 1, fake, None)] == \
+        "PGG_ERR_WORKSPACE"
+    assert pgg.STATUS[pgg.pgg_dw_execute(*args, pgg.PGG_BF16, fake, need, 0, None)] == \
+        "PGG_ERR_NULL"
+    assert pgg.STATUS[pgg.pgg_dw_execute(*args, pgg.PGG_F32, fake, need, fake + 2, None)] == \
+        "PGG_ERR_ALIGN"
+    assert pgg.STATUS[pgg.pgg_dw_execute(fake + 1, *args[1:], pgg.PGG_BF16, fake, need, fake,
+                                         None)] == "PGG_ERR_ALIGN"

@@ -1,0 +1,220 @@
+"""GPU parity of the weight gradient against the fp64 oracle, through the C ABI.
+
+Tolerance, derived from the arithmetic: the kernels accumulate in fp32, so an
+fp32 output must satisfy max |GPU - oracle| <= 1e-4 * max |oracle| (as d_x); a
+16-bit output is that fp32 sum rounded to nearest even once more, which adds
+at most half a unit in the last place: per element |GPU - oracle| <=
+2^-8 * |oracle| (bf16; 2^-11 for fp16) + 1e-4 * max |oracle|.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_case, make_inputs
+from workloads.moe import forward_input, with_row_idx_type
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+ROUND = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11, torch.float32: 0.0}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from permute_grouped_gemm_gb300 import build as pbuild
+    pbuild.build()
+    oracle.build()
+    pgg.load()
+    yield
+    pgg.pgg_debug_force_variant(-1)
+
+
+def run(inp, x, **kw):
+    out, ws = pgg.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch,
+                     inp.top_k, inp.row_idx_type, **kw)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0, pgg.STATUS.get(pgg.status(ws))
+    return out
+
+
+def ref_of(inp, x, sel=None):
+    return oracle.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k,
+                     inp.row_idx_type, sel=sel)
+
+
+def assert_close(got_t, ref, what=""):
+    got = got_t.double().cpu().numpy()
+    scale = np.abs(ref).max()
+    bound = ROUND[got_t.dtype] * np.abs(ref) + TOL * scale
+    err = np.abs(got - ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (f"{what}: |diff| {err[worst]:.3e} > bound {bound[worst]:.3e} "
+                                  f"at {worst} (ref {ref[worst]:.4e})")
+
+
+def plan_variant(inp, x):
+    M, N = inp.grad_y.shape
+    K = x.shape[1]
+    G = inp.group_list.shape[0]
+    return pgg.pgg_dw_plan(M, N, K, G, M, inp.batch, inp.top_k, inp.row_idx_type,
+                           pgg.dtype_code(x.dtype))["variant"]
+
+
+# The page's white-box shapes (section 4.2.1) plus multi-stage / ragged cases.
+CASES = {
+    "one_token_one_expert": dict(batch=1, K=128, N=256, top_k=1, G=1),
+    "one_token_multi_expert": dict(batch=1, K=128, N=256, top_k=3, G=3),
+    "multi_token_one_expert": dict(batch=128, K=128, N=256, top_k=1, G=1),
+    "multi_token_multi_expert": dict(batch=128, K=128, N=256, top_k=3, G=10),
+    "empty_expert": dict(batch=10, K=128, N=256, top_k=2, G=4, empty=(1,)),
+    "tail_k178_n286": dict(batch=10, K=178, N=286, top_k=3, G=4),
+    "n_is_1": dict(batch=128, K=128, N=1, top_k=3, G=4),
+    "k_is_1": dict(batch=128, K=1, N=256, top_k=3, G=4),
+    "ragged_tc": dict(batch=700, K=184, N=328, top_k=3, G=5),
+}
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_cases(case, dtype, out_f32):
+    inp = make_case(dtype=dtype, seed=21, device="cuda", **CASES[case])
+    x = forward_input(inp)
+    out = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert_close(out, ref_of(inp, x), case)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_tensor_and_fp32_pipe_kernels_agree_with_the_oracle(dtype):
+    # rows of several stages per expert, a partial last stage, ragged k and n
+    inp = make_case(batch=900, top_k=4, G=7, K=312, N=520, dtype=dtype, routing="zipf",
+                    zipf_zero=2, seed=22, device="cuda")
+    x = forward_input(inp)
+    assert plan_variant(inp, x) == 0
+    ref = ref_of(inp, x)
+    tc = run(inp, x, out_dtype=torch.float32)
+    assert_close(tc, ref, "tensor cores")
+    try:
+        pgg.pgg_debug_force_variant(3)
+        simt = run(inp, x, out_dtype=torch.float32)
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert_close(simt, ref, "FP32 pipes")
+    assert (inp.group_list == 0).sum() == 2
+    for g in torch.nonzero(inp.group_list == 0).flatten().tolist():
+        assert torch.count_nonzero(tc[g]) == 0 and torch.count_nonzero(simt[g]) == 0
+
+
+@pytest.mark.parametrize("force_simt", [False, True])
+def test_bitwise_repeatable_and_index_form_independent(force_simt):
+    inp = make_case(batch=1500, top_k=6, G=12, K=256, N=512, dtype="bf16", seed=23,
+                    device="cuda")
+    x = forward_input(inp)
+    try:
+        if force_simt:
+            pgg.pgg_debug_force_variant(3)
+        first = run(inp, x, out_dtype=torch.float32)
+        for _ in range(3):
+            assert torch.equal(run(inp, x, out_dtype=torch.float32).view(torch.int32),
+                               first.view(torch.int32))
+        other = run(with_row_idx_type(inp, 1), x, out_dtype=torch.float32)
+        assert torch.equal(other.view(torch.int32), first.view(torch.int32))
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert_close(first, ref_of(inp, x))
+
+
+def test_expanded_x_input_gives_the_same_bits():
+    # a caller that kept expanded_x [M, K] passes it as x with topK = 1 and the
+    # identity index: same rows, same order of additions
+    inp = make_case(batch=400, top_k=4, G=6, K=192, N=256, dtype="fp16", seed=24, device="cuda")
+    x = forward_input(inp)
+    gathered = run(inp, x)
+    pos = inp.gather.to("cuda")
+    ex = x[pos // inp.top_k].contiguous()
+    M = ex.shape[0]
+    ident = torch.arange(M, dtype=torch.int64, device="cuda")
+    out, ws = pgg.dw(ex, inp.grad_y, ident, inp.group_list, M, 1, 0)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(out.view(torch.int16), gathered.view(torch.int16))
+
+
+def _shifted(t, elems):
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    v = buf[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def test_misaligned_pointers_take_the_fp32_pipes():
+    inp = make_case(batch=300, top_k=4, G=6, K=256, N=256, dtype="bf16", seed=25, device="cuda")
+    x = forward_input(inp)
+    try:
+        pgg.pgg_debug_force_variant(3)
+        simt = run(inp, x, out_dtype=torch.float32)
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    out, ws = pgg.dw(_shifted(x, 1), _shifted(inp.grad_y, 3), inp.expanded_row_idx,
+                     inp.group_list, inp.batch, inp.top_k, 0, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(out.view(torch.int32), simt.view(torch.int32))
+    obuf = torch.empty(6 * 256 * 256 + 1, dtype=torch.float32, device="cuda")
+    o = obuf[1:].view(6, 256, 256)
+    _, ws = pgg.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k, 0,
+                   out_dtype=torch.float32, out=o)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(o.view(torch.int32), simt.view(torch.int32))
+
+
+def test_device_detected_errors_zero_the_output():
+    base = make_case(batch=64, top_k=2, G=4, K=128, N=64, dtype="bf16", seed=26, device="cuda")
+    x = forward_input(base)
+    for variant in (-1, 3):
+        idx = base.expanded_row_idx.clone()
+        idx[5] = idx[6]
+        out = torch.full((4, 128, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+        try:
+            pgg.pgg_debug_force_variant(variant)
+            _, ws = pgg.dw(x, base.grad_y, idx, base.group_list, 64, 2, 0, out=out)
+            torch.cuda.synchronize()
+        finally:
+            pgg.pgg_debug_force_variant(-1)
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_NOT_PERM"
+        assert torch.count_nonzero(out) == 0
+    assert_close(run(base, x), ref_of(base, x), "after errors")
+
+
+def test_gpu_results_satisfy_the_adjoint_identity():
+    # sum(dW * W) == sum(d_x * x), both from the GPU (fp32 outputs)
+    inp = make_case(batch=512, top_k=4, G=8, K=256, N=192, dtype="bf16", seed=27, device="cuda")
+    x = forward_input(inp)
+    dwt = run(inp, x, out_dtype=torch.float32).double()
+    dx, _ = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                   inp.top_k, 0)
+    lhs = float((dwt * inp.weight.double()).sum())
+    rhs = float((dx.double() * x.double()).sum())
+    assert abs(lhs - rhs) <= 1e-4 * (abs(lhs) + abs(rhs))
+
+
+@pytest.mark.parametrize("name", ["uniform-bf16", "skewed-fp16", "large-bf16", "skinny-bf16",
+                                  "unaligned-bf16"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda")
+    x = forward_input(inp)
+    out = run(inp, x)
+    rng = np.random.default_rng(2)
+    g = rng.integers(0, w.G, 48)
+    k = rng.integers(0, w.K, 48)
+    ref = ref_of(inp, x, sel=(g, k))
+    assert_close(out[torch.as_tensor(g), torch.as_tensor(k)], ref, name)
+    again = run(inp, x)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
