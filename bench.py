@@ -10,8 +10,11 @@ write) between steps, outside the per-step CUDA events.
 Metric: fused d_x TFLOP/s = 2*M*N*K / step time, with the roofline fraction
 of the grouped-GEMM kernel and the workspace bytes.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--op dx|dw]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+--op dw times the companion weight-gradient kernel (x^T d_y per expert with
+the x rows gathered by the routing) on the same workload instead.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload on its own GPU (the path needs no exchange); value sums the work of
@@ -30,6 +33,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -43,6 +48,8 @@ _COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh",
 KERNEL_SOURCES = {
     "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", *_COMMON],
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
+    "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", *_COMMON],
+    "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],
 }
 SIMT_VARIANT = 3
 FP32_LANES_PER_SM = 128    # FP32 fused multiply-add lanes per SM
@@ -56,6 +63,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--op", default="dx", choices=["dx", "dw"],
+                    help="dx: the fused input gradient (default); dw: the weight gradient")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -167,86 +176,191 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def algorithmic(inp):
-    """(flops, bytes) of one step: 2*M*N*K, and d_y once + weight of non-empty
-    experts once + d_x written once + the two index arrays."""
-    w = inp.workload
-    es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
-    nonempty = int((inp.group_list > 0).sum())
-    flops = 2 * w.M * w.N * w.K
-    nbytes = (w.M * w.N * es + nonempty * w.K * w.N * es + w.batch * w.K * 4
-              + w.M * 8 + w.G * 8)
-    return flops, nbytes
+class DxOp:
+    """d_x: the fused permute + grouped-matmul backward (the default)."""
+    name = "dx"
+    metric = METRIC
 
+    def __init__(self, inp, pgg, dev):
+        import torch
+        self.inp, self.pgg = inp, pgg
+        w = inp.workload
+        self.dt = pgg.dtype_code(inp.grad_y.dtype)
+        self.sizes = (w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k)
+        self.plan = pgg.pgg_dx_plan(*self.sizes, w.row_idx_type, self.dt)
+        self.ws_bytes = pgg.pgg_dx_workspace_size(*self.sizes, w.row_idx_type, self.dt)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.out = torch.empty(w.batch, w.K, dtype=torch.float32, device=dev)
+        self.kernel = "gmm_dx_simt_kernel" if self.plan["variant"] == SIMT_VARIANT else "gmm_dx_kernel"
 
-def cpu_baseline(inp, target_s: float):
-    """The oracle (as it stands) on a bounded sample of the workload's tokens."""
-    import numpy as np
-    import oracle
-    oracle.build()
-    w = inp.workload
-    host = inp.to("cpu")
-    rng = np.random.default_rng(0)
-    per_tok = 2 * w.top_k * w.N * w.K
-    cores = oracle.host_cores()
-    n = max(1, min(w.batch, cores))
-    toks = np.sort(rng.choice(w.batch, n, replace=False))
-    t0 = time.perf_counter()
-    oracle.dx(host.grad_y, host.weight, host.expanded_row_idx, host.group_list, w.batch,
-              w.top_k, w.row_idx_type, tokens=toks)
-    dt = time.perf_counter() - t0
-    if dt < target_s / 4 and n < w.batch:
-        n = int(min(w.batch, max(n, n * target_s / max(dt, 1e-3))))
+    def values(self):
+        return self.inp.grad_y, self.inp.weight
+
+    def stage2(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_dx_grouped_gemm(a.data_ptr(), b.data_ptr(), idx.data_ptr(),
+                                            gl.data_ptr(), *self.sizes, w.row_idx_type, self.dt,
+                                            self.ws.data_ptr(), self.ws_bytes, out.data_ptr(), sp)
+
+    def execute(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_dx_execute(a.data_ptr(), b.data_ptr(), idx.data_ptr(), gl.data_ptr(),
+                                       *self.sizes, w.row_idx_type, self.dt, self.ws.data_ptr(),
+                                       self.ws_bytes, out.data_ptr(), sp)
+
+    def algorithmic(self):
+        """(flops, bytes) of one step: 2*M*N*K, and d_y once + weight of non-empty
+        experts once + d_x written once + the two index arrays."""
+        inp = self.inp
+        w = inp.workload
+        es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+        nonempty = int((inp.group_list > 0).sum())
+        flops = 2 * w.M * w.N * w.K
+        nbytes = (w.M * w.N * es + nonempty * w.K * w.N * es + w.batch * w.K * 4
+                  + w.M * 8 + w.G * 8)
+        return flops, nbytes
+
+    def oracle_sample(self, host, rng, n):
+        """Runs the oracle on n sampled units; returns the flops of the sample."""
+        import oracle
+        w = host.workload
+        n = max(1, min(w.batch, n))
         toks = np.sort(rng.choice(w.batch, n, replace=False))
-        t0 = time.perf_counter()
         oracle.dx(host.grad_y, host.weight, host.expanded_row_idx, host.group_list, w.batch,
                   w.top_k, w.row_idx_type, tokens=toks)
+        return 2 * w.top_k * w.N * w.K * n, f"{n} of {w.batch} tokens (all topK rows each)"
+
+    def units(self):
+        return self.inp.workload.batch
+
+
+class DwOp(DxOp):
+    """d_weight: the companion weight-gradient grouped matmul."""
+    name = "dw"
+    metric = ("d_weight TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300: x^T d_y per expert, "
+              "x rows gathered by routing")
+
+    def __init__(self, inp, pgg, dev):
+        import torch
+        from workloads.moe import forward_input
+        self.inp, self.pgg = inp, pgg
+        w = inp.workload
+        self.dt = pgg.dtype_code(inp.grad_y.dtype)
+        self.sizes = (w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k)
+        self.plan = pgg.pgg_dw_plan(*self.sizes, w.row_idx_type, self.dt)
+        self.ws_bytes = pgg.pgg_dw_workspace_size(*self.sizes, w.row_idx_type, self.dt)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.x = forward_input(inp, dev)
+        self.out = torch.empty(w.G, w.K, w.N, dtype=inp.grad_y.dtype, device=dev)
+        self.kernel = "gmm_dw_simt_kernel" if self.plan["variant"] == SIMT_VARIANT else "gmm_dw_kernel"
+
+    def values(self):
+        return self.x, self.inp.grad_y
+
+    def stage2(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_dw_grouped_gemm(a.data_ptr(), b.data_ptr(), idx.data_ptr(),
+                                            gl.data_ptr(), *self.sizes, w.row_idx_type, self.dt,
+                                            self.dt, self.ws.data_ptr(), self.ws_bytes,
+                                            out.data_ptr(), sp)
+
+    def execute(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_dw_execute(a.data_ptr(), b.data_ptr(), idx.data_ptr(), gl.data_ptr(),
+                                       *self.sizes, w.row_idx_type, self.dt, self.dt,
+                                       self.ws.data_ptr(), self.ws_bytes, out.data_ptr(), sp)
+
+    def algorithmic(self):
+        """(flops, bytes): 2*M*N*K, and x once + d_y once + d_weight written once
+        (input dtype) + the two index arrays."""
+        w = self.inp.workload
+        es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+        flops = 2 * w.M * w.N * w.K
+        nbytes = (w.batch * w.K * es + w.M * w.N * es + w.G * w.K * w.N * es
+                  + w.M * 8 + w.G * 8)
+        return flops, nbytes
+
+    def oracle_sample(self, host, rng, n):
+        import oracle
+        from workloads.moe import forward_input
+        w = host.workload
+        if not hasattr(self, "_host_x"):
+            self._host_x = self.x.cpu()
+        n = max(1, min(w.G * w.K, n))
+        g = rng.integers(0, w.G, n)
+        k = rng.integers(0, w.K, n)
+        oracle.dw(self._host_x, host.grad_y, host.expanded_row_idx, host.group_list, w.batch,
+                  w.top_k, w.row_idx_type, sel=(g, k))
+        rows = host.group_list.numpy()[g]
+        return int(2 * w.N * rows.sum()), f"{n} of {w.G * w.K} rows (g, k) of d_weight"
+
+    def units(self):
+        return self.inp.workload.G * self.inp.workload.K
+
+
+OPS = {"dx": DxOp, "dw": DwOp}
+
+
+def cpu_baseline(op, target_s: float):
+    """The oracle (as it stands) on a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    host = op.inp.to("cpu")
+    rng = np.random.default_rng(0)
+    cores = oracle.host_cores()
+    n = cores
+    t0 = time.perf_counter()
+    flops, desc = op.oracle_sample(host, rng, n)
+    dt = time.perf_counter() - t0
+    if dt < target_s / 4 and n < op.units():
+        n = int(min(op.units(), max(n, n * target_s / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        flops, desc = op.oracle_sample(host, rng, n)
         dt = time.perf_counter() - t0
-    return {"value": per_tok * n / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, n),
-            "kind": "oracle",
-            "sample": f"{n} of {w.batch} tokens (all topK rows each), fp64 C++ loops, "
-                      f"{dt:.1f} s"}
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, n),
+            "kind": "oracle", "sample": f"{desc}, fp64 C++ loops, {dt:.1f} s"}
 
 
 def run_reference(args):
-    """The oracle timed on the host cores: each step a bounded token sample."""
+    """The oracle timed on the host cores: each step a bounded sample."""
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    import numpy as np
     import oracle
     from workloads import WORKLOADS, make_inputs
     oracle.build()
     w = WORKLOADS[args.workload]
     inp = make_inputs(w, device="cpu")
+    op = OPS[args.op].__new__(OPS[args.op])
+    op.inp = inp
+    if args.op == "dw":
+        from workloads.moe import forward_input
+        op.x = forward_input(inp, "cpu")
     cores = oracle.host_cores()
-    per_tok = 2 * w.top_k * w.N * w.K
     # size each step to ~ (a few minutes) / (steps + warmup)
     budget = 150.0 / max(1, args.steps + args.warmup)
     rng = np.random.default_rng(0)
-    n = max(1, min(w.batch, cores))
+    n = cores
     t0 = time.perf_counter()
-    oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, w.batch, w.top_k,
-              w.row_idx_type, tokens=np.arange(n))
+    op.oracle_sample(inp, rng, n)
     probe = time.perf_counter() - t0
-    n = int(max(1, min(w.batch, n * budget / max(probe, 1e-3))))
-    times = []
+    n = int(max(1, min(op.units(), n * budget / max(probe, 1e-3))))
+    times, flops, desc = [], 0, ""
     for s in range(args.warmup + args.steps):
-        toks = np.sort(rng.choice(w.batch, n, replace=False))
         t0 = time.perf_counter()
-        oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, w.batch,
-                  w.top_k, w.row_idx_type, tokens=toks)
+        flops_s, desc = op.oracle_sample(inp, rng, n)
         if s >= args.warmup:
             times.append(time.perf_counter() - t0)
-    dt = statistics.mean(times)
-    value = per_tok * n / dt / 1e12
-    sample = f"{n} of {w.batch} tokens per step (all topK rows each), fp64 C++ loops"
+            flops += flops_s
+    dt = sum(times)
+    value = flops / dt / 1e12
+    sample = f"{desc} per step, fp64 C++ loops"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": op.metric, "value": value, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**w.describe(), "sample_tokens": n},
+        "ms_per_step": dt / max(1, len(times)) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "op": args.op, "sample_units": n},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(cores, n),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -275,28 +389,22 @@ def run_ours(args):
 
     w = WORKLOADS[args.workload]
     inp = make_inputs(w, device=dev)
-    dt_code = pgg.dtype_code(inp.grad_y.dtype)
-    M, N, K, G = w.M, w.N, w.K, w.G
-    sizes = (M, N, K, G, M, w.batch, w.top_k)
-    ws_bytes = pgg.pgg_dx_workspace_size(*sizes, w.row_idx_type, dt_code)
-    plan = pgg.pgg_dx_plan(*sizes, w.row_idx_type, dt_code)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    out = torch.empty(w.batch, K, dtype=torch.float32, device=dev)
+    op = OPS[args.op](inp, pgg, dev)
+    plan, ws, ws_bytes, out = op.plan, op.ws, op.ws_bytes, op.out
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    ptrs = (inp.grad_y.data_ptr(), inp.weight.data_ptr(), inp.expanded_row_idx.data_ptr(),
-            inp.group_list.data_ptr())
+    va, vb = op.values()
+    idx, gl = inp.expanded_row_idx, inp.group_list
 
     def route_prep():
-        rc = pgg.pgg_dx_route_prep(ptrs[2], ptrs[3], *sizes, w.row_idx_type, dt_code,
-                                   ws.data_ptr(), ws_bytes, sp)
+        rc = pgg.pgg_dx_route_prep(idx.data_ptr(), gl.data_ptr(), *op.sizes, w.row_idx_type,
+                                   op.dt, ws.data_ptr(), ws_bytes, sp)
         if rc:
             raise pgg.PggError(rc, "route_prep")
 
     def gemm():
-        rc = pgg.pgg_dx_grouped_gemm(*ptrs, *sizes, w.row_idx_type, dt_code, ws.data_ptr(),
-                                     ws_bytes, out.data_ptr(), sp)
+        rc = op.stage2(va, vb, idx, gl, out, sp)
         if rc:
             raise pgg.PggError(rc, "grouped_gemm")
 
@@ -340,7 +448,7 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         mean_step, mean_gemm = float(t[0]), float(t[1])
 
-    flops, nbytes = algorithmic(inp)
+    flops, nbytes = op.algorithmic()
     value = world * flops / (mean_step * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
@@ -352,7 +460,7 @@ def run_ours(args):
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     simt = plan["variant"] == SIMT_VARIANT
-    kernel = "gmm_dx_simt_kernel" if simt else "gmm_dx_kernel"
+    kernel = op.kernel
     if simt:
         # FP32 pipes: SMs x FP32 lanes x 2 flops x the maximum SM clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -375,17 +483,16 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(inp, pgg, dt_code, sizes, w, ws, ws_bytes, dev, stream, flops, world,
-                          dist)
+        e2e = measure_e2e(op, pgg, w, dev, stream, flops, world, dist)
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": op.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded; routing and value recipe in DESIGN.md)",
         "config": {**w.describe(), "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "plan": plan},
+                   "plan": plan, **({"op": op.name} if op.name != "dx" else {})},
         "workspace_bytes": ws_bytes,
         "torch_alloc_delta_bytes": int(alloc_delta),
         "phases_ms": {"route_prep": statistics.mean(prep_ms), "grouped_gemm": mean_gemm},
@@ -401,41 +508,34 @@ def run_ours(args):
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(op, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
-def measure_e2e(inp, pgg, dt_code, sizes, w, ws, ws_bytes, dev, stream, flops, world, dist):
+def measure_e2e(op, pgg, w, dev, stream, flops, world, dist):
     """Same metric through the public call with host buffers: every step copies
-    the inputs from pinned host memory, runs pgg_dx_execute and copies d_x back."""
+    the inputs from pinned host memory, runs the execute call and copies the
+    result back."""
     import torch
-    h_dy = inp.grad_y.cpu().pin_memory()
-    h_w = inp.weight.cpu().pin_memory()
-    h_idx = inp.expanded_row_idx.cpu().pin_memory()
-    h_gl = inp.group_list.cpu().pin_memory()
-    h_out = torch.empty(w.batch, w.K, dtype=torch.float32).pin_memory()
-    d_dy = torch.empty_like(inp.grad_y)
-    d_w = torch.empty_like(inp.weight)
-    d_idx = torch.empty_like(inp.expanded_row_idx)
-    d_gl = torch.empty_like(inp.group_list)
-    d_out = torch.empty(w.batch, w.K, dtype=torch.float32, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (h_dy, h_w, h_idx, h_gl))
-    d2h = h_out.numel() * 4
+    va, vb = op.values()
+    inp = op.inp
+    hosts = [t.cpu().pin_memory() for t in (va, vb, inp.expanded_row_idx, inp.group_list)]
+    devs = [torch.empty_like(t) for t in (va, vb, inp.expanded_row_idx, inp.group_list)]
+    d_out = torch.empty_like(op.out)
+    h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hosts)
+    d2h = h_out.numel() * h_out.element_size()
     steps = 5
 
     def step():
-        d_dy.copy_(h_dy, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True)
-        d_gl.copy_(h_gl, non_blocking=True)
-        rc = pgg.pgg_dx_execute(d_dy.data_ptr(), d_w.data_ptr(), d_idx.data_ptr(),
-                                d_gl.data_ptr(), *sizes, w.row_idx_type, dt_code, ws.data_ptr(),
-                                ws_bytes, d_out.data_ptr(), stream.cuda_stream)
+        for d, h in zip(devs, hosts):
+            d.copy_(h, non_blocking=True)
+        rc = op.execute(*devs, d_out, stream.cuda_stream)
         if rc:
-            raise pgg.PggError(rc, "pgg_dx_execute")
+            raise pgg.PggError(rc, "execute")
         h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(2):

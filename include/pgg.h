@@ -271,6 +271,18 @@ int pgg_dw_execute(const void* x, const void* gradY, const int64_t* expandedRowI
                    pgg_stream_t stream);
 
 /*
+ * Second stage of pgg_dw_execute, exposed so that the kernel can be timed on
+ * its own: the weight-gradient kernel alone, on a workspace prepared by
+ * pgg_dx_route_prep with the same sizes and routing (the routing step is the
+ * same for both gradients). Same arguments and errors as pgg_dw_execute.
+ */
+int pgg_dw_grouped_gemm(const void* x, const void* gradY, const int64_t* expandedRowIdx,
+                        const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                        int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                        pgg_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                        void* dweight, pgg_stream_t stream);
+
+/*
  * How pgg_dw_execute runs these sizes with 16-byte aligned pointers: variant 0
  * (tensor cores: k_per_block = 128 output rows, 256 output columns, 64
  * reduction rows per stage) or 3 (FP32 pipes: 64 rows, 128 columns, 32 rows

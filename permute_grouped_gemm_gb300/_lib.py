@@ -68,9 +68,12 @@ def load(path: str | None = None):
             lib.pgg_dw_workspace_size.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(sz)]
             lib.pgg_dw_plan.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(PlanInfo)]
             lib.pgg_dw_execute.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz, vp, vp]
+            lib.pgg_dw_grouped_gemm.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz,
+                                                vp, vp]
             for f in ("pgg_dx_workspace_size", "pgg_dx_plan", "pgg_dx_execute",
                       "pgg_dx_grouped_gemm", "pgg_dx_route_prep", "pgg_dx_execute_static_scratch",
-                      "pgg_dw_workspace_size", "pgg_dw_plan", "pgg_dw_execute"):
+                      "pgg_dw_workspace_size", "pgg_dw_plan", "pgg_dw_execute",
+                      "pgg_dw_grouped_gemm"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.pgg_status_string.argtypes = [ctypes.c_int]
             lib.pgg_status_string.restype = ctypes.c_char_p
@@ -155,6 +158,14 @@ def pgg_dw_execute(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, to
     return load().pgg_dw_execute(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
                                  rowIdxType, dtype, out_dtype, workspace, workspace_bytes,
                                  dweight, stream)
+
+
+def pgg_dw_grouped_gemm(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                        rowIdxType, dtype, out_dtype, workspace, workspace_bytes, dweight,
+                        stream) -> int:
+    return load().pgg_dw_grouped_gemm(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch,
+                                      topK, rowIdxType, dtype, out_dtype, workspace,
+                                      workspace_bytes, dweight, stream)
 
 
 def pgg_status_string(code: int) -> str:

@@ -129,6 +129,53 @@ __device__ void dy_producer(uint8_t* smem, DwCtl* ctl, const CUtensorMap* tm_dy,
       ptx::mbar_wait(&ctl->full_b[s], (last_parity >> s) & 1u, lim, &no_abort);
 }
 
+// The sequence of (tile, first row) stages a CTA works through: tiles
+// blockIdx.x + j * gridDim.x, experts with no rows skipped, 64 rows a stage.
+struct StageIt {
+  uint32_t t;
+  int64_t r;
+  Tile x;
+  bool valid;
+};
+
+__device__ __forceinline__ void stage_seek(StageIt& s, const DwArgs& a, uint32_t total) {
+  while (s.t < total) {
+    s.x = tile_of(s.t, a);
+    if (s.r < s.x.m) {
+      s.valid = true;
+      return;
+    }
+    s.t += gridDim.x;
+    s.r = 0;
+  }
+  s.valid = false;
+}
+
+__device__ __forceinline__ StageIt stage_first(const DwArgs& a, uint32_t total) {
+  StageIt s;
+  s.t = blockIdx.x;
+  s.r = 0;
+  stage_seek(s, a, total);
+  return s;
+}
+
+__device__ __forceinline__ StageIt stage_next(StageIt s, const DwArgs& a, uint32_t total) {
+  if (!s.valid) return s;
+  s.r += kDwRows;
+  stage_seek(s, a, total);
+  return s;
+}
+
+// Tokens of this thread's 8 rows (rr0 + 8 j) of a stage; -1 past the expert's end.
+__device__ __forceinline__ void stage_tokens(const StageIt& s, const DwArgs& a, int rr0,
+                                             int32_t (&tok)[kDwRows / 8]) {
+#pragma unroll
+  for (int j = 0; j < kDwRows / 8; ++j) {
+    const int64_t r = s.r + rr0 + 8 * j;
+    tok[j] = (s.valid && r < s.x.m) ? a.rowinfo[s.x.row0 + r].token : -1;
+  }
+}
+
 template <int DT>
 __device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t total) {
   const uint64_t lim = a.wait_limit_ns;
@@ -142,42 +189,52 @@ __device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t 
   int pend[kGatherLag + 1];
   int npend = 0;
   bool failed = false;
-  for (uint32_t t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-    const Tile x = tile_of(t, a);
-    const int64_t k = x.k0 + kc * 8;
+  // The row tokens (the gather addresses) are loaded two stages ahead, so
+  // that their latency is not paid before every stage's copies.
+  StageIt cur = stage_first(a, total);
+  StageIt nxt = stage_next(cur, a, total);
+  int32_t tok0[kDwRows / 8], tok1[kDwRows / 8], tok2[kDwRows / 8];
+  stage_tokens(cur, a, rr0, tok0);
+  stage_tokens(nxt, a, rr0, tok1);
+  while (cur.valid) {
+    const StageIt nn = stage_next(nxt, a, total);
+    stage_tokens(nn, a, rr0, tok2);
+    if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
+      failed = true;
+      break;
+    }
+    const int64_t k = cur.x.k0 + kc * 8;
     const bool k_ok = k < a.K;
-    for (int64_t r = 0; r < x.m; r += kDwRows) {
-      if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
-        failed = true;
-        break;
-      }
-      const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes) + (kc >> 3) * kPanel;
+    const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes) + (kc >> 3) * kPanel;
 #pragma unroll
-      for (int j = 0; j < kDwRows / 8; ++j) {
-        const int rr = rr0 + 8 * j;
-        const bool ok = k_ok && r + rr < x.m;
-        const void* src = xb;
-        if (ok) {
-          const int64_t tok = a.rowinfo[x.row0 + r + rr].token;
-          src = xb + (tok * a.K + k) * 2;
-        }
-        ptx::cp_async_16(sa + rr * 128 + (((kc & 7) ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
-      }
-      ptx::cp_async_commit();
-      pend[npend++] = stage;
-      if (npend > kGatherLag) {
-        // the oldest stage's copies are complete: make them visible to the
-        // tensor cores, then report them
-        ptx::cp_async_wait<kGatherLag>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&ctl->full_a[pend[0]]);
-        for (int q = 0; q < kGatherLag; ++q) pend[q] = pend[q + 1];
-        --npend;
-      }
-      if (++stage == kDwStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    for (int j = 0; j < kDwRows / 8; ++j) {
+      const int rr = rr0 + 8 * j;
+      const bool ok = k_ok && tok0[j] >= 0;
+      const void* src = ok ? static_cast<const void*>(xb + (static_cast<int64_t>(tok0[j]) * a.K + k) * 2)
+                           : static_cast<const void*>(xb);
+      ptx::cp_async_16(sa + rr * 128 + (((kc & 7) ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
+    }
+    ptx::cp_async_commit();
+    pend[npend++] = stage;
+    if (npend > kGatherLag) {
+      // the oldest stage's copies are complete: make them visible to the
+      // tensor cores, then report them
+      ptx::cp_async_wait<kGatherLag>();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&ctl->full_a[pend[0]]);
+      for (int q = 0; q < kGatherLag; ++q) pend[q] = pend[q + 1];
+      --npend;
+    }
+    if (++stage == kDwStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    cur = nxt;
+    nxt = nn;
+#pragma unroll
+    for (int j = 0; j < kDwRows / 8; ++j) {
+      tok0[j] = tok1[j];
+      tok1[j] = tok2[j];
     }
   }
   ptx::cp_async_wait<0>();

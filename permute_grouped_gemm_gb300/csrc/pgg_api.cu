@@ -494,6 +494,19 @@ int pgg_dw_execute(const void* x, const void* gradY, const int64_t* expandedRowI
   return run_dw(plan, x, gradY, workspace, dweight, out_dtype, s);
 }
 
+int pgg_dw_grouped_gemm(const void* x, const void* gradY, const int64_t* expandedRowIdx,
+                        const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                        int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                        pgg_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                        void* dweight, pgg_stream_t stream) {
+  Plan plan;
+  int rc = check_dw(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType,
+                    dtype, out_dtype, workspace, workspace_bytes, dweight, &plan);
+  if (rc != PGG_OK) return rc;
+  return run_dw(plan, x, gradY, workspace, dweight, out_dtype,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char* pgg_status_string(int status) {
   switch (status) {
     case PGG_OK: return "ok";
