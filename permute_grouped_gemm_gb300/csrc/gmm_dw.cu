@@ -9,25 +9,33 @@
 // expanded_x is never materialised: its rows are gathered from x by token
 // while they are staged.
 //
-// Tile: one expert g, 128 output rows k (MMA M, tensor-memory lanes) x 256
-// output columns n (MMA N), reduced over the expert's rows 64 at a time. Both
-// operands are MN-major (the reduction index is the outer one in memory):
-//   A = x rows of the expert's tokens, 64 rows x 128 k, gathered with 16-byte
-//       cp.async by four producer warps into two 64-k panels of 128-byte rows
-//       in the 128-byte swizzle layout (rows past the expert's end read as 0);
-//   B = d_y rows of the expert, 64 rows x 256 n, by TMA: four 64-n boxes.
-// The accumulator (fp32, 256 columns, two buffers) is written by four
-// epilogue warps in the output dtype (the input dtype or fp32): each lane owns
-// one k and stores its row segment of n. Every output element is produced by
-// exactly one tile with a fixed order of MMAs, so the result is bitwise
-// repeatable. An expert with no rows gets zeros.
+// Tile: one expert g, 256 output rows k (MMA M) x 256 output columns n (MMA
+// N), on a pair of CTAs (a cluster of two; tcgen05 cta_group::2), reduced
+// over the expert's rows 64 at a time. CTA r owns k rows 128 r .. 128 r + 127
+// of the tile: their accumulators (fp32, 128 lanes x 256 columns, two
+// buffers) live in its tensor memory. Both operands are MN-major (the
+// reduction index is the outer one in memory):
+//   A = x rows of the expert's tokens: each CTA gathers its 128 k of the 64
+//       rows with 16-byte cp.async into two 64-k panels of 128-byte rows in the
+//       128-byte swizzle layout (rows past the expert's end read as 0), one
+//       producer warp per stage slot so that every slot can be in flight;
+//   B = d_y rows of the expert: each CTA loads its half of the 256 n (two
+//       64-n panels) by TMA, one copy through a 3-D view {64 n, rows, n / 64}
+//       when N is a multiple of 64, else one 2-D box per panel.
+// Per SM a stage is 32 KB, so six stages fit: enough tensor work buffered to
+// cover the round trip of a stage (MMA done -> slot free -> copies -> slot
+// full). The even CTA issues the MMAs; completions are multicast to both.
+// Every output element is produced by exactly one tile with a fixed order of
+// MMAs, so the result is bitwise repeatable. An expert with no rows gets
+// zeros. Four epilogue warps per CTA write the output dtype (the input dtype
+// or fp32): each lane owns one k and stores its row segment of n.
 //
-// Warp roles (320 threads): 0 TMA for d_y; 1 tensor-memory allocation and MMA
-// issue; 2-5 gather of x; 6-9 epilogue. Tiles are statically interleaved over
-// the persistent grid (tile = blockIdx.x + j * gridDim.x), so every role walks
-// the same list without a queue. Waits are bounded; when one runs out the
-// kernel records PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor
-// memory and returns.
+// Warp roles per CTA: 0 TMA for d_y; 1 tensor-memory allocation and (even
+// CTA) MMA issue; one gather warp per stage slot; four epilogue warps. Tiles
+// are statically interleaved over the clusters (tile = cluster + j *
+// clusters), so every role walks the same list without a queue. Waits are
+// bounded; when one runs out the kernel records PGG_ERR_TIMEOUT, drains its
+// copies and MMAs, frees tensor memory and returns.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,28 +48,28 @@
 namespace pgg {
 namespace {
 
-constexpr int kDwM = 128;      // output rows k per tile (MMA M)
+constexpr int kDwM = 128;      // output rows k per CTA (the pair's MMA M is 256)
 constexpr int kDwN = 256;      // output columns n per tile (MMA N)
 constexpr int kDwRows = 64;    // reduction rows per stage
-constexpr int kDwStages = 4;
+constexpr int kDwStages = 6;   // shared-memory stage slots, one gather warp each
 constexpr int kPanel = kDwRows * 128;            // one 64-element panel: 64 rows x 128 bytes
-constexpr int kABytes = 2 * kPanel;              // x: 128 k
-constexpr int kBBytes = 4 * kPanel;              // d_y: 256 n
+constexpr int kABytes = 2 * kPanel;              // x: this CTA's 128 k
+constexpr int kBBytes = 2 * kPanel;              // d_y: this CTA's 128 n
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kGatherThreads = 128;
-constexpr int kGatherLag = 2;                    // cp.async groups in flight per gather thread
-constexpr int kThreads = 320;
+constexpr int kGatherWarps = kDwStages;          // one per stage slot
+constexpr int kEpiWarp0 = 2 + kGatherWarps;      // first of the four epilogue warps
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kTmemCols = 512;                   // two 256-column accumulators
 constexpr int kAccCols = 256;
 
-static_assert(kGatherLag <= kDwStages - 1, "gather lag must leave a stage to the consumer");
+static_assert(kDwRows == 64, "the gather lane layout assumes 64 rows per stage");
 
 struct DwCtl {
-  uint64_t full_b[kDwStages];  // d_y copies landed (TMA transaction bytes)
-  uint64_t full_a[kDwStages];  // x gathered (128 arrivals)
-  uint64_t empty[kDwStages];   // MMAs of the stage done
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[kDwStages];    // even CTA: stage ready: d_y bytes of both CTAs (with the even
+                               // CTA's expect-tx arrival) and x gathered in both (two arrivals)
+  uint64_t empty[kDwStages];   // each CTA: MMAs of the stage done (multicast commit)
+  uint64_t tfull[2];           // each CTA: accumulator ready (multicast commit)
+  uint64_t tempty[2];          // even CTA: accumulator drained (4 warps x 2 CTAs)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -74,42 +82,65 @@ __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint3
 }
 
 struct Tile {
-  int64_t g, k0, n0, row0, m;
+  int64_t g, k0, n0, row0, m;  // k0: this CTA's first k; n0: the tile's first n
 };
 
-__device__ __forceinline__ Tile tile_of(uint32_t t, const DwArgs& a) {
+__device__ __forceinline__ Tile tile_of(uint32_t t, const DwArgs& a, uint32_t rank) {
   const uint32_t per_g = static_cast<uint32_t>(a.k_blocks) * static_cast<uint32_t>(a.n_blocks);
   Tile x;
   x.g = t / per_g;
   const uint32_t rem = t - static_cast<uint32_t>(x.g) * per_g;
-  x.k0 = static_cast<int64_t>(rem / a.n_blocks) * kDwM;
+  x.k0 = static_cast<int64_t>(rem / a.n_blocks) * (2 * kDwM) + kDwM * rank;
   x.n0 = static_cast<int64_t>(rem % a.n_blocks) * kDwN;
   x.row0 = a.off[x.g];
   x.m = a.off[x.g + 1] - x.row0;
   return x;
 }
 
+__device__ __forceinline__ uint32_t cluster_id() { return blockIdx.x >> 1; }
+__device__ __forceinline__ uint32_t n_clusters() { return gridDim.x >> 1; }
+
+// Bytes of d_y the CTA of `rank` stages for a tile starting at n0.
+__device__ __forceinline__ uint32_t b_bytes(const DwArgs& a, int64_t n0, uint32_t rank) {
+  const int64_t nc = n0 + 128 * rank;
+  if (a.dy_3d) return nc < a.N ? static_cast<uint32_t>(kBBytes) : 0u;
+  uint32_t b = 0;
+  for (int j = 0; j < 2; ++j) b += (nc + 64 * j < a.N) ? static_cast<uint32_t>(kPanel) : 0u;
+  return b;
+}
+
 __device__ void dy_producer(uint8_t* smem, DwCtl* ctl, const CUtensorMap* tm_dy, const DwArgs& a,
-                            uint32_t total) {
+                            uint32_t total, uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
+  const bool leader = rank == 0;
   int stage = 0;
   uint32_t phase = 0, outstanding = 0, last_parity = 0;
   bool failed = false;
-  for (uint32_t t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-    const Tile x = tile_of(t, a);
-    int boxes = 0;
-    for (int j = 0; j < kDwN / 64; ++j) boxes += (x.n0 + 64 * j < a.N) ? 1 : 0;
+  for (uint32_t t = cluster_id(); t < total && !failed; t += n_clusters()) {
+    const Tile x = tile_of(t, a, rank);
+    const uint32_t mine = b_bytes(a, x.n0, rank);
+    const uint32_t both = b_bytes(a, x.n0, 0) + b_bytes(a, x.n0, 1);
+    const int64_t nc = x.n0 + 128 * rank;
     for (int64_t r = 0; r < x.m; r += kDwRows) {
-      if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
+      if (!ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
         failed = true;
         break;
       }
       uint8_t* sb = smem + stage * kStageBytes + kABytes;
-      ptx::mbar_arrive_expect_tx(&ctl->full_b[stage], static_cast<uint32_t>(boxes * kPanel));
-      for (int j = 0; j < boxes; ++j)
-        ptx::tma_load_2d(sb + j * kPanel, tm_dy, &ctl->full_b[stage],
-                         static_cast<int32_t>(x.n0 + 64 * j), static_cast<int32_t>(x.row0 + r));
+      const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
+      if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], both);
+      if (mine) {
+        if (a.dy_3d) {
+          ptx::tma_load_3d_pair(sb, tm_dy, fb, 0, static_cast<int32_t>(x.row0 + r),
+                                static_cast<int32_t>(nc / 64));
+        } else {
+          for (int j = 0; j < 2; ++j)
+            if (nc + 64 * j < a.N)
+              ptx::tma_load_2d_pair(sb + j * kPanel, tm_dy, fb, static_cast<int32_t>(nc + 64 * j),
+                                    static_cast<int32_t>(x.row0 + r));
+        }
+      }
       outstanding |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == kDwStages) {
@@ -122,15 +153,19 @@ __device__ void dy_producer(uint8_t* smem, DwCtl* ctl, const CUtensorMap* tm_dy,
     ctl->abort = 1;
     raise_status(a.hdr, kStTimeout, 12);
   }
-  // Never leave while a copy into this CTA's shared memory may be in flight.
-  int no_abort = 0;
-  for (int s = 0; s < kDwStages; ++s)
-    if (outstanding & (1u << s))
-      ptx::mbar_wait(&ctl->full_b[s], (last_parity >> s) & 1u, lim, &no_abort);
+  // Never leave while a copy into either CTA's shared memory may be in flight:
+  // the even CTA's full barriers count both CTAs' bytes; the odd CTA is held
+  // by the cluster barrier at the end of the kernel.
+  if (leader) {
+    int no_abort = 0;
+    for (int s = 0; s < kDwStages; ++s)
+      if (outstanding & (1u << s))
+        ptx::mbar_wait_cluster(&ctl->full[s], (last_parity >> s) & 1u, lim, &no_abort);
+  }
 }
 
-// The sequence of (tile, first row) stages a CTA works through: tiles
-// blockIdx.x + j * gridDim.x, experts with no rows skipped, 64 rows a stage.
+// The sequence of (tile, first row) stages a CTA works through: its
+// cluster's tiles, experts with no rows skipped, 64 rows a stage.
 struct StageIt {
   uint32_t t;
   int64_t r;
@@ -138,111 +173,104 @@ struct StageIt {
   bool valid;
 };
 
-__device__ __forceinline__ void stage_seek(StageIt& s, const DwArgs& a, uint32_t total) {
+__device__ __forceinline__ void stage_seek(StageIt& s, const DwArgs& a, uint32_t total,
+                                           uint32_t rank) {
   while (s.t < total) {
-    s.x = tile_of(s.t, a);
+    if (s.r == 0) s.x = tile_of(s.t, a, rank);
     if (s.r < s.x.m) {
       s.valid = true;
       return;
     }
-    s.t += gridDim.x;
+    s.t += n_clusters();
     s.r = 0;
   }
   s.valid = false;
 }
 
-__device__ __forceinline__ StageIt stage_first(const DwArgs& a, uint32_t total) {
+__device__ __forceinline__ StageIt stage_first(const DwArgs& a, uint32_t total, uint32_t rank) {
   StageIt s;
-  s.t = blockIdx.x;
+  s.t = cluster_id();
   s.r = 0;
-  stage_seek(s, a, total);
+  stage_seek(s, a, total, rank);
   return s;
 }
 
-__device__ __forceinline__ StageIt stage_next(StageIt s, const DwArgs& a, uint32_t total) {
+__device__ __forceinline__ StageIt stage_next(StageIt s, const DwArgs& a, uint32_t total,
+                                              uint32_t rank) {
   if (!s.valid) return s;
   s.r += kDwRows;
-  stage_seek(s, a, total);
+  if (s.r >= s.x.m) {
+    s.t += n_clusters();
+    s.r = 0;
+  }
+  stage_seek(s, a, total, rank);
   return s;
 }
 
-// Tokens of this thread's 8 rows (rr0 + 8 j) of a stage; -1 past the expert's end.
-__device__ __forceinline__ void stage_tokens(const StageIt& s, const DwArgs& a, int rr0,
-                                             int32_t (&tok)[kDwRows / 8]) {
+// Tokens of rows `lane` and `lane + 32` of a stage; -1 past the expert's end.
+__device__ __forceinline__ void stage_tokens(const StageIt& s, const DwArgs& a, int lane,
+                                             int32_t (&tok)[2]) {
 #pragma unroll
-  for (int j = 0; j < kDwRows / 8; ++j) {
-    const int64_t r = s.r + rr0 + 8 * j;
-    tok[j] = (s.valid && r < s.x.m) ? a.rowinfo[s.x.row0 + r].token : -1;
+  for (int h = 0; h < 2; ++h) {
+    const int64_t r = s.r + lane + 32 * h;
+    tok[h] = (s.valid && r < s.x.m) ? a.rowinfo[s.x.row0 + r].token : -1;
   }
 }
 
+// Gather warp w fills shared-memory stage slot w: the stages w, w + S, ... of
+// the sequence. It issues the slot's 64 rows x 128 k as 16-byte cp.async
+// copies (32 per lane), waits for its own copies, makes them visible to the
+// tensor cores and reports the slot full to the even CTA; meanwhile the other
+// warps have their slots in flight. The tokens of the warp's next stage are
+// loaded while its copies are in flight.
 template <int DT>
-__device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t total) {
+__device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t total,
+                           uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
-  const int gt = threadIdx.x - 64;        // 0 .. 127
-  const int kc = gt & 15;                 // 16-byte chunk of the 128 k: 8 elements
-  const int rr0 = gt >> 4;                // rows rr0 + 8 j
+  const int w = (threadIdx.x >> 5) - 2;   // the warp's stage slot
+  const int lane = threadIdx.x & 31;
+  const int kc = lane & 15;               // 16-byte chunk of the 128 k: 8 elements
   const char* xb = static_cast<const char*>(a.x);
-  int stage = 0;
+  const uint32_t sa_slot = ptx::smem_addr(smem + w * kStageBytes) + (kc >> 3) * kPanel;
+  const uint32_t full = ptx::mapa(&ctl->full[w], 0);
   uint32_t phase = 0;
-  int pend[kGatherLag + 1];
-  int npend = 0;
   bool failed = false;
-  // The row tokens (the gather addresses) are loaded two stages ahead, so
-  // that their latency is not paid before every stage's copies.
-  StageIt cur = stage_first(a, total);
-  StageIt nxt = stage_next(cur, a, total);
-  int32_t tok0[kDwRows / 8], tok1[kDwRows / 8], tok2[kDwRows / 8];
-  stage_tokens(cur, a, rr0, tok0);
-  stage_tokens(nxt, a, rr0, tok1);
+  StageIt cur = stage_first(a, total, rank);
+  for (int i = 0; i < w; ++i) cur = stage_next(cur, a, total, rank);
+  int32_t tok[2];
+  stage_tokens(cur, a, lane, tok);
   while (cur.valid) {
-    const StageIt nn = stage_next(nxt, a, total);
-    stage_tokens(nn, a, rr0, tok2);
-    if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
+    StageIt nxt = cur;
+    for (int i = 0; i < kDwStages; ++i) nxt = stage_next(nxt, a, total, rank);
+    if (!ptx::mbar_wait_cluster(&ctl->empty[w], phase ^ 1u, lim, abort)) {
       failed = true;
       break;
     }
     const int64_t k = cur.x.k0 + kc * 8;
     const bool k_ok = k < a.K;
-    const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes) + (kc >> 3) * kPanel;
 #pragma unroll
-    for (int j = 0; j < kDwRows / 8; ++j) {
-      const int rr = rr0 + 8 * j;
-      const bool ok = k_ok && tok0[j] >= 0;
-      const void* src = ok ? static_cast<const void*>(xb + (static_cast<int64_t>(tok0[j]) * a.K + k) * 2)
+    for (int j = 0; j < kDwRows / 2; ++j) {
+      const int rr = (lane >> 4) + 2 * j;  // row of the stage this copy fills
+      const int32_t t = __shfl_sync(0xFFFFFFFFu, tok[rr >> 5], rr & 31);
+      const bool ok = k_ok && t >= 0;
+      const void* src = ok ? static_cast<const void*>(xb + (static_cast<int64_t>(t) * a.K + k) * 2)
                            : static_cast<const void*>(xb);
-      ptx::cp_async_16(sa + rr * 128 + (((kc & 7) ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
+      ptx::cp_async_16(sa_slot + rr * 128 + (((kc & 7) ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
     }
     ptx::cp_async_commit();
-    pend[npend++] = stage;
-    if (npend > kGatherLag) {
-      // the oldest stage's copies are complete: make them visible to the
-      // tensor cores, then report them
-      ptx::cp_async_wait<kGatherLag>();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&ctl->full_a[pend[0]]);
-      for (int q = 0; q < kGatherLag; ++q) pend[q] = pend[q + 1];
-      --npend;
-    }
-    if (++stage == kDwStages) {
-      stage = 0;
-      phase ^= 1u;
-    }
+    stage_tokens(nxt, a, lane, tok);
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_remote(full);
+    phase ^= 1u;
     cur = nxt;
-    nxt = nn;
-#pragma unroll
-    for (int j = 0; j < kDwRows / 8; ++j) {
-      tok0[j] = tok1[j];
-      tok1[j] = tok2[j];
-    }
   }
   ptx::cp_async_wait<0>();
-  ptx::fence_proxy_async_smem();
-  for (int q = 0; q < npend; ++q) ptx::mbar_arrive(&ctl->full_a[pend[q]]);
   if (failed) {
     ctl->abort = 1;
-    raise_status(a.hdr, kStTimeout, 13);
+    if (lane == 0) raise_status(a.hdr, kStTimeout, 13);
   }
 }
 
@@ -250,24 +278,23 @@ template <int DT>
 __device__ void mma_issuer(uint8_t* smem, DwCtl* ctl, uint32_t tmem_base, const DwArgs& a,
                            uint32_t total) {
   constexpr uint32_t kFmt = DT == PGG_BF16 ? 1u : 0u;
-  constexpr uint32_t idesc = ptx::idesc_make_mn(kFmt, kDwM, kDwN);
+  constexpr uint32_t idesc = ptx::idesc_make_mn(kFmt, 2 * kDwM, kDwN);
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   int stage = 0, acc = 0;
   uint32_t phase = 0, aph = 0;
   bool issued = false, failed = false;
-  for (uint32_t t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-    const Tile x = tile_of(t, a);
+  for (uint32_t t = cluster_id(); t < total && !failed; t += n_clusters()) {
+    const Tile x = tile_of(t, a, 0);
     if (x.m == 0) continue;
-    if (!ptx::mbar_wait(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
+    if (!ptx::mbar_wait_cluster(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
       failed = true;
       break;
     }
     ptx::tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
     for (int64_t r = 0; r < x.m; r += kDwRows) {
-      if (!ptx::mbar_wait(&ctl->full_b[stage], phase, lim, abort) ||
-          !ptx::mbar_wait(&ctl->full_a[stage], phase, lim, abort)) {
+      if (!ptx::mbar_wait_cluster(&ctl->full[stage], phase, lim, abort)) {
         failed = true;
         break;
       }
@@ -279,17 +306,17 @@ __device__ void mma_issuer(uint8_t* smem, DwCtl* ctl, uint32_t tmem_base, const 
       const int nks = left >= kDwRows ? kDwRows / 16 : static_cast<int>((left + 15) / 16);
       for (int ks = 0; ks < nks; ++ks) {
         const uint64_t koff = static_cast<uint64_t>((ks * 16 * 128) >> 4);
-        ptx::mma_f16(d_tmem, da + koff, db + koff, idesc, (r > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_f16_pair(d_tmem, da + koff, db + koff, idesc, (r > 0 || ks > 0) ? 1u : 0u);
       }
       issued = true;
-      ptx::mma_commit(&ctl->empty[stage]);
+      ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
       if (++stage == kDwStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (failed) break;
-    ptx::mma_commit(&ctl->tfull[acc]);
+    ptx::mma_commit_pair(&ctl->tfull[acc], 0x3);
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
@@ -300,7 +327,7 @@ __device__ void mma_issuer(uint8_t* smem, DwCtl* ctl, uint32_t tmem_base, const 
   if (issued) {
     // Tensor memory is released only after every issued MMA has completed.
     int no_abort = 0;
-    ptx::mma_commit(&ctl->drain);
+    ptx::mma_commit_pair(&ctl->drain, 0x1);
     ptx::mbar_wait(&ctl->drain, 0u, lim, &no_abort);
   }
 }
@@ -324,16 +351,19 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* v) {
 }
 
 template <int DT>
-__device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32_t total) {
+__device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32_t total,
+                         uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31 are this warp's
   const bool f32 = a.out_f32 != 0;
+  const uint32_t tempty0 = ptx::mapa(&ctl->tempty[0], 0);
+  const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   int acc = 0;
   uint32_t aph = 0;
-  for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
-    const Tile x = tile_of(t, a);
+  for (uint32_t t = cluster_id(); t < total; t += n_clusters()) {
+    const Tile x = tile_of(t, a, rank);
     const int64_t k = x.k0 + 32 * quarter + lane;
     const bool k_ok = k < a.K;
     const int64_t base = (x.g * a.K + k) * a.N + x.n0;
@@ -349,7 +379,7 @@ __device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32
       }
       continue;
     }
-    const bool ok = ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
+    const bool ok = ptx::mbar_wait_cluster(&ctl->tfull[acc], aph, lim, abort);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
       if (lane == 0) {
         ctl->abort = 1;
@@ -383,7 +413,7 @@ __device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ctl->tempty[acc]);
+    if (lane == 0) ptx::mbar_arrive_remote(acc ? tempty1 : tempty0);
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
@@ -397,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   auto* ctl = reinterpret_cast<DwCtl*>(smem + kDwStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
 
-  // Routing validation failed: the result is defined as zeros.
+  // Routing validation failed: the result is defined as zeros. (Both CTAs of
+  // a pair see the same status and leave before any cluster operation.)
   const uint32_t st = a.hdr->status;
   if (st == kStIndex || st == kStGroupSum || st == kStNotPerm) {
     const int64_t n = a.G * a.K * a.N;
@@ -416,13 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDwStages; ++s) {
-      ptx::mbar_init(&ctl->full_b[s], 1);
-      ptx::mbar_init(&ctl->full_a[s], kGatherThreads);
+      ptx::mbar_init(&ctl->full[s], 3);
       ptx::mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->tfull[b], 1);
-      ptx::mbar_init(&ctl->tempty[b], 4);
+      ptx::mbar_init(&ctl->tempty[b], 8);
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -430,40 +461,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) ptx::tma_prefetch_desc(&tm_dy);
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers are initialised
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) dy_producer(smem, ctl, &tm_dy, a, total);
+    if (lane == 0) dy_producer(smem, ctl, &tm_dy, a, total, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<DT>(smem, ctl, tmem_base, a, total);
-  } else if (warp < 6) {
-    x_gatherer<DT>(smem, ctl, a, total);
+    if (lane == 0 && rank == 0) mma_issuer<DT>(smem, ctl, tmem_base, a, total);
+  } else if (warp < kEpiWarp0) {
+    x_gatherer<DT>(smem, ctl, a, total, rank);
   } else {
-    epilogue<DT>(ctl, tmem_base, a, total);
+    epilogue<DT>(ctl, tmem_base, a, total, rank);
   }
 
   ptx::tc_fence_before_sync();
   __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still use it
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
 }  // namespace
 
 int dw_smem_bytes() { return kSmemBytes; }
+int dw_stage_rows() { return kDwRows; }
 int dw_threads() { return kThreads; }
 
-// Tiles of 128 k x 256 n per expert.
+// Tiles of 256 k (a CTA pair) x 256 n per expert.
 void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks) {
-  *k_blocks = static_cast<int>((K + kDwM - 1) / kDwM);
+  *k_blocks = static_cast<int>((K + 2 * kDwM - 1) / (2 * kDwM));
   *n_blocks = static_cast<int>((N + kDwN - 1) / kDwN);
 }
 
@@ -479,10 +513,27 @@ cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int 
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
   if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const int64_t total = a.G * a.k_blocks * a.n_blocks;
-  const int64_t grid = total < num_sms ? total : num_sms;
-  kern<<<static_cast<unsigned>(grid < 1 ? 1 : grid), kThreads, kSmemBytes, stream>>>(tm_dy, a);
-  return cudaGetLastError();
+  int64_t want = total < num_sms / 2 ? total : num_sms / 2;
+  if (want < 1) want = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * want), 1, 1);
+  int clusters = 0;
+  err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (err != cudaSuccess) return err;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, tm_dy, a);
 }
 
 }  // namespace pgg

@@ -28,6 +28,7 @@ cudaError_t launch_simt(int dtype, const SimtArgs& a, int64_t max_tiles, int num
                         cudaStream_t stream);
 int dw_smem_bytes();
 int dw_threads();
+int dw_stage_rows();
 void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
 cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int num_sms,
                       cudaStream_t stream);
@@ -334,20 +335,37 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
   a.G = plan.G;
   a.batch = plan.batch;
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
+  a.dy_3d = 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   if (dw_tensor_path(plan.dtype, plan.N, plan.K, x, gradY, dweight)) {
     dw_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PGG_ERR_CUDA;
     CUtensorMap tm;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(plan.N) * 2};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t estr[2] = {1, 1};
-    if (enc(&tm, tmap_type(plan.dtype), 2, const_cast<void*>(gradY), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PGG_ERR_CUDA;
+    const cuuint32_t rows = static_cast<cuuint32_t>(dw_stage_rows());
+    CUresult cr;
+    a.dy_3d = plan.N % 64 == 0 ? 1 : 0;
+    if (a.dy_3d) {
+      // {64 n, rows, n-chunk}: a box of 4 chunks lands as four 64-n panels;
+      // chunks past N / 64 read as zero
+      cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(plan.M),
+                            static_cast<cuuint64_t>(plan.N / 64)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(plan.N) * 2, 128};
+      cuuint32_t box[3] = {64, rows, 2};  // one CTA's half of the tile's 256 n
+      cuuint32_t estr[3] = {1, 1, 1};
+      cr = enc(&tm, tmap_type(plan.dtype), 3, const_cast<void*>(gradY), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      cuuint64_t dims[2] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.M)};
+      cuuint64_t strides[1] = {static_cast<cuuint64_t>(plan.N) * 2};
+      cuuint32_t box[2] = {64, rows};
+      cuuint32_t estr[2] = {1, 1};
+      cr = enc(&tm, tmap_type(plan.dtype), 2, const_cast<void*>(gradY), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (cr != CUDA_SUCCESS) return PGG_ERR_CUDA;
     return launch_dw(plan.dtype, tm, a, di.num_sms, stream) == cudaSuccess ? PGG_OK : PGG_ERR_CUDA;
   }
   dw_simt_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
@@ -458,9 +476,10 @@ int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   if (tc) {
     dw_tiles(K, N, &kb, &nb);
     info->variant = 0;
-    info->rows_per_block = 64;
-    info->k_per_block = 128;
-    info->stages = 4;
+    info->rows_per_block = dw_stage_rows();
+    info->k_per_block = 256;
+    info->stages = dw_smem_bytes() / (dw_stage_rows() * 4 * 128);
+    info->cta_pair = 1;
     info->threads = dw_threads();
     info->smem_bytes = dw_smem_bytes();
   } else {

@@ -123,6 +123,7 @@ struct DwArgs {
   int32_t k_blocks;  // output rows (k) blocks per expert
   int32_t n_blocks;  // output column (n) blocks per expert
   int32_t out_f32;   // 1: out is fp32; 0: out has the input dtype
+  int32_t dy_3d;     // tensor-core kernel: d_y map is 3-D {64 n, rows, n / 64} (N % 64 == 0)
   uint64_t wait_limit_ns;
 };
 

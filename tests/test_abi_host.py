@@ -144,8 +144,9 @@ def test_weight_gradient_plan_and_host_errors(lib):
     a = LARGE
     sizes = (a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"], a["topK"], 0)
     p = pgg.pgg_dw_plan(*sizes, pgg.PGG_BF16)
-    assert p["variant"] == 0 and p["k_per_block"] == 128 and p["threads"] == 320
-    assert p["k_blocks"] == 56 and p["band_k_blocks"] == 8 and p["smem_bytes"] <= 227 * 1024
+    assert p["variant"] == 0 and p["k_per_block"] == 256 and p["threads"] % 32 == 0
+    assert p["cta_pair"] == 1 and p["stages"] == 6
+    assert p["k_blocks"] == 28 and p["band_k_blocks"] == 8 and p["smem_bytes"] <= 227 * 1024
     assert pgg.pgg_dw_plan(*sizes, pgg.PGG_F32)["variant"] == 3
     assert pgg.pgg_dw_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
                            pgg.PGG_BF16)["variant"] == 3
