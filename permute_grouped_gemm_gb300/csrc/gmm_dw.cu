@@ -28,7 +28,7 @@
 // Every output element is produced by exactly one tile with a fixed order of
 // MMAs, so the result is bitwise repeatable. An expert with no rows gets
 // zeros. Four epilogue warps per CTA write the output dtype (the input dtype
-// or fp32): each lane owns one k and stores its row segment of n.
+// or fp32) through shared memory with TMA stores.
 //
 // Warp roles per CTA: 0 TMA for d_y; 1 tensor-memory allocation and (even
 // CTA) MMA issue; one gather warp per stage slot; four epilogue warps. Tiles
@@ -61,6 +61,8 @@ constexpr int kEpiWarp0 = 2 + kGatherWarps;      // first of the four epilogue w
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);
 constexpr int kTmemCols = 512;                   // two 256-column accumulators
 constexpr int kAccCols = 256;
+constexpr int kOutBuf = 32 * 128;                // epilogue staging: 32 rows x 128 bytes
+constexpr int kOutBytes = 4 * 2 * kOutBuf;       // four epilogue warps, two buffers each
 
 static_assert(kDwRows == 64, "the gather lane layout assumes 64 rows per stage");
 
@@ -75,7 +77,9 @@ struct DwCtl {
   int abort;
 };
 
-constexpr int kSmemBytes = kDwStages * kStageBytes + static_cast<int>(sizeof(DwCtl)) + 1024;
+constexpr int kSmemBytes =
+    kDwStages * kStageBytes + kOutBytes + static_cast<int>(sizeof(DwCtl)) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint32_t site) {
   if (atomicCAS(&hdr->status, 0u, code) == 0u) hdr->timeout_site = site;
@@ -350,25 +354,49 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* v) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Rows of 128 bytes of the output chunk: 64 values of the 16-bit dtype or 32
+// of fp32, converted from the accumulator words v.
 template <int DT>
-__device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32_t total,
-                         uint32_t rank) {
+__device__ __forceinline__ void stage_row(uint8_t* buf, int row, const uint32_t* v, bool f32) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    uint4 q;
+    if (f32)
+      q = make_uint4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+    else
+      q = pack8<DT>(v + 8 * p);
+    // 128-byte swizzle: 16-byte piece p of row r sits at piece p ^ (r % 8)
+    *reinterpret_cast<uint4*>(buf + row * 128 + ((p ^ (row & 7)) << 4)) = q;
+  }
+}
+
+// Each epilogue warp owns 32 accumulator lanes (k) of its CTA. Per tile it
+// reads the accumulator in chunks of 128 bytes per row (64 columns of a
+// 16-bit output, 32 of fp32), converts them into a shared-memory buffer in
+// the 128-byte swizzle layout and writes the 32 x 128-byte box with one TMA
+// store (rows past K and columns past N are clipped by the tensor map), two
+// buffers per warp so the next chunk is staged while a store reads the last.
+template <int DT>
+__device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CUtensorMap* tm_out,
+                         const DwArgs& a, uint32_t total, uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31 are this warp's
   const bool f32 = a.out_f32 != 0;
+  const int cols = f32 ? 32 : 64;  // output columns per 128-byte chunk
+  uint8_t* bufs = obuf + (warp - kEpiWarp0) * 2 * kOutBuf;
   const uint32_t tempty0 = ptx::mapa(&ctl->tempty[0], 0);
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
-  int acc = 0;
+  int acc = 0, nb = 0;
   uint32_t aph = 0;
   for (uint32_t t = cluster_id(); t < total; t += n_clusters()) {
     const Tile x = tile_of(t, a, rank);
     const int64_t k = x.k0 + 32 * quarter + lane;
     const bool k_ok = k < a.K;
-    const int64_t base = (x.g * a.K + k) * a.N + x.n0;
     if (x.m == 0) {
       if (k_ok) {
+        const int64_t base = (x.g * a.K + k) * a.N + x.n0;
         if (f32) {
           float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + base);
           for (int c = 0; c < kDwN / 4 && x.n0 + 4 * c < a.N; ++c) o[c] = make_float4(0, 0, 0, 0);
@@ -390,26 +418,30 @@ __device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32
     ptx::tc_fence_after_sync();
     const uint32_t t_lane =
         tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(acc * kAccCols);
+    const int32_t k_row = static_cast<int32_t>(x.k0 + 32 * quarter);
 #pragma unroll 1
-    for (int c = 0; c < kDwN / 32; ++c) {
-      uint32_t v[32];
-      ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(32 * c), v);
+    for (int c0 = 0; c0 < kDwN && x.n0 + c0 < a.N; c0 += cols) {
+      uint32_t v[64];
+      ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0),
+                              *reinterpret_cast<uint32_t(*)[32]>(v));
+      if (!f32)
+        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0 + 32),
+                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       ptx::tmem_ld_wait();
-      const int64_t n = x.n0 + 32 * c;
-      if (!k_ok || n >= a.N) continue;
-      if (f32) {
-        float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + base + 32 * c);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (n + 4 * q < a.N)
-            o[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-      } else {
-        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + base + 32 * c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (n + 8 * q < a.N) o[q] = pack8<DT>(v + 8 * q);
+      uint8_t* buf = bufs + (nb & 1) * kOutBuf;
+      // the store issued two chunks ago read this buffer: wait for it
+      if (lane == 0) ptx::bulk_wait_read<1>();
+      __syncwarp();
+      stage_row<DT>(buf, lane, v, f32);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (k_row < a.K)
+          ptx::tma_store_3d(tm_out, buf, static_cast<int32_t>(x.n0 + c0), k_row,
+                            static_cast<int32_t>(x.g));
+        ptx::bulk_commit();
       }
+      ++nb;
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
@@ -417,15 +449,19 @@ __device__ void epilogue(DwCtl* ctl, uint32_t tmem_base, const DwArgs& a, uint32
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
+  if (lane == 0) ptx::bulk_wait<0>();
+  __syncwarp();
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gmm_dw_kernel(const __grid_constant__ CUtensorMap tm_dy, const DwArgs a) {
+    gmm_dw_kernel(const __grid_constant__ CUtensorMap tm_dy,
+                  const __grid_constant__ CUtensorMap tm_out, const DwArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  auto* ctl = reinterpret_cast<DwCtl*>(smem + kDwStages * kStageBytes);
+  uint8_t* obuf = smem + kDwStages * kStageBytes;
+  auto* ctl = reinterpret_cast<DwCtl*>(obuf + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
@@ -459,7 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) ptx::tma_prefetch_desc(&tm_dy);
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_dy);
+    ptx::tma_prefetch_desc(&tm_out);
+  }
   if (warp == 1) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
     ptx::tmem_relinquish_pair();
@@ -477,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     x_gatherer<DT>(smem, ctl, a, total, rank);
   } else {
-    epilogue<DT>(ctl, tmem_base, a, total, rank);
+    epilogue<DT>(obuf, ctl, tmem_base, &tm_out, a, total, rank);
   }
 
   ptx::tc_fence_before_sync();
@@ -501,9 +540,9 @@ void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks) {
   *n_blocks = static_cast<int>((N + kDwN - 1) / kDwN);
 }
 
-cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int num_sms,
-                      cudaStream_t stream) {
-  void (*kern)(const CUtensorMap, const DwArgs) = nullptr;
+cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const CUtensorMap& tm_out,
+                      const DwArgs& a, int num_sms, cudaStream_t stream) {
+  void (*kern)(const CUtensorMap, const CUtensorMap, const DwArgs) = nullptr;
   if (dtype == PGG_BF16)
     kern = gmm_dw_kernel<PGG_BF16>;
   else if (dtype == PGG_F16)
@@ -533,7 +572,7 @@ cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int 
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_dy, a);
+  return cudaLaunchKernelEx(&cfg, kern, tm_dy, tm_out, a);
 }
 
 }  // namespace pgg

@@ -30,8 +30,8 @@ int dw_smem_bytes();
 int dw_threads();
 int dw_stage_rows();
 void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
-cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const DwArgs& a, int num_sms,
-                      cudaStream_t stream);
+cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const CUtensorMap& tm_out,
+                      const DwArgs& a, int num_sms, cudaStream_t stream);
 void dw_simt_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
 int dw_simt_smem_bytes();
 cudaError_t launch_dw_simt(int dtype, const DwArgs& a, int vec, int num_sms, cudaStream_t stream);
@@ -366,7 +366,24 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (cr != CUDA_SUCCESS) return PGG_ERR_CUDA;
-    return launch_dw(plan.dtype, tm, a, di.num_sms, stream) == cudaSuccess ? PGG_OK : PGG_ERR_CUDA;
+    // the output [G, K, N] as a 3-D map, boxes of 128 bytes x 32 rows of k
+    CUtensorMap tm_out;
+    {
+      const int oes = out_dtype == PGG_F32 ? 4 : 2;
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.K),
+                            static_cast<cuuint64_t>(plan.G)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(plan.N) * oes,
+                               static_cast<cuuint64_t>(plan.N) * static_cast<cuuint64_t>(plan.K) *
+                                   oes};
+      cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / oes), 32, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (enc(&tm_out, tmap_type(out_dtype), 3, dweight, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PGG_ERR_CUDA;
+    }
+    return launch_dw(plan.dtype, tm, tm_out, a, di.num_sms, stream) == cudaSuccess ? PGG_OK
+                                                                                   : PGG_ERR_CUDA;
   }
   dw_simt_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
   const uintptr_t vec_align = out_dtype == PGG_F32 ? 16 : 8;
