@@ -27,11 +27,11 @@
 // full). The even CTA issues the MMAs; completions are multicast to both.
 // Every output element is produced by exactly one tile with a fixed order of
 // MMAs, so the result is bitwise repeatable. An expert with no rows gets
-// zeros. Four epilogue warps per CTA write the output dtype (the input dtype
-// or fp32) through shared memory with TMA stores.
+// zeros. The epilogue warps write the output dtype (the input dtype or fp32)
+// through shared memory with TMA stores.
 //
 // Warp roles per CTA: 0 TMA for d_y; 1 tensor-memory allocation and (even
-// CTA) MMA issue; one gather warp per stage slot; four epilogue warps. Tiles
+// CTA) MMA issue; one gather warp per stage slot; eight epilogue warps. Tiles
 // are statically interleaved over the clusters (tile = cluster + j *
 // clusters), so every role walks the same list without a queue. Waits are
 // bounded; when one runs out the kernel records PGG_ERR_TIMEOUT, drains its
@@ -57,12 +57,14 @@ constexpr int kABytes = 2 * kPanel;              // x: this CTA's 128 k
 constexpr int kBBytes = 2 * kPanel;              // d_y: this CTA's 128 n
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kGatherWarps = kDwStages;          // one per stage slot
-constexpr int kEpiWarp0 = 2 + kGatherWarps;      // first of the four epilogue warps
-constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+constexpr int kEpiWarps = 8;                     // 4: one per lane quarter; 8: also split n in two
+constexpr int kOutBufs = 1;                      // staging buffers per epilogue warp
+constexpr int kEpiWarp0 = 2 + kGatherWarps;      // first epilogue warp
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;                   // two 256-column accumulators
 constexpr int kAccCols = 256;
 constexpr int kOutBuf = 32 * 128;                // epilogue staging: 32 rows x 128 bytes
-constexpr int kOutBytes = 4 * 2 * kOutBuf;       // four epilogue warps, two buffers each
+constexpr int kOutBytes = kEpiWarps * kOutBufs * kOutBuf;
 
 static_assert(kDwRows == 64, "the gather lane layout assumes 64 rows per stage");
 
@@ -71,7 +73,7 @@ struct DwCtl {
                                // CTA's expect-tx arrival) and x gathered in both (two arrivals)
   uint64_t empty[kDwStages];   // each CTA: MMAs of the stage done (multicast commit)
   uint64_t tfull[2];           // each CTA: accumulator ready (multicast commit)
-  uint64_t tempty[2];          // even CTA: accumulator drained (4 warps x 2 CTAs)
+  uint64_t tempty[2];          // even CTA: accumulator drained (epilogue warps x 2 CTAs)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -370,12 +372,12 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int row, const uint32_t*
   }
 }
 
-// Each epilogue warp owns 32 accumulator lanes (k) of its CTA. Per tile it
-// reads the accumulator in chunks of 128 bytes per row (64 columns of a
-// 16-bit output, 32 of fp32), converts them into a shared-memory buffer in
-// the 128-byte swizzle layout and writes the 32 x 128-byte box with one TMA
-// store (rows past K and columns past N are clipped by the tensor map), two
-// buffers per warp so the next chunk is staged while a store reads the last.
+// Each epilogue warp owns 32 accumulator lanes (k) of its CTA and, with eight
+// warps, half of the tile's columns. Per tile it reads the accumulator in
+// chunks of 128 bytes per row (64 columns of a 16-bit output, 32 of fp32),
+// converts them into a shared-memory buffer in the 128-byte swizzle layout
+// and writes the 32 x 128-byte box with one TMA store (rows past K and
+// columns past N are clipped by the tensor map).
 template <int DT>
 __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CUtensorMap* tm_out,
                          const DwArgs& a, uint32_t total, uint32_t rank) {
@@ -383,9 +385,12 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31 are this warp's
+  const int e = warp - kEpiWarp0;
+  const int span = kDwN / (kEpiWarps / 4);      // accumulator columns this warp writes
+  const int col0 = (e / 4) * span;
   const bool f32 = a.out_f32 != 0;
   const int cols = f32 ? 32 : 64;  // output columns per 128-byte chunk
-  uint8_t* bufs = obuf + (warp - kEpiWarp0) * 2 * kOutBuf;
+  uint8_t* bufs = obuf + e * kOutBufs * kOutBuf;
   const uint32_t tempty0 = ptx::mapa(&ctl->tempty[0], 0);
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   int acc = 0, nb = 0;
@@ -396,13 +401,14 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
     const bool k_ok = k < a.K;
     if (x.m == 0) {
       if (k_ok) {
-        const int64_t base = (x.g * a.K + k) * a.N + x.n0;
+        const int64_t n0 = x.n0 + col0;
+        const int64_t base = (x.g * a.K + k) * a.N + n0;
         if (f32) {
           float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + base);
-          for (int c = 0; c < kDwN / 4 && x.n0 + 4 * c < a.N; ++c) o[c] = make_float4(0, 0, 0, 0);
+          for (int c = 0; c < span / 4 && n0 + 4 * c < a.N; ++c) o[c] = make_float4(0, 0, 0, 0);
         } else {
           uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + base);
-          for (int c = 0; c < kDwN / 8 && x.n0 + 8 * c < a.N; ++c) o[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < span / 8 && n0 + 8 * c < a.N; ++c) o[c] = make_uint4(0, 0, 0, 0);
         }
       }
       continue;
@@ -420,7 +426,7 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
         tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(acc * kAccCols);
     const int32_t k_row = static_cast<int32_t>(x.k0 + 32 * quarter);
 #pragma unroll 1
-    for (int c0 = 0; c0 < kDwN && x.n0 + c0 < a.N; c0 += cols) {
+    for (int c0 = col0; c0 < col0 + span && x.n0 + c0 < a.N; c0 += cols) {
       uint32_t v[64];
       ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0),
                               *reinterpret_cast<uint32_t(*)[32]>(v));
@@ -428,9 +434,9 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
         ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0 + 32),
                                 *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       ptx::tmem_ld_wait();
-      uint8_t* buf = bufs + (nb & 1) * kOutBuf;
-      // the store issued two chunks ago read this buffer: wait for it
-      if (lane == 0) ptx::bulk_wait_read<1>();
+      uint8_t* buf = bufs + (nb % kOutBufs) * kOutBuf;
+      // the store issued kOutBufs chunks ago read this buffer: wait for it
+      if (lane == 0) ptx::bulk_wait_read<kOutBufs - 1>();
       __syncwarp();
       stage_row<DT>(buf, lane, v, f32);
       ptx::fence_proxy_async_smem();
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl->tfull[b], 1);
-      ptx::mbar_init(&ctl->tempty[b], 8);
+      ptx::mbar_init(&ctl->tempty[b], 2 * kEpiWarps);
     }
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -532,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int dw_smem_bytes() { return kSmemBytes; }
 int dw_stage_rows() { return kDwRows; }
+int dw_stages() { return kDwStages; }
 int dw_threads() { return kThreads; }
 
 // Tiles of 256 k (a CTA pair) x 256 n per expert.

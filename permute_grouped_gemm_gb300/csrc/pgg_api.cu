@@ -29,6 +29,7 @@ cudaError_t launch_simt(int dtype, const SimtArgs& a, int64_t max_tiles, int num
 int dw_smem_bytes();
 int dw_threads();
 int dw_stage_rows();
+int dw_stages();
 void dw_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
 cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const CUtensorMap& tm_out,
                       const DwArgs& a, int num_sms, cudaStream_t stream);
@@ -495,7 +496,7 @@ int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
     info->variant = 0;
     info->rows_per_block = dw_stage_rows();
     info->k_per_block = 256;
-    info->stages = dw_smem_bytes() / (dw_stage_rows() * 4 * 128);
+    info->stages = dw_stages();
     info->cta_pair = 1;
     info->threads = dw_threads();
     info->smem_bytes = dw_smem_bytes();
