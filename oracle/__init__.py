@@ -1,4 +1,5 @@
-"""Oracle for the MoE permute + grouped-matmul backward: d_x and d_weight.
+"""Oracle for the MoE permute + grouped matmul: the backward (d_x, d_weight)
+and the forward y it differentiates.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package. The product path
@@ -86,6 +87,9 @@ def load_library(path: str):
     lib.oracle_dw.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64,
                               i64, i64, ctypes.c_int, vp, vp, i64, dp, ctypes.c_int]
     lib.oracle_dw.restype = ctypes.c_int
+    lib.oracle_fwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64,
+                               i64, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
+    lib.oracle_fwd.restype = ctypes.c_int
     return lib
 
 
@@ -213,6 +217,39 @@ def dw(x, grad_y, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_
     if rc != 0:
         raise OracleError(rc)
     return out.reshape(G, K, N) if sel is None else out
+
+
+def fwd(x, weight, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_type: int,
+        rows=None, nthreads: int = 0, lib=None) -> np.ndarray:
+    """fp64 forward y [M, N] in expanded order (or the listed ``rows``):
+    y[i] = x[batch(i)] @ weight[g(i)]. x: [batch, K], weight: [G, K, N], same
+    dtype."""
+    lib = lib or _load()
+    xr, dt = _raw(x)
+    w, dtw = _raw(weight)
+    if dt != dtw:
+        raise OracleError(4)
+    B, K = xr.shape
+    G, Kw, N = w.shape
+    idx = _i64(expanded_row_idx)
+    gl = _i64(group_list)
+    M = idx.shape[0]
+    if B != batch or Kw != K or gl.shape != (G,):
+        raise OracleError(2)
+    if rows is None:
+        rw = None
+        nr = M
+    else:
+        rw = _i64(rows)
+        nr = rw.shape[0]
+    out = np.empty((nr, N), dtype=np.float64)
+    rc = lib.oracle_fwd(xr.ctypes.data, w.ctypes.data, dt, idx.ctypes.data, gl.ctypes.data,
+                        M, N, K, G, batch, top_k, row_idx_type,
+                        None if rw is None else rw.ctypes.data, nr, out.ctypes.data,
+                        int(nthreads))
+    if rc != 0:
+        raise OracleError(rc)
+    return out
 
 
 def decode(raw_bits: np.ndarray, dtype_code: int, lib=None) -> np.ndarray:

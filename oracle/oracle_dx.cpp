@@ -49,6 +49,16 @@
 // row from the index; for each requested (g, k), for the rows i of expert g in
 // increasing order, add x[batch(i), k] * d_y[i, n] into an accumulator row
 // over n. An expert with no rows has a zero gradient.
+//
+// The forward that these are the gradients of (same page, section 1.1 and
+// the forward chain of section 1.2: MoeInitRouting(x) -> expanded_x, then
+// GroupedMatmul(expanded_x, weight) -> y, expanded_x @ weight per expert):
+//
+//     y[i, n] = sum over k of x[batch(i), k] * weight[g(i), k, n]
+//
+// Steps: widen; expert and original position of each row as above; for each
+// requested expanded row i, the dot products over k (ascending) of x's row
+// batch(i) with the columns of weight[g(i)].
 
 #include <cmath>
 #include <cstdint>
@@ -229,6 +239,33 @@ void run_dw_rows(const DwJob& job, int64_t s_begin, int64_t s_end) {
   }
 }
 
+struct FwdJob {
+  const void* x;
+  const void* w;
+  const Decoder* dec;
+  const Routing* routing;
+  const int64_t* rows;
+  int64_t nrows, N, K, topK;
+  double* out;
+};
+
+void run_fwd_rows(const FwdJob& job, int64_t s_begin, int64_t s_end) {
+  const int64_t N = job.N, K = job.K;
+  std::vector<double> x_row(K);
+  for (int64_t s = s_begin; s < s_end; ++s) {
+    const int64_t i = job.rows ? job.rows[s] : s;
+    const int64_t b = job.routing->pos_of_row[i] / job.topK;
+    const int64_t g = job.routing->group_of_row[i];
+    for (int64_t k = 0; k < K; ++k) x_row[k] = job.dec->at(job.x, b * K + k);
+    double* o = job.out + s * N;
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += x_row[k] * job.dec->at(job.w, (g * K + k) * N + n);
+      o[n] = acc;
+    }
+  }
+}
+
 template <class JobT, class Fn>
 void run_pool(const JobT& job, int64_t count, int nthreads, Fn fn) {
   if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
@@ -282,6 +319,32 @@ int oracle_dx(const void* dy, const void* w, int dtype, const int64_t* expanded_
   Decoder dec(dtype);
   Job job{dy, w, &dec, &routing, tokens, ntokens, N, K, topK, out};
   run_pool(job, ntokens, nthreads, run_tokens);
+  return kOk;
+}
+
+// Forward rows y[rows[s], 0..N-1] for s < nrows (all M rows in order when
+// rows == NULL, then nrows must equal M). out is [nrows, N] double. x is
+// [batch, K], w is [G, K, N], both in the given dtype.
+int oracle_fwd(const void* x, const void* w, int dtype, const int64_t* expanded_row_idx,
+               const int64_t* group_list, int64_t M, int64_t N, int64_t K, int64_t G,
+               int64_t batch, int64_t topK, int row_idx_type, const int64_t* rows, int64_t nrows,
+               double* out, int nthreads) {
+  if (!x || !w || !expanded_row_idx || !group_list || !out) return kErrNull;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return kErrDtype;
+  if (batch <= 0 || topK <= 0 || (row_idx_type != 0 && row_idx_type != 1)) return kErrAttr;
+  if (M <= 0 || N <= 0 || K <= 0 || G <= 0) return kErrShape;
+  if (M != batch * topK) return kErrShape;
+  if (!rows && nrows != M) return kErrShape;
+  for (int64_t s = 0; rows && s < nrows; ++s)
+    if (rows[s] < 0 || rows[s] >= M) return kErrShape;
+
+  Routing routing;
+  const int rc = build_routing(expanded_row_idx, group_list, M, G, row_idx_type, &routing);
+  if (rc != kOk) return rc;
+
+  Decoder dec(dtype);
+  FwdJob job{x, w, &dec, &routing, rows, nrows, N, K, topK, out};
+  run_pool(job, nrows, nthreads, run_fwd_rows);
   return kOk;
 }
 

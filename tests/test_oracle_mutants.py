@@ -2,7 +2,7 @@
 
 Each mutant is the oracle's C++ source with one edit (a dropped term, a wrong
 index, a transposed operand, swapped index forms, a wrong exponent bias, in
-the input gradient or the weight gradient),
+the input gradient, the weight gradient or the forward),
 compiled to a temporary library on the CPU. The check fails if any mutant
 passes every pin below, i.e. if the pins could not tell it from the real
 oracle. Every mutant keeps all memory accesses in bounds.
@@ -43,6 +43,13 @@ MUTANTS = {
                                      "const int64_t b = i / job.topK;"),
     "dw_k_n_swapped_in_x": ("job.dec->at(job.x, b * K + k)",
                             "job.dec->at(job.x, b * K + (K - 1 - k))"),
+    # forward
+    "fwd_transposed_weight": ("acc += x_row[k] * job.dec->at(job.w, (g * K + k) * N + n);",
+                              "acc += x_row[k] * job.dec->at(job.w, (g * K + n) * N + k);"),
+    "fwd_group_of_previous_row": ("    const int64_t g = job.routing->group_of_row[i];\n    for (int64_t k = 0; k < K; ++k) x_row[k]",
+                                  "    const int64_t g = job.routing->group_of_row[i > 0 ? i - 1 : 0];\n    for (int64_t k = 0; k < K; ++k) x_row[k]"),
+    "fwd_drop_last_k": ("for (int64_t k = 0; k < K; ++k) acc += x_row[k]",
+                        "for (int64_t k = 0; k < K - 1; ++k) acc += x_row[k]"),
 }
 
 
@@ -61,6 +68,7 @@ def build_mutant(tmp_path, name):
 def pins_pass(lib) -> bool:
     from test_oracle_pins import brute_force, unfused_numpy, rel_err
     from test_oracle_dw_pins import brute_force_dw
+    from test_oracle_fwd_pins import brute_force_fwd
     from workloads.moe import forward_input
     # decoders against numpy / torch
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
@@ -97,6 +105,14 @@ def pins_pass(lib) -> bool:
             except oracle.OracleError:
                 return False
             if rel_err(gw, brute_force_dw(inp, x)) > 1e-12:
+                return False
+            # forward against its brute force
+            try:
+                y = oracle.fwd(x, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                               inp.top_k, rit, lib=lib)
+            except oracle.OracleError:
+                return False
+            if rel_err(y, brute_force_fwd(inp, x)) > 1e-12:
                 return False
     return True
 
