@@ -41,8 +41,8 @@ MUTANTS = {
                            "for (int64_t i = 0;"),
     "dw_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;",
                                      "const int64_t b = i / job.topK;"),
-    "dw_k_n_swapped_in_x": ("job.dec->at(job.x, b * K + k)",
-                            "job.dec->at(job.x, b * K + (K - 1 - k))"),
+    "dw_k_n_swapped_in_x": ("const double xv = job.dec->at(job.x, b * K + k);",
+                            "const double xv = job.dec->at(job.x, b * K + (K - 1 - k));"),
     # forward
     "fwd_transposed_weight": ("acc += x_row[k] * job.dec->at(job.w, (g * K + k) * N + n);",
                               "acc += x_row[k] * job.dec->at(job.w, (g * K + n) * N + k);"),
