@@ -39,8 +39,8 @@ MUTANTS = {
                          "i + 1 < job.routing->first_row[g + 1]; ++i)"),
     "dw_rows_from_start": ("for (int64_t i = job.routing->first_row[g];",
                            "for (int64_t i = 0;"),
-    "dw_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;",
-                                     "const int64_t b = i / job.topK;"),
+    "dw_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;\n      const double xv",
+                                     "const int64_t b = i / job.topK;\n      const double xv"),
     "dw_k_n_swapped_in_x": ("const double xv = job.dec->at(job.x, b * K + k);",
                             "const double xv = job.dec->at(job.x, b * K + (K - 1 - k));"),
     # forward
@@ -48,6 +48,8 @@ MUTANTS = {
                               "acc += x_row[k] * job.dec->at(job.w, (g * K + n) * N + k);"),
     "fwd_group_of_previous_row": ("    const int64_t g = job.routing->group_of_row[i];\n    for (int64_t k = 0; k < K; ++k) x_row[k]",
                                   "    const int64_t g = job.routing->group_of_row[i > 0 ? i - 1 : 0];\n    for (int64_t k = 0; k < K; ++k) x_row[k]"),
+    "fwd_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;\n    const int64_t g",
+                                      "const int64_t b = i / job.topK;\n    const int64_t g"),
     "fwd_drop_last_k": ("for (int64_t k = 0; k < K; ++k) acc += x_row[k]",
                         "for (int64_t k = 0; k < K - 1; ++k) acc += x_row[k]"),
 }
