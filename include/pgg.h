@@ -291,6 +291,71 @@ int pgg_dw_grouped_gemm(const void* x, const void* gradY, const int64_t* expande
 int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
                 int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
 
+/*
+ * ---------------------------------------------------------------------------
+ * Forward (the operation these are the gradients of; page
+ * "MoeInitRoutingGroupedMatmulGrad design", sections 1.1 and 1.2, forward
+ * chain: MoeInitRouting(x) -> expanded_x, GroupedMatmul(expanded_x, weight)
+ * -> y):
+ *
+ *     y[i, n] = sum_k x[batch(i), k] * weight[g(i), k, n]      (i in expanded order)
+ *
+ *   x              device, [batch, K] of `dtype`, original token order; the rows
+ *                  of expanded_x are gathered from it by the routing, never
+ *                  materialised
+ *   weight         device, [G, K, N] of `dtype`
+ *   expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType, dtype:
+ *                  as for pgg_dx_execute
+ *   out_dtype      dtype of y: `dtype` or PGG_F32 (else PGG_ERR_DTYPE); FP32
+ *                  accumulation, one round-to-nearest-even for 16-bit outputs
+ *   workspace      at least pgg_fwd_workspace_size bytes, 256-byte aligned;
+ *                  status word at offset 0 as for pgg_dx_execute
+ *   y              device, [M, N] of out_dtype, expanded order, fully
+ *                  overwritten; zero-filled when the routing validation fails
+ *
+ * Each element is one dot product over k in a fixed order: bitwise
+ * repeatable. Tensor cores when dtype is 16-bit, K and N are multiples of 8
+ * and x, weight, y are 16-byte aligned; otherwise the FP32 pipes (also forced
+ * by pgg_debug_force_variant(3)). x and weight aligned to their element size,
+ * y to its element size.
+ */
+int pgg_fwd_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                           int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                           size_t* workspace_bytes);
+
+int pgg_fwd_execute(const void* x, const void* weight, const int64_t* expandedRowIdx,
+                    const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                    int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                    pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* y,
+                    pgg_stream_t stream);
+
+/*
+ * The two stages of pgg_fwd_execute, exposed so that each can be timed on its
+ * own: the routing step (validation, expert offsets, row blocks of up to 256
+ * rows, tokens) and the forward kernel on the workspace it prepared. Same
+ * arguments and errors as pgg_fwd_execute (the routing step without the value
+ * tensors and y).
+ */
+int pgg_fwd_route_prep(const int64_t* expandedRowIdx, const int64_t* groupList, int64_t M,
+                       int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                       int rowIdxType, pgg_dtype dtype, void* workspace, size_t workspace_bytes,
+                       pgg_stream_t stream);
+
+int pgg_fwd_grouped_gemm(const void* x, const void* weight, const int64_t* expandedRowIdx,
+                         const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                         int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                         pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* y,
+                         pgg_stream_t stream);
+
+/*
+ * How pgg_fwd_execute runs these sizes with 16-byte aligned pointers: variant
+ * 0 (tensor cores on CTA pairs: row blocks of rows_per_block = 256 expanded
+ * rows x 256 n, k_per_block = 64 per stage) or 3 (FP32 pipes: 64 rows x 128 n,
+ * 32 k per step); band_k_blocks holds the n blocks per row block.
+ */
+int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                 int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
+
 #ifdef __cplusplus
 }
 #endif

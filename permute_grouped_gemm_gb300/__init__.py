@@ -13,6 +13,8 @@ from ._lib import (  # noqa: F401
     CODES, PGG_BF16, PGG_F16, PGG_F32, STATUS, PggError, load,
     pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
     pgg_dw_execute, pgg_dw_grouped_gemm, pgg_dw_plan, pgg_dw_workspace_size,
+    pgg_fwd_execute, pgg_fwd_grouped_gemm, pgg_fwd_plan, pgg_fwd_route_prep,
+    pgg_fwd_workspace_size,
     pgg_dx_execute, pgg_dx_execute_static_scratch, pgg_dx_grouped_gemm, pgg_dx_plan,
     pgg_dx_route_prep,
     pgg_dx_workspace_size, pgg_status_string,
@@ -111,6 +113,40 @@ def dw(x, grad_y, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_
                         out.data_ptr(), stream.cuda_stream)
     if rc != 0:
         raise PggError(rc, "pgg_dw_execute")
+    return out, workspace
+
+
+def fwd(x, weight, expanded_row_idx, group_list, batch: int, top_k: int, row_idx_type: int,
+        out_dtype=None, out=None, workspace=None, stream=None):
+    """Forward y [M, N] (expanded order; ``out_dtype``: x's dtype by default, or
+    torch.float32) from x [batch, K] and weight [G, K, N]. Returns (y, workspace)."""
+    import torch
+    for t in (x, weight, expanded_row_idx, group_list):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if expanded_row_idx.dtype != torch.int64 or group_list.dtype != torch.int64:
+        raise ValueError("expandedRowIdx and groupList must be int64")
+    if x.dtype != weight.dtype:
+        raise PggError(CODES["PGG_ERR_DTYPE"], "fwd")
+    G, K, N = weight.shape
+    M = expanded_row_idx.shape[0]
+    sizes = (M, N, K, G, M, batch, top_k)
+    dt = dtype_code(x.dtype)
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    odt = dtype_code(out_dtype)
+    need = pgg_fwd_workspace_size(*sizes, row_idx_type, dt)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    rc = pgg_fwd_execute(x.data_ptr(), weight.data_ptr(), expanded_row_idx.data_ptr(),
+                         group_list.data_ptr(), *sizes, row_idx_type, dt, odt,
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                         out.data_ptr(), stream.cuda_stream)
+    if rc != 0:
+        raise PggError(rc, "pgg_fwd_execute")
     return out, workspace
 
 

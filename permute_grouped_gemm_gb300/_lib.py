@@ -70,6 +70,16 @@ def load(path: str | None = None):
             lib.pgg_dw_execute.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz, vp, vp]
             lib.pgg_dw_grouped_gemm.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz,
                                                 vp, vp]
+            lib.pgg_fwd_workspace_size.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(sz)]
+            lib.pgg_fwd_plan.argtypes = [*_SIZES, i32, i32, ctypes.POINTER(PlanInfo)]
+            lib.pgg_fwd_execute.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz, vp,
+                                            vp]
+            lib.pgg_fwd_grouped_gemm.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz,
+                                                 vp, vp]
+            lib.pgg_fwd_route_prep.argtypes = [vp, vp, *_SIZES, i32, i32, vp, sz, vp]
+            for f in ("pgg_fwd_workspace_size", "pgg_fwd_plan", "pgg_fwd_execute",
+                      "pgg_fwd_grouped_gemm", "pgg_fwd_route_prep"):
+                getattr(lib, f).restype = ctypes.c_int
             for f in ("pgg_dx_workspace_size", "pgg_dx_plan", "pgg_dx_execute",
                       "pgg_dx_grouped_gemm", "pgg_dx_route_prep", "pgg_dx_execute_static_scratch",
                       "pgg_dw_workspace_size", "pgg_dw_plan", "pgg_dw_execute",
@@ -166,6 +176,42 @@ def pgg_dw_grouped_gemm(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batc
     return load().pgg_dw_grouped_gemm(x, gradY, expandedRowIdx, groupList, M, N, K, G, L, batch,
                                       topK, rowIdxType, dtype, out_dtype, workspace,
                                       workspace_bytes, dweight, stream)
+
+
+def pgg_fwd_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pgg_fwd_workspace_size(M, N, K, G, L, batch, topK, rowIdxType, dtype,
+                                         ctypes.byref(out)), "pgg_fwd_workspace_size")
+    return out.value
+
+
+def pgg_fwd_plan(M, N, K, G, L, batch, topK, rowIdxType, dtype) -> dict:
+    info = PlanInfo()
+    _check(load().pgg_fwd_plan(M, N, K, G, L, batch, topK, rowIdxType, dtype,
+                               ctypes.byref(info)), "pgg_fwd_plan")
+    return info.as_dict()
+
+
+def pgg_fwd_execute(x, weight, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                    rowIdxType, dtype, out_dtype, workspace, workspace_bytes, y, stream) -> int:
+    """Raw call with integer device addresses; returns the pgg_status code."""
+    return load().pgg_fwd_execute(x, weight, expandedRowIdx, groupList, M, N, K, G, L, batch,
+                                  topK, rowIdxType, dtype, out_dtype, workspace, workspace_bytes,
+                                  y, stream)
+
+
+def pgg_fwd_route_prep(expandedRowIdx, groupList, M, N, K, G, L, batch, topK, rowIdxType, dtype,
+                       workspace, workspace_bytes, stream) -> int:
+    return load().pgg_fwd_route_prep(expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                                      rowIdxType, dtype, workspace, workspace_bytes, stream)
+
+
+def pgg_fwd_grouped_gemm(x, weight, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
+                         rowIdxType, dtype, out_dtype, workspace, workspace_bytes, y,
+                         stream) -> int:
+    return load().pgg_fwd_grouped_gemm(x, weight, expandedRowIdx, groupList, M, N, K, G, L,
+                                       batch, topK, rowIdxType, dtype, out_dtype, workspace,
+                                       workspace_bytes, y, stream)
 
 
 def pgg_status_string(code: int) -> str:

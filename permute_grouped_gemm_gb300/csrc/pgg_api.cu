@@ -36,6 +36,17 @@ cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const CUtensorMap& tm
 void dw_simt_tiles(int64_t K, int64_t N, int* k_blocks, int* n_blocks);
 int dw_simt_smem_bytes();
 cudaError_t launch_dw_simt(int dtype, const DwArgs& a, int vec, int num_sms, cudaStream_t stream);
+int fwd_smem_bytes();
+int fwd_threads();
+int fwd_rows_per_block();
+int fwd_stages();
+void fwd_tiles(int64_t N, int* n_blocks);
+cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const CUtensorMap& tm_y,
+                       const FwdArgs& a, int64_t max_tiles, int num_sms, cudaStream_t stream);
+void fwd_simt_tiles(int64_t N, int* n_blocks);
+int fwd_simt_smem_bytes();
+cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
+                            cudaStream_t stream);
 
 namespace {
 
@@ -68,8 +79,10 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
 // byte length must be a multiple of 16.
 bool rows_streamable(int64_t N, int dtype) { return (N * elem_size(dtype)) % 16 == 0; }
 
+// rows_override > 0: row blocks of that many rows (the forward's 256) instead
+// of the d_x variant's.
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
-              int rowIdxType, int dtype, Plan* p) {
+              int rowIdxType, int dtype, Plan* p, int rows_override = 0) {
   std::memset(p, 0, sizeof(*p));
   p->dtype = dtype;
   int variant = g_force_variant.load();
@@ -82,6 +95,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
                             &p->smem_bytes, &p->pair)) {
     return PGG_ERR_DTYPE;
   }
+  if (rows_override > 0) p->rows_per_block = rows_override;
   p->M = M;
   p->N = N;
   p->K = K;
@@ -393,6 +407,107 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
                                                                                   : PGG_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- forward
+
+// The tensor-core forward takes 16-bit inputs whose x, weight and y rows are
+// whole 16-byte units, with x, weight and y 16-byte aligned.
+bool fwd_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void* w,
+                     const void* y) {
+  if (g_force_variant.load() == kVariantSimt) return false;
+  if (dtype == PGG_F32) return false;
+  if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0) return false;
+  return aligned(x, 16) && aligned(w, 16) && aligned(y, 16);
+}
+
+int make_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
+                  int rowIdxType, int dtype, Plan* p) {
+  return make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, p, fwd_rows_per_block());
+}
+
+int check_fwd(const void* x, const void* weight, const int64_t* idx, const int64_t* gl,
+              bool need_values, int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+              int64_t batch, int64_t topK, int rowIdxType, int dtype, int out_dtype, void* ws,
+              size_t ws_bytes, const void* y, Plan* plan) {
+  if (!idx || !gl || !ws) return PGG_ERR_NULL;
+  if (need_values && (!x || !weight || !y)) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  if (out_dtype != dtype && out_dtype != PGG_F32) return PGG_ERR_DTYPE;
+  rc = make_fwd_plan(M, N, K, G, batch, topK, rowIdxType, dtype, plan);
+  if (rc != PGG_OK) return rc;
+  if (!aligned(ws, 256) || !aligned(idx, 8) || !aligned(gl, 8)) return PGG_ERR_ALIGN;
+  const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
+  if (need_values && (!aligned(x, es) || !aligned(weight, es) ||
+                      !aligned(y, static_cast<uintptr_t>(elem_size(out_dtype)))))
+    return PGG_ERR_ALIGN;
+  if (ws_bytes < plan->layout.total) return PGG_ERR_WORKSPACE;
+  return PGG_OK;
+}
+
+int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void* y,
+            int out_dtype, cudaStream_t stream) {
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  char* w = static_cast<char*>(ws);
+  FwdArgs a;
+  a.x = x;
+  a.w = weight;
+  a.rblist = reinterpret_cast<const int4*>(w + plan.layout.rblist);
+  a.rowinfo = reinterpret_cast<const RowInfo*>(w + plan.layout.rowinfo);
+  a.hdr = reinterpret_cast<WsHeader*>(w + plan.layout.hdr);
+  a.out = y;
+  a.M = plan.M;
+  a.N = plan.N;
+  a.K = plan.K;
+  a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  if (fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
+    fwd_tiles(plan.N, &a.n_blocks);
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PGG_ERR_CUDA;
+    CUtensorMap tm_w, tm_y;
+    {
+      // weight [G, K, N]: boxes of 64 n x 64 k of one expert
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.K),
+                            static_cast<cuuint64_t>(plan.G)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(plan.N) * 2,
+                               static_cast<cuuint64_t>(plan.N) * static_cast<cuuint64_t>(plan.K) *
+                                   2};
+      cuuint32_t box[3] = {64, 64, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (enc(&tm_w, tmap_type(plan.dtype), 3, const_cast<void*>(weight), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PGG_ERR_CUDA;
+    }
+    {
+      // y [M, N] (as {N, M, 1}): boxes of 128 bytes x 32 rows
+      const int oes = out_dtype == PGG_F32 ? 4 : 2;
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.M), 1};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(plan.N) * oes,
+                               static_cast<cuuint64_t>(plan.N) * static_cast<cuuint64_t>(plan.M) *
+                                   oes};
+      cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / oes), 32, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (enc(&tm_y, tmap_type(out_dtype), 3, y, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PGG_ERR_CUDA;
+    }
+    return launch_fwd(plan.dtype, tm_w, tm_y, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
+                      stream) == cudaSuccess
+               ? PGG_OK
+               : PGG_ERR_CUDA;
+  }
+  fwd_simt_tiles(plan.N, &a.n_blocks);
+  const uintptr_t vec_align = out_dtype == PGG_F32 ? 16 : 8;
+  const int vec = (plan.N % 4 == 0 && aligned(y, vec_align)) ? 1 : 0;
+  return launch_fwd_simt(plan.dtype, a, vec, plan.max_row_blocks * a.n_blocks, di.num_sms,
+                         stream) == cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pgg
 
@@ -542,6 +657,93 @@ int pgg_dw_grouped_gemm(const void* x, const void* gradY, const int64_t* expande
   if (rc != PGG_OK) return rc;
   return run_dw(plan, x, gradY, workspace, dweight, out_dtype,
                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pgg_fwd_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                           int64_t topK, int rowIdxType, pgg_dtype dtype, size_t* workspace_bytes) {
+  if (!workspace_bytes) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  Plan plan;
+  rc = make_fwd_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &plan);
+  if (rc != PGG_OK) return rc;
+  *workspace_bytes = plan.layout.total;
+  return PGG_OK;
+}
+
+int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
+                 int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info) {
+  if (!info) return PGG_ERR_NULL;
+  int rc = check_sizes(M, N, K, G, L, batch, topK, rowIdxType, dtype);
+  if (rc != PGG_OK) return rc;
+  Plan p;
+  rc = make_fwd_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
+  if (rc != PGG_OK) return rc;
+  alignas(16) static const char probe[16] = {0};
+  const bool tc = fwd_tensor_path(dtype, N, K, probe, probe, probe);
+  std::memset(info, 0, sizeof(*info));
+  int nb = 0;
+  info->rows_per_block = p.rows_per_block;
+  info->max_row_blocks = p.max_row_blocks;
+  info->workspace_bytes = p.layout.total;
+  if (tc) {
+    fwd_tiles(N, &nb);
+    info->variant = 0;
+    info->k_per_block = 64;
+    info->stages = fwd_stages();
+    info->threads = fwd_threads();
+    info->smem_bytes = fwd_smem_bytes();
+    info->cta_pair = 1;
+  } else {
+    fwd_simt_tiles(N, &nb);
+    info->variant = kVariantSimt;
+    info->k_per_block = 32;
+    info->stages = 2;
+    info->threads = 128;
+    info->smem_bytes = fwd_simt_smem_bytes();
+  }
+  info->k_blocks = static_cast<int32_t>((K + info->k_per_block - 1) / info->k_per_block);
+  info->band_k_blocks = nb;
+  return PGG_OK;
+}
+
+int pgg_fwd_route_prep(const int64_t* expandedRowIdx, const int64_t* groupList, int64_t M,
+                       int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch, int64_t topK,
+                       int rowIdxType, pgg_dtype dtype, void* workspace, size_t workspace_bytes,
+                       pgg_stream_t stream) {
+  Plan plan;
+  int rc = check_fwd(nullptr, nullptr, expandedRowIdx, groupList, false, M, N, K, G, L, batch,
+                     topK, rowIdxType, dtype, dtype, workspace, workspace_bytes, nullptr, &plan);
+  if (rc != PGG_OK) return rc;
+  return run_route_prep(plan, expandedRowIdx, groupList, workspace,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pgg_fwd_grouped_gemm(const void* x, const void* weight, const int64_t* expandedRowIdx,
+                         const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G,
+                         int64_t L, int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                         pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* y,
+                         pgg_stream_t stream) {
+  Plan plan;
+  int rc = check_fwd(x, weight, expandedRowIdx, groupList, true, M, N, K, G, L, batch, topK,
+                     rowIdxType, dtype, out_dtype, workspace, workspace_bytes, y, &plan);
+  if (rc != PGG_OK) return rc;
+  return run_fwd(plan, x, weight, workspace, y, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pgg_fwd_execute(const void* x, const void* weight, const int64_t* expandedRowIdx,
+                    const int64_t* groupList, int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
+                    int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
+                    pgg_dtype out_dtype, void* workspace, size_t workspace_bytes, void* y,
+                    pgg_stream_t stream) {
+  Plan plan;
+  int rc = check_fwd(x, weight, expandedRowIdx, groupList, true, M, N, K, G, L, batch, topK,
+                     rowIdxType, dtype, out_dtype, workspace, workspace_bytes, y, &plan);
+  if (rc != PGG_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = run_route_prep(plan, expandedRowIdx, groupList, workspace, s);
+  if (rc != PGG_OK) return rc;
+  return run_fwd(plan, x, weight, workspace, y, out_dtype, s);
 }
 
 const char* pgg_status_string(int status) {

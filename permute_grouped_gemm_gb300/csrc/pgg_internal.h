@@ -127,4 +127,18 @@ struct DwArgs {
   uint64_t wait_limit_ns;
 };
 
+// Arguments of the forward kernels (gmm_fwd.cu, gmm_fwd_simt.cu).
+struct FwdArgs {
+  const void* x;           // [batch, K] dtype: the forward input, original token order
+  const void* w;           // [G, K, N] dtype (read directly by the FP32-pipe kernel)
+  const int4* rblist;      // {expert, first row, rows, 0} per row block (routing step)
+  const RowInfo* rowinfo;  // [M] token of each expanded row
+  WsHeader* hdr;
+  void* out;               // y [M, N] in the output dtype, expanded order
+  int64_t M, N, K;
+  int32_t n_blocks;  // output column blocks per row block
+  int32_t out_f32;   // 1: y is fp32; 0: y has the input dtype
+  uint64_t wait_limit_ns;
+};
+
 }  // namespace pgg

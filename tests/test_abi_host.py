@@ -164,3 +164,27 @@ def test_weight_gradient_plan_and_host_errors(lib):
         "PGG_ERR_ALIGN"
     assert pgg.STATUS[pgg.pgg_dw_execute(fake + 1, *args[1:], pgg.PGG_BF16, fake, need, fake,
                                          None)] == "PGG_ERR_ALIGN"
+
+
+def test_forward_plan_and_host_errors(lib):
+    a = LARGE
+    sizes = (a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"], a["topK"], 0)
+    p = pgg.pgg_fwd_plan(*sizes, pgg.PGG_BF16)
+    assert p["variant"] == 0 and p["rows_per_block"] == 256 and p["cta_pair"] == 1
+    assert p["k_per_block"] == 64 and p["k_blocks"] == 112 and p["band_k_blocks"] == 8
+    assert p["smem_bytes"] <= 227 * 1024
+    assert pgg.pgg_fwd_plan(*sizes, pgg.PGG_F32)["variant"] == 3
+    assert pgg.pgg_fwd_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
+                            pgg.PGG_BF16)["variant"] == 3
+    need = pgg.pgg_fwd_workspace_size(*sizes, pgg.PGG_BF16)
+    assert need <= 16 * 2**20
+    fake = 1 << 20
+    args = (fake, fake, fake, fake, *sizes[:-1], 0, pgg.PGG_BF16)
+    assert pgg.STATUS[pgg.pgg_fwd_execute(*args, pgg.PGG_F16, fake, need, fake, None)] == \
+        "PGG_ERR_DTYPE"
+    assert pgg.STATUS[pgg.pgg_fwd_execute(*args, pgg.PGG_BF16, fake, need - 1, fake, None)] == \
+        "PGG_ERR_WORKSPACE"
+    assert pgg.STATUS[pgg.pgg_fwd_execute(*args, pgg.PGG_BF16, fake, need, 0, None)] == \
+        "PGG_ERR_NULL"
+    assert pgg.STATUS[pgg.pgg_fwd_execute(fake + 1, *args[1:], pgg.PGG_BF16, fake, need, fake,
+                                          None)] == "PGG_ERR_ALIGN"
