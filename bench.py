@@ -14,7 +14,8 @@ of the grouped-GEMM kernel and the workspace bytes.
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
 
 --op dw times the companion weight-gradient kernel (x^T d_y per expert with
-the x rows gathered by the routing) on the same workload instead.
+the x rows gathered by the routing) on the same workload instead; --op fwd
+the forward y = expanded_x W per expert it differentiates.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload on its own GPU (the path needs no exchange); value sums the work of
@@ -49,6 +50,8 @@ KERNEL_SOURCES = {
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
     "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", *_COMMON],
     "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],
+    "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", *_COMMON],
+    "gmm_fwd_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd_simt.cu", *_COMMON],
 }
 SIMT_VARIANT = 3
 FP32_LANES_PER_SM = 128    # FP32 fused multiply-add lanes per SM
@@ -62,8 +65,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--op", default="dx", choices=["dx", "dw"],
-                    help="dx: the fused input gradient (default); dw: the weight gradient")
+    ap.add_argument("--op", default="dx", choices=["dx", "dw", "fwd"],
+                    help="dx: the fused input gradient (default); dw: the weight gradient; "
+                         "fwd: the forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -195,6 +199,12 @@ class DxOp:
     def values(self):
         return self.inp.grad_y, self.inp.weight
 
+    def stage1(self, idx, gl, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_dx_route_prep(idx.data_ptr(), gl.data_ptr(), *self.sizes,
+                                          w.row_idx_type, self.dt, self.ws.data_ptr(),
+                                          self.ws_bytes, sp)
+
     def stage2(self, a, b, idx, gl, out, sp):
         w = self.inp.workload
         return self.pgg.pgg_dx_grouped_gemm(a.data_ptr(), b.data_ptr(), idx.data_ptr(),
@@ -297,7 +307,78 @@ class DwOp(DxOp):
         return self.inp.workload.G * self.inp.workload.K
 
 
-OPS = {"dx": DxOp, "dw": DwOp}
+class FwdOp(DxOp):
+    """The forward y = GroupedMatmul(Permute(x), weight) these are the gradients of."""
+    name = "fwd"
+    metric = ("forward TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300: y = expanded_x W per expert, "
+              "x rows gathered by routing")
+
+    def __init__(self, inp, pgg, dev):
+        import torch
+        from workloads.moe import forward_input
+        self.inp, self.pgg = inp, pgg
+        w = inp.workload
+        self.dt = pgg.dtype_code(inp.grad_y.dtype)
+        self.sizes = (w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k)
+        self.plan = pgg.pgg_fwd_plan(*self.sizes, w.row_idx_type, self.dt)
+        self.ws_bytes = pgg.pgg_fwd_workspace_size(*self.sizes, w.row_idx_type, self.dt)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.x = forward_input(inp, dev)
+        self.out = torch.empty(w.M, w.N, dtype=inp.grad_y.dtype, device=dev)
+        self.kernel = ("gmm_fwd_simt_kernel" if self.plan["variant"] == SIMT_VARIANT
+                       else "gmm_fwd_kernel")
+
+    def values(self):
+        return self.x, self.inp.weight
+
+    def stage1(self, idx, gl, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_fwd_route_prep(idx.data_ptr(), gl.data_ptr(), *self.sizes,
+                                           w.row_idx_type, self.dt, self.ws.data_ptr(),
+                                           self.ws_bytes, sp)
+
+    def stage2(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_fwd_grouped_gemm(a.data_ptr(), b.data_ptr(), idx.data_ptr(),
+                                             gl.data_ptr(), *self.sizes, w.row_idx_type, self.dt,
+                                             self.dt, self.ws.data_ptr(), self.ws_bytes,
+                                             out.data_ptr(), sp)
+
+    def execute(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_fwd_execute(a.data_ptr(), b.data_ptr(), idx.data_ptr(),
+                                        gl.data_ptr(), *self.sizes, w.row_idx_type, self.dt,
+                                        self.dt, self.ws.data_ptr(), self.ws_bytes,
+                                        out.data_ptr(), sp)
+
+    def algorithmic(self):
+        """(flops, bytes): 2*M*N*K, and x once + weight of non-empty experts once +
+        y written once (input dtype) + the two index arrays."""
+        inp = self.inp
+        w = inp.workload
+        es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+        nonempty = int((inp.group_list > 0).sum())
+        flops = 2 * w.M * w.N * w.K
+        nbytes = (w.batch * w.K * es + nonempty * w.K * w.N * es + w.M * w.N * es
+                  + w.M * 8 + w.G * 8)
+        return flops, nbytes
+
+    def oracle_sample(self, host, rng, n):
+        import oracle
+        w = host.workload
+        if not hasattr(self, "_host_x"):
+            self._host_x = self.x.cpu()
+        n = max(1, min(w.M, n))
+        rows = np.sort(rng.choice(w.M, n, replace=False))
+        oracle.fwd(self._host_x, host.weight, host.expanded_row_idx, host.group_list, w.batch,
+                   w.top_k, w.row_idx_type, rows=rows)
+        return 2 * w.N * w.K * n, f"{n} of {w.M} rows of y"
+
+    def units(self):
+        return self.inp.workload.M
+
+
+OPS = {"dx": DxOp, "dw": DwOp, "fwd": FwdOp}
 
 
 def cpu_baseline(op, target_s: float):
@@ -332,7 +413,7 @@ def run_reference(args):
     inp = make_inputs(w, device="cpu")
     op = OPS[args.op].__new__(OPS[args.op])
     op.inp = inp
-    if args.op == "dw":
+    if args.op in ("dw", "fwd"):
         from workloads.moe import forward_input
         op.x = forward_input(inp, "cpu")
     cores = oracle.host_cores()
@@ -397,8 +478,7 @@ def run_ours(args):
     idx, gl = inp.expanded_row_idx, inp.group_list
 
     def route_prep():
-        rc = pgg.pgg_dx_route_prep(idx.data_ptr(), gl.data_ptr(), *op.sizes, w.row_idx_type,
-                                   op.dt, ws.data_ptr(), ws_bytes, sp)
+        rc = op.stage1(idx, gl, sp)
         if rc:
             raise pgg.PggError(rc, "route_prep")
 
