@@ -42,8 +42,7 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "uniform-bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace bytes"
-_COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh",
-           "permute_grouped_gemm_gb300/csrc/pgg_internal.h"]
+_COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh"]
 # grouped-GEMM kernel -> the sources its ncu counters depend on
 KERNEL_SOURCES = {
     "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", *_COMMON],
