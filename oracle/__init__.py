@@ -1,5 +1,5 @@
-"""Oracle for the MoE permute + grouped matmul: the backward (d_x, d_weight)
-and the forward y it differentiates.
+"""Oracle for the MoE permute + grouped matmul: the backward (d_x, d_weight),
+the forward y it differentiates, and the probs-weighted unpermute backward.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package. The product path
@@ -90,6 +90,9 @@ def load_library(path: str):
     lib.oracle_fwd.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64,
                                i64, i64, ctypes.c_int, vp, i64, dp, ctypes.c_int]
     lib.oracle_fwd.restype = ctypes.c_int
+    lib.oracle_unpermute_grad.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, i64, i64, i64,
+                                          ctypes.c_int, dp, dp, ctypes.c_int]
+    lib.oracle_unpermute_grad.restype = ctypes.c_int
     return lib
 
 
@@ -250,6 +253,37 @@ def fwd(x, weight, expanded_row_idx, group_list, batch: int, top_k: int, row_idx
     if rc != 0:
         raise OracleError(rc)
     return out
+
+
+def unpermute_grad(permuted, d_out, probs, expanded_row_idx, batch: int, top_k: int,
+                   row_idx_type: int, nthreads: int = 0, lib=None):
+    """fp64 (perm_grad [M, H], probs_grad [batch, topK] or None) of the
+    probs-weighted unpermute: permuted [M, H] (may be None without probs),
+    d_out [batch, H], probs [batch, topK] or None, same dtype."""
+    lib = lib or _load()
+    d, dt = _raw(d_out)
+    B, H = d.shape
+    idx = _i64(expanded_row_idx)
+    M = idx.shape[0]
+    if B != batch:
+        raise OracleError(2)
+    pr = pm = None
+    if probs is not None:
+        pr, dtp = _raw(probs)
+        pm, dtm = _raw(permuted)
+        if dtp != dt or dtm != dt:
+            raise OracleError(4)
+        if pr.shape != (batch, top_k) or pm.shape != (M, H):
+            raise OracleError(2)
+    pg = np.empty((M, H), dtype=np.float64)
+    qg = np.empty((batch, top_k), dtype=np.float64) if probs is not None else None
+    rc = lib.oracle_unpermute_grad(None if pm is None else pm.ctypes.data, d.ctypes.data,
+                                   None if pr is None else pr.ctypes.data, dt, idx.ctypes.data,
+                                   M, H, batch, top_k, row_idx_type, pg.ctypes.data,
+                                   None if qg is None else qg.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise OracleError(rc)
+    return pg, qg
 
 
 def decode(raw_bits: np.ndarray, dtype_code: int, lib=None) -> np.ndarray:

@@ -59,6 +59,18 @@
 // Steps: widen; expert and original position of each row as above; for each
 // requested expanded row i, the dot products over k (ascending) of x's row
 // batch(i) with the columns of weight[g(i)].
+//
+// The probs-weighted unpermute backward (page "NPU DeepSeek-V3.2-Exp TileLang
+// operator practice", section moe_token_unpermute_grad): the forward combine
+// out[b] = sum_j prob[b, j] * permuted[row(b, j)] has the gradients
+//
+//     perm_grad[row(b, j), h] = d_out[b, h] * prob[b, j]       (prob = 1 without probs)
+//     probs_grad[b, j]        = sum over h of d_out[b, h] * permuted[row(b, j), h]
+//
+// with row(b, j) the expanded row of original position b * topK + j, read from
+// the index in either form as above. Steps: widen; the position -> row map;
+// for each token b and j in increasing order, the scaled copy and the dot
+// product over h (ascending).
 
 #include <cmath>
 #include <cstdint>
@@ -266,6 +278,36 @@ void run_fwd_rows(const FwdJob& job, int64_t s_begin, int64_t s_end) {
   }
 }
 
+struct UnpermJob {
+  const void* perm;
+  const void* dout;
+  const void* probs;  // may be null
+  const Decoder* dec;
+  const Routing* routing;
+  int64_t batch, topK, H;
+  double* perm_grad;   // [M, H]
+  double* probs_grad;  // [batch, topK] (only with probs)
+};
+
+void run_unperm_tokens(const UnpermJob& job, int64_t b_begin, int64_t b_end) {
+  const int64_t H = job.H;
+  std::vector<double> d(H);
+  for (int64_t b = b_begin; b < b_end; ++b) {
+    for (int64_t h = 0; h < H; ++h) d[h] = job.dec->at(job.dout, b * H + h);
+    for (int64_t j = 0; j < job.topK; ++j) {
+      const int64_t p = b * job.topK + j;
+      const int64_t i = job.routing->row_of_pos[p];
+      const double pr = job.probs ? job.dec->at(job.probs, p) : 1.0;
+      double dot = 0.0;
+      for (int64_t h = 0; h < H; ++h) {
+        job.perm_grad[i * H + h] = d[h] * pr;
+        if (job.probs) dot += d[h] * job.dec->at(job.perm, i * H + h);
+      }
+      if (job.probs) job.probs_grad[p] = dot;
+    }
+  }
+}
+
 template <class JobT, class Fn>
 void run_pool(const JobT& job, int64_t count, int nthreads, Fn fn) {
   if (nthreads <= 0) nthreads = static_cast<int>(std::thread::hardware_concurrency());
@@ -319,6 +361,31 @@ int oracle_dx(const void* dy, const void* w, int dtype, const int64_t* expanded_
   Decoder dec(dtype);
   Job job{dy, w, &dec, &routing, tokens, ntokens, N, K, topK, out};
   run_pool(job, ntokens, nthreads, run_tokens);
+  return kOk;
+}
+
+// Probs-weighted unpermute backward. perm [M, H] (needed only with probs),
+// dout [batch, H], probs [batch, topK] or null, all in the given dtype;
+// perm_grad [M, H] double; probs_grad [batch, topK] double (written only
+// with probs). The index is the permutation between original positions and
+// expanded rows (rowIdxType as for oracle_dx); there are no experts here.
+int oracle_unpermute_grad(const void* perm, const void* dout, const void* probs, int dtype,
+                          const int64_t* expanded_row_idx, int64_t M, int64_t H, int64_t batch,
+                          int64_t topK, int row_idx_type, double* perm_grad, double* probs_grad,
+                          int nthreads) {
+  if (!dout || !expanded_row_idx || !perm_grad) return kErrNull;
+  if (probs && (!perm || !probs_grad)) return kErrNull;
+  if (dtype != kF32 && dtype != kF16 && dtype != kBF16) return kErrDtype;
+  if (batch <= 0 || topK <= 0 || (row_idx_type != 0 && row_idx_type != 1)) return kErrAttr;
+  if (M <= 0 || H <= 0) return kErrShape;
+  if (M != batch * topK) return kErrShape;
+  const int64_t one_group = M;
+  Routing routing;
+  const int rc = build_routing(expanded_row_idx, &one_group, M, 1, row_idx_type, &routing);
+  if (rc != kOk) return rc;
+  Decoder dec(dtype);
+  UnpermJob job{perm, dout, probs, &dec, &routing, batch, topK, H, perm_grad, probs_grad};
+  run_pool(job, batch, nthreads, run_unperm_tokens);
   return kOk;
 }
 

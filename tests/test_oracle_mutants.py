@@ -2,7 +2,8 @@
 
 Each mutant is the oracle's C++ source with one edit (a dropped term, a wrong
 index, a transposed operand, swapped index forms, a wrong exponent bias, in
-the input gradient, the weight gradient or the forward),
+the input gradient, the weight gradient, the forward or the probs-weighted
+unpermute backward),
 compiled to a temporary library on the CPU. The check fails if any mutant
 passes every pin below, i.e. if the pins could not tell it from the real
 oracle. Every mutant keeps all memory accesses in bounds.
@@ -20,8 +21,8 @@ from workloads import make_case
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle_dx.cpp")
 
 MUTANTS = {
-    "drop_last_topk_term": ("for (int64_t j = 0; j < job.topK; ++j)",
-                            "for (int64_t j = 0; j < job.topK - 1; ++j)"),
+    "drop_last_topk_term": ("for (int64_t j = 0; j < job.topK; ++j) {\n      const int64_t i = job.routing->row_of_pos[b * job.topK + j];",
+                            "for (int64_t j = 0; j < job.topK - 1; ++j) {\n      const int64_t i = job.routing->row_of_pos[b * job.topK + j];"),
     "j_major_original_position": ("row_of_pos[b * job.topK + j]",
                                   "row_of_pos[b + j * static_cast<int64_t>("
                                   "job.routing->row_of_pos.size() / job.topK)]"),
@@ -50,6 +51,12 @@ MUTANTS = {
                                   "    const int64_t g = job.routing->group_of_row[i > 0 ? i - 1 : 0];\n    for (int64_t k = 0; k < K; ++k) x_row[k]"),
     "fwd_token_of_row_not_position": ("const int64_t b = job.routing->pos_of_row[i] / job.topK;\n    const int64_t g",
                                       "const int64_t b = i / job.topK;\n    const int64_t g"),
+    "unperm_prob_of_first_j": ("const double pr = job.probs ? job.dec->at(job.probs, p) : 1.0;",
+                               "const double pr = job.probs ? job.dec->at(job.probs, b * job.topK) : 1.0;"),
+    "unperm_dot_drops_last_h": ("if (job.probs) dot += d[h] * job.dec->at(job.perm, i * H + h);",
+                                "if (job.probs && h + 1 < H) dot += d[h] * job.dec->at(job.perm, i * H + h);"),
+    "unperm_maps_confused": ("const int64_t i = job.routing->row_of_pos[p];",
+                             "const int64_t i = job.routing->pos_of_row[p];"),
     "fwd_drop_last_k": ("for (int64_t k = 0; k < K; ++k) acc += x_row[k]",
                         "for (int64_t k = 0; k < K - 1; ++k) acc += x_row[k]"),
 }
@@ -71,6 +78,8 @@ def pins_pass(lib) -> bool:
     from test_oracle_pins import brute_force, unfused_numpy, rel_err
     from test_oracle_dw_pins import brute_force_dw
     from test_oracle_fwd_pins import brute_force_fwd
+    from test_oracle_unperm_pins import brute as brute_unperm
+    from workloads.moe import unpermute_inputs
     from workloads.moe import forward_input
     # decoders against numpy / torch
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
@@ -115,6 +124,16 @@ def pins_pass(lib) -> bool:
             except oracle.OracleError:
                 return False
             if rel_err(y, brute_force_fwd(inp, x)) > 1e-12:
+                return False
+            # probs-weighted unpermute backward against its brute force
+            d_out, probs = unpermute_inputs(inp)
+            try:
+                pg, qg = oracle.unpermute_grad(inp.grad_y, d_out, probs, inp.expanded_row_idx,
+                                               inp.batch, inp.top_k, rit, lib=lib)
+            except oracle.OracleError:
+                return False
+            bpg, bqg = brute_unperm(inp, d_out, probs)
+            if rel_err(pg, bpg) > 1e-12 or rel_err(qg, bqg) > 1e-12:
                 return False
     return True
 

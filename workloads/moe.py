@@ -192,6 +192,23 @@ def forward_input(inp: Inputs, device=None) -> torch.Tensor:
     return x.to(DTYPES[w.dtype])
 
 
+def unpermute_inputs(inp: Inputs, device=None):
+    """(d_out [batch, N], probs [batch, top_k]) for the probs-weighted unpermute
+    backward that goes with ``inp`` (whose grad_y [M, N] stands for the expert
+    outputs being combined): d_out ~ N(0, 1) (seed + 3); probs drawn uniform in
+    (0, 1] and normalised per token (seed + 4); both in fp32, rounded to the
+    workload dtype."""
+    w = inp.workload
+    device = inp.grad_y.device if device is None else device
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed + 3)
+    d_out = torch.randn(w.batch, w.N, generator=gen, device=device, dtype=torch.float32)
+    gen.manual_seed(w.seed + 4)
+    p = torch.rand(w.batch, w.top_k, generator=gen, device=device, dtype=torch.float32) + 1e-3
+    p = p / p.sum(dim=1, keepdim=True)
+    return d_out.to(DTYPES[w.dtype]), p.to(DTYPES[w.dtype])
+
+
 def make_case(batch, top_k, G, K, N, dtype="bf16", routing="uniform", row_idx_type=0,
               seed=0, empty=(), device="cpu", name="case", **kw) -> Inputs:
     w = Workload(name, batch=batch, top_k=top_k, G=G, K=K, N=N, dtype=dtype, routing=routing,
