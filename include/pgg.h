@@ -356,6 +356,44 @@ int pgg_fwd_grouped_gemm(const void* x, const void* weight, const int64_t* expan
 int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
                  int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
 
+/*
+ * ---------------------------------------------------------------------------
+ * Probs-weighted unpermute backward (page "NPU DeepSeek-V3.2-Exp TileLang
+ * operator practice", section moe_token_unpermute_grad). For the combine that
+ * follows the expert matmul, out[b] = sum_j prob[b, j] * permuted[row(b, j)]:
+ *
+ *     perm_grad[row(b, j), h] = d_out[b, h] * prob[b, j]        (prob = 1 when probs is NULL)
+ *     probs_grad[b, j]        = sum_h d_out[b, h] * permuted[row(b, j), h]
+ *
+ * with row(b, j) the expanded row of original position b * topK + j, read from
+ * expandedRowIdx in the rowIdxType form (0 gather, 1 scatter, as above). No
+ * experts are involved. perm_grad is the gradY of pgg_dx_execute and
+ * pgg_dw_execute.
+ *
+ *   permuted       device, [M, H] of `dtype` (may be NULL when probs is NULL)
+ *   d_out          device, [batch, H] of `dtype`
+ *   probs          device, [batch, topK] of `dtype`, or NULL (plain scatter copy)
+ *   probs_grad_dtype  `dtype` or PGG_F32 (the dot products accumulate in FP32)
+ *   workspace      pgg_unpermute_grad_workspace_size bytes, 256-byte aligned;
+ *                  status word at offset 0 (PGG_ERR_INDEX / PGG_ERR_NOT_PERM
+ *                  zero-fill both outputs)
+ *   perm_grad      device, [M, H] of `dtype`, fully overwritten
+ *   probs_grad     device, [batch, topK], required with probs
+ *
+ * perm_grad is d_out * prob rounded once to `dtype`; each probs_grad is one
+ * FP32 sum in a fixed order: bitwise repeatable. All pointers aligned to their
+ * element size; 16-byte vector access when H * sizeof(dtype) is a multiple of
+ * 16 and the row pointers are 16-byte aligned.
+ */
+int pgg_unpermute_grad_workspace_size(int64_t M, int64_t batch, int64_t topK,
+                                      size_t* workspace_bytes);
+
+int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* probs,
+                       const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
+                       int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_dtype probs_grad_dtype,
+                       void* workspace, size_t workspace_bytes, void* perm_grad, void* probs_grad,
+                       pgg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,7 @@ from ._lib import (  # noqa: F401
     pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
     pgg_dw_execute, pgg_dw_grouped_gemm, pgg_dw_plan, pgg_dw_workspace_size,
     pgg_fwd_execute, pgg_fwd_grouped_gemm, pgg_fwd_plan, pgg_fwd_route_prep,
-    pgg_fwd_workspace_size,
+    pgg_fwd_workspace_size, pgg_unpermute_grad, pgg_unpermute_grad_workspace_size,
     pgg_dx_execute, pgg_dx_execute_static_scratch, pgg_dx_grouped_gemm, pgg_dx_plan,
     pgg_dx_route_prep,
     pgg_dx_workspace_size, pgg_status_string,
@@ -148,6 +148,40 @@ def fwd(x, weight, expanded_row_idx, group_list, batch: int, top_k: int, row_idx
     if rc != 0:
         raise PggError(rc, "pgg_fwd_execute")
     return out, workspace
+
+
+def unpermute_grad(permuted, d_out, probs, expanded_row_idx, top_k: int, row_idx_type: int,
+                   probs_grad_dtype=None, perm_grad=None, probs_grad=None, workspace=None,
+                   stream=None):
+    """(perm_grad [M, H], probs_grad [batch, topK] or None, workspace) of the
+    probs-weighted unpermute (probs None: plain scatter copy)."""
+    import torch
+    for t in (d_out, expanded_row_idx) + ((permuted, probs) if probs is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    batch, H = d_out.shape
+    M = expanded_row_idx.shape[0]
+    dt = dtype_code(d_out.dtype)
+    pdt = d_out.dtype if probs_grad_dtype is None else probs_grad_dtype
+    need = pgg_unpermute_grad_workspace_size(M, batch, top_k)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=d_out.device)
+    if perm_grad is None:
+        perm_grad = torch.empty(M, H, dtype=d_out.dtype, device=d_out.device)
+    if probs is not None and probs_grad is None:
+        probs_grad = torch.empty(batch, top_k, dtype=pdt, device=d_out.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(d_out.device)
+    rc = pgg_unpermute_grad(permuted.data_ptr() if probs is not None else 0, d_out.data_ptr(),
+                            probs.data_ptr() if probs is not None else 0,
+                            expanded_row_idx.data_ptr(), M, H, batch, top_k, row_idx_type, dt,
+                            dtype_code(pdt), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), perm_grad.data_ptr(),
+                            probs_grad.data_ptr() if probs is not None else 0,
+                            stream.cuda_stream)
+    if rc != 0:
+        raise PggError(rc, "pgg_unpermute_grad")
+    return perm_grad, (probs_grad if probs is not None else None), workspace
 
 
 def status(workspace) -> int:

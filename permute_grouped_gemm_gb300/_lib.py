@@ -77,6 +77,12 @@ def load(path: str | None = None):
             lib.pgg_fwd_grouped_gemm.argtypes = [vp, vp, vp, vp, *_SIZES, i32, i32, i32, vp, sz,
                                                  vp, vp]
             lib.pgg_fwd_route_prep.argtypes = [vp, vp, *_SIZES, i32, i32, vp, sz, vp]
+            lib.pgg_unpermute_grad_workspace_size.argtypes = [ctypes.c_int64] * 3 + [
+                ctypes.POINTER(sz)]
+            lib.pgg_unpermute_grad.argtypes = [vp, vp, vp, vp] + [ctypes.c_int64] * 4 + [
+                i32, i32, i32, vp, sz, vp, vp, vp]
+            lib.pgg_unpermute_grad_workspace_size.restype = ctypes.c_int
+            lib.pgg_unpermute_grad.restype = ctypes.c_int
             for f in ("pgg_fwd_workspace_size", "pgg_fwd_plan", "pgg_fwd_execute",
                       "pgg_fwd_grouped_gemm", "pgg_fwd_route_prep"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -212,6 +218,23 @@ def pgg_fwd_grouped_gemm(x, weight, expandedRowIdx, groupList, M, N, K, G, L, ba
     return load().pgg_fwd_grouped_gemm(x, weight, expandedRowIdx, groupList, M, N, K, G, L,
                                        batch, topK, rowIdxType, dtype, out_dtype, workspace,
                                        workspace_bytes, y, stream)
+
+
+def pgg_unpermute_grad_workspace_size(M, batch, topK) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pgg_unpermute_grad_workspace_size(M, batch, topK, ctypes.byref(out)),
+           "pgg_unpermute_grad_workspace_size")
+    return out.value
+
+
+def pgg_unpermute_grad(permuted, d_out, probs, expandedRowIdx, M, H, batch, topK, rowIdxType,
+                       dtype, probs_grad_dtype, workspace, workspace_bytes, perm_grad, probs_grad,
+                       stream) -> int:
+    """Raw call with integer device addresses (0 for an absent optional one)."""
+    return load().pgg_unpermute_grad(permuted or None, d_out, probs or None, expandedRowIdx, M,
+                                     H, batch, topK, rowIdxType, dtype, probs_grad_dtype,
+                                     workspace, workspace_bytes, perm_grad, probs_grad or None,
+                                     stream)
 
 
 def pgg_status_string(code: int) -> str:

@@ -47,6 +47,10 @@ void fwd_simt_tiles(int64_t N, int* n_blocks);
 int fwd_simt_smem_bytes();
 cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
                             cudaStream_t stream);
+cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, int32_t* inv,
+                              WsHeader* hdr, int num_sms, cudaStream_t stream);
+cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, int num_sms,
+                                  cudaStream_t stream);
 
 namespace {
 
@@ -744,6 +748,67 @@ int pgg_fwd_execute(const void* x, const void* weight, const int64_t* expandedRo
   rc = run_route_prep(plan, expandedRowIdx, groupList, workspace, s);
   if (rc != PGG_OK) return rc;
   return run_fwd(plan, x, weight, workspace, y, out_dtype, s);
+}
+
+// Workspace of the unpermute backward: the header, then the inverse index.
+static size_t unperm_inv_offset() { return 256; }
+
+int pgg_unpermute_grad_workspace_size(int64_t M, int64_t batch, int64_t topK,
+                                      size_t* workspace_bytes) {
+  if (!workspace_bytes) return PGG_ERR_NULL;
+  if (batch <= 0 || topK <= 0) return PGG_ERR_ATTR;
+  if (M <= 0 || M > kInt32Max || batch * topK != M) return PGG_ERR_SHAPE;
+  *workspace_bytes = unperm_inv_offset() + align_up(sizeof(int32_t) * static_cast<size_t>(M), 256);
+  return PGG_OK;
+}
+
+int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* probs,
+                       const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
+                       int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_dtype probs_grad_dtype,
+                       void* workspace, size_t workspace_bytes, void* perm_grad, void* probs_grad,
+                       pgg_stream_t stream) {
+  if (!d_out || !expandedRowIdx || !workspace || !perm_grad) return PGG_ERR_NULL;
+  if (probs && (!permuted || !probs_grad)) return PGG_ERR_NULL;
+  if (dtype != PGG_F32 && dtype != PGG_F16 && dtype != PGG_BF16) return PGG_ERR_DTYPE;
+  if (probs_grad_dtype != dtype && probs_grad_dtype != PGG_F32) return PGG_ERR_DTYPE;
+  if (rowIdxType != 0 && rowIdxType != 1) return PGG_ERR_ATTR;
+  if (H <= 0 || H > kInt32Max) return PGG_ERR_SHAPE;
+  size_t need = 0;
+  int rc = pgg_unpermute_grad_workspace_size(M, batch, topK, &need);
+  if (rc != PGG_OK) return rc;
+  const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
+  if (!aligned(workspace, 256) || !aligned(expandedRowIdx, 8) || !aligned(d_out, es) ||
+      !aligned(perm_grad, es) || (probs && (!aligned(permuted, es) || !aligned(probs, es) ||
+                                            !aligned(probs_grad, elem_size(probs_grad_dtype)))))
+    return PGG_ERR_ALIGN;
+  if (workspace_bytes < need) return PGG_ERR_WORKSPACE;
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  char* w = static_cast<char*>(workspace);
+  UnpermArgs a;
+  a.perm = permuted;
+  a.dout = d_out;
+  a.probs = probs;
+  a.idx = expandedRowIdx;
+  a.inv = reinterpret_cast<const int32_t*>(w + unperm_inv_offset());
+  a.hdr = reinterpret_cast<WsHeader*>(w);
+  a.perm_grad = perm_grad;
+  a.probs_grad = probs ? probs_grad : nullptr;
+  a.M = M;
+  a.H = H;
+  a.batch = batch;
+  a.topK = topK;
+  a.row_idx_type = rowIdxType;
+  a.probs_grad_f32 = probs_grad_dtype == PGG_F32 ? 1 : 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_index_prep(expandedRowIdx, M, rowIdxType,
+                        reinterpret_cast<int32_t*>(w + unperm_inv_offset()), a.hdr, di.num_sms,
+                        s) != cudaSuccess)
+    return PGG_ERR_CUDA;
+  const bool vec = (H * static_cast<int64_t>(es)) % 16 == 0 && aligned(d_out, 16) &&
+                   aligned(perm_grad, 16) && (!probs || aligned(permuted, 16));
+  return launch_unpermute_grad(dtype, a, vec, di.num_sms, s) == cudaSuccess ? PGG_OK
+                                                                             : PGG_ERR_CUDA;
 }
 
 const char* pgg_status_string(int status) {

@@ -141,4 +141,19 @@ struct FwdArgs {
   uint64_t wait_limit_ns;
 };
 
+// Arguments of the probs-weighted unpermute backward (unpermute_grad.cu).
+struct UnpermArgs {
+  const void* perm;       // [M, H] dtype (with probs)
+  const void* dout;       // [batch, H] dtype
+  const void* probs;      // [batch, topK] dtype, or null
+  const int64_t* idx;     // [M] expandedRowIdx
+  const int32_t* inv;     // [M] inverse of idx (index prep)
+  WsHeader* hdr;
+  void* perm_grad;        // [M, H] dtype
+  void* probs_grad;       // [batch, topK] in the probs-grad dtype, or null
+  int64_t M, H, batch, topK;
+  int32_t row_idx_type;
+  int32_t probs_grad_f32;  // 1: probs_grad is fp32; 0: it has the input dtype
+};
+
 }  // namespace pgg

@@ -191,7 +191,39 @@ __global__ void route_rank_kernel(const int64_t* __restrict__ idx, const int32_t
   if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
 }
 
+__global__ void header_reset_kernel(WsHeader* hdr) {
+  hdr->status = 0;
+  hdr->sched_next = 0;
+  hdr->n_row_blocks = 0;
+  hdr->timeout_site = 0;
+}
+
+// Every original position must have an expanded row (see row_of_position).
+__global__ void perm_check_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                                  int64_t M, int row_idx_type, WsHeader* hdr) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < M; p += stride)
+    if (row_of_position(idx, inv, p, M, row_idx_type) < 0) bad = true;
+  if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
+}
+
 }  // namespace
+
+// Index validation without experts (for the unpermute backward): header
+// reset, range check and inverse, permutation check. Afterwards the expanded
+// row of position p is inv[p] (rowIdxType 0) or idx[p] (rowIdxType 1).
+cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, int32_t* inv,
+                              WsHeader* hdr, int num_sms, cudaStream_t stream) {
+  header_reset_kernel<<<1, 1, 0, stream>>>(hdr);
+  int64_t blocks = (M + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, M, inv, hdr, nullptr, 0);
+  perm_check_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, inv, M, row_idx_type, hdr);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
                               void* workspace, int num_sms, cudaStream_t stream) {

@@ -1,0 +1,216 @@
+// Probs-weighted unpermute backward ("NPU DeepSeek-V3.2-Exp TileLang operator
+// practice", section moe_token_unpermute_grad). For the combine that follows
+// the expert grouped matmul, out[b] = sum_j prob[b, j] * permuted[row(b, j)],
+// with row(b, j) the expanded row of original position b * topK + j:
+//
+//     perm_grad[row(b, j), h] = d_out[b, h] * prob[b, j]     (prob = 1 without probs)
+//     probs_grad[b, j]        = sum over h of d_out[b, h] * permuted[row(b, j), h]
+//
+// perm_grad is the d_y that the fused d_x backward and the weight gradient
+// take. Bound by HBM: d_out is read once per token (its re-reads for the
+// token's topK rows hit L1), permuted is read once and perm_grad written
+// once. One 256-thread CTA per token (grid-stride); 16-byte loads and stores
+// along h when the rows allow it; the dot product in fp32, each thread over
+// its own positions in increasing order, then a fixed shuffle and
+// shared-memory tree, so that it is bitwise repeatable.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "pgg_internal.h"
+
+namespace pgg {
+namespace {
+
+constexpr int kUThreads = 256;
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<PGG_F32> {
+  static constexpr int kPer16 = 4;
+  __device__ static float get(const void* p, int64_t i) { return static_cast<const float*>(p)[i]; }
+  __device__ static void put(void* p, int64_t i, float v) { static_cast<float*>(p)[i] = v; }
+};
+template <>
+struct Elem<PGG_F16> {
+  static constexpr int kPer16 = 8;
+  __device__ static float get(const void* p, int64_t i) {
+    return __half2float(static_cast<const __half*>(p)[i]);
+  }
+  __device__ static void put(void* p, int64_t i, float v) {
+    static_cast<__half*>(p)[i] = __float2half_rn(v);
+  }
+};
+template <>
+struct Elem<PGG_BF16> {
+  static constexpr int kPer16 = 8;
+  __device__ static float get(const void* p, int64_t i) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  }
+  __device__ static void put(void* p, int64_t i, float v) {
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+// 16 bytes as floats (8 of a 16-bit dtype, 4 of fp32) and back.
+template <int DT>
+__device__ __forceinline__ void unpack16(const uint4& q, float* f) {
+  if constexpr (DT == PGG_F32) {
+    f[0] = __uint_as_float(q.x);
+    f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z);
+    f[3] = __uint_as_float(q.w);
+  } else {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (DT == PGG_BF16) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      } else {
+        const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+        const float2 t = __half22float2(h);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+      }
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack16(const float* f) {
+  if constexpr (DT == PGG_F32) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (DT == PGG_BF16) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+      } else {
+        const __half2 p = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Sum over the block in a fixed order: shuffle tree in each warp, then the
+// warps' sums added by thread 0 in warp order.
+__device__ __forceinline__ float block_sum(float v, float* s_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+  __syncthreads();  // s_part of the previous call has been read
+  if (lane == 0) s_part[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kUThreads / 32; ++w) t += s_part[w];
+  return t;
+}
+
+template <int DT, bool PROBS, bool VEC>
+__global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermArgs a) {
+  __shared__ float s_part[kUThreads / 32];
+  using E = Elem<DT>;
+  const uint32_t st = a.hdr->status;
+  if (st == kStIndex || st == kStGroupSum || st == kStNotPerm) {
+    const int64_t n = a.M * a.H;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t q = t0; q < n; q += stride) E::put(a.perm_grad, q, 0.0f);
+    if (PROBS && a.probs_grad)
+      for (int64_t q = t0; q < a.M; q += stride) {
+        if (a.probs_grad_f32)
+          static_cast<float*>(a.probs_grad)[q] = 0.0f;
+        else
+          E::put(a.probs_grad, q, 0.0f);
+      }
+    return;
+  }
+  const int64_t H = a.H;
+  for (int64_t b = blockIdx.x; b < a.batch; b += gridDim.x) {
+    for (int64_t j = 0; j < a.topK; ++j) {
+      const int64_t p = b * a.topK + j;
+      const int64_t row = a.row_idx_type == 0 ? static_cast<int64_t>(a.inv[p]) : a.idx[p];
+      const float pr = PROBS ? E::get(a.probs, p) : 1.0f;
+      float dot = 0.0f;
+      if constexpr (VEC) {
+        constexpr int kE = E::kPer16;
+        constexpr int64_t kEs = DT == PGG_F32 ? 4 : 2;  // bytes per element
+        const uint4* d4 =
+            reinterpret_cast<const uint4*>(static_cast<const char*>(a.dout) + b * H * kEs);
+        const uint4* p4 = PROBS ? reinterpret_cast<const uint4*>(
+                                      static_cast<const char*>(a.perm) + row * H * kEs)
+                                : nullptr;
+        uint4* g4 = reinterpret_cast<uint4*>(static_cast<char*>(a.perm_grad) + row * H * kEs);
+        for (int64_t v = threadIdx.x; v < H / kE; v += kUThreads) {
+          float d[kE], o[kE];
+          unpack16<DT>(d4[v], d);
+#pragma unroll
+          for (int i = 0; i < kE; ++i) o[i] = d[i] * pr;
+          g4[v] = pack16<DT>(o);
+          if constexpr (PROBS) {
+            float x[kE];
+            unpack16<DT>(__ldg(p4 + v), x);
+#pragma unroll
+            for (int i = 0; i < kE; ++i) dot = fmaf(d[i], x[i], dot);
+          }
+        }
+      } else {
+        for (int64_t h = threadIdx.x; h < H; h += kUThreads) {
+          const float d = E::get(a.dout, b * H + h);
+          E::put(a.perm_grad, row * H + h, d * pr);
+          if constexpr (PROBS) dot = fmaf(d, E::get(a.perm, row * H + h), dot);
+        }
+      }
+      if constexpr (PROBS) {
+        const float t = block_sum(dot, s_part);
+        if (threadIdx.x == 0 && a.probs_grad) {
+          if (a.probs_grad_f32)
+            static_cast<float*>(a.probs_grad)[p] = t;
+          else
+            E::put(a.probs_grad, p, t);
+        }
+      }
+    }
+  }
+}
+
+template <int DT>
+cudaError_t launch_t(const UnpermArgs& a, bool probs, bool vec, int grid, cudaStream_t s) {
+  if (probs && vec)
+    unpermute_grad_kernel<DT, true, true><<<grid, kUThreads, 0, s>>>(a);
+  else if (probs)
+    unpermute_grad_kernel<DT, true, false><<<grid, kUThreads, 0, s>>>(a);
+  else if (vec)
+    unpermute_grad_kernel<DT, false, true><<<grid, kUThreads, 0, s>>>(a);
+  else
+    unpermute_grad_kernel<DT, false, false><<<grid, kUThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// vec: H * sizeof(dtype) a multiple of 16 and perm, d_out, perm_grad 16-byte aligned.
+cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, int num_sms,
+                                  cudaStream_t stream) {
+  int64_t grid = a.batch;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  const bool probs = a.probs != nullptr;
+  if (dtype == PGG_F32) return launch_t<PGG_F32>(a, probs, vec, static_cast<int>(grid), stream);
+  if (dtype == PGG_F16) return launch_t<PGG_F16>(a, probs, vec, static_cast<int>(grid), stream);
+  if (dtype == PGG_BF16) return launch_t<PGG_BF16>(a, probs, vec, static_cast<int>(grid), stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pgg

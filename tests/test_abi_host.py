@@ -188,3 +188,26 @@ def test_forward_plan_and_host_errors(lib):
         "PGG_ERR_NULL"
     assert pgg.STATUS[pgg.pgg_fwd_execute(fake + 1, *args[1:], pgg.PGG_BF16, fake, need, fake,
                                           None)] == "PGG_ERR_ALIGN"
+
+
+def test_unpermute_grad_host_errors(lib):
+    assert pgg.pgg_unpermute_grad_workspace_size(108000, 13500, 8) == 256 + 432128  # 4 M, 256-aligned
+    with pytest.raises(pgg.PggError):
+        pgg.pgg_unpermute_grad_workspace_size(108000, 13499, 8)
+    fake = 1 << 20
+    need = pgg.pgg_unpermute_grad_workspace_size(1000, 250, 4)
+    base = dict(permuted=fake, d_out=fake, probs=fake, expandedRowIdx=fake, M=1000, H=512,
+                batch=250, topK=4, rowIdxType=0, dtype=pgg.PGG_BF16,
+                probs_grad_dtype=pgg.PGG_BF16, workspace=fake, workspace_bytes=need,
+                perm_grad=fake, probs_grad=fake, stream=None)
+
+    def code(**o):
+        a = dict(base, **o)
+        return pgg.STATUS[pgg.pgg_unpermute_grad(**a)]
+
+    assert code(probs_grad_dtype=pgg.PGG_F16) == "PGG_ERR_DTYPE"
+    assert code(workspace_bytes=need - 1) == "PGG_ERR_WORKSPACE"
+    assert code(probs_grad=0) == "PGG_ERR_NULL"
+    assert code(d_out=fake + 1) == "PGG_ERR_ALIGN"
+    assert code(rowIdxType=2) == "PGG_ERR_ATTR"
+    assert code(M=999) == "PGG_ERR_SHAPE"

@@ -1,0 +1,163 @@
+"""GPU parity of the probs-weighted unpermute backward against the fp64 oracle.
+
+perm_grad is d_out * prob rounded once to the dtype: per element |GPU - oracle|
+<= 2^-8 |oracle| (bf16; 2^-11 fp16; 2^-23 fp32). probs_grad is an fp32 sum
+over h: |GPU - oracle| <= 1e-4 * max |oracle| plus the same one rounding when
+it is returned in a 16-bit dtype.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_case, make_inputs
+from workloads.moe import unpermute_inputs, with_row_idx_type
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+ROUND = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11, torch.float32: 2.0 ** -23}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from permute_grouped_gemm_gb300 import build as pbuild
+    pbuild.build()
+    oracle.build()
+    pgg.load()
+    yield
+
+
+def run(inp, d_out, probs, **kw):
+    pg, qg, ws = pgg.unpermute_grad(inp.grad_y, d_out, probs, inp.expanded_row_idx, inp.top_k,
+                                    inp.row_idx_type, **kw)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0, pgg.STATUS.get(pgg.status(ws))
+    return pg, qg
+
+
+def ref_of(inp, d_out, probs):
+    return oracle.unpermute_grad(inp.grad_y, d_out, probs, inp.expanded_row_idx, inp.batch,
+                                 inp.top_k, inp.row_idx_type)
+
+
+def check_pg(pg, ref):
+    got = pg.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= ROUND[pg.dtype] * np.abs(ref))
+
+
+def check_qg(qg, ref):
+    got = qg.double().cpu().numpy()
+    r = ROUND[qg.dtype] if qg.dtype != torch.float32 else 0.0
+    bound = r * np.abs(ref) + TOL * np.abs(ref).max()
+    assert np.all(np.abs(got - ref) <= bound), np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("qg_f32", [False, True])
+@pytest.mark.parametrize("row_idx_type", [0, 1])
+@pytest.mark.parametrize("n", [256, 286, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+def test_cases(dtype, n, row_idx_type, qg_f32):
+    inp = make_case(batch=150, top_k=3, G=5, K=16, N=n, dtype=dtype, seed=41,
+                    row_idx_type=row_idx_type, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs, probs_grad_dtype=torch.float32 if qg_f32 else None)
+    rpg, rqg = ref_of(inp, d_out, probs)
+    check_pg(pg, rpg)
+    check_qg(qg, rqg)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_without_probs_is_an_exact_scatter_copy(dtype):
+    inp = make_case(batch=300, top_k=4, G=6, K=16, N=512, dtype=dtype, seed=42, device="cuda")
+    d_out, _ = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, None)
+    assert qg is None
+    b = inp.gather.to("cuda") // inp.top_k
+    assert torch.equal(pg.view(torch.int16 if dtype != "fp32" else torch.int32),
+                       d_out[b].view(torch.int16 if dtype != "fp32" else torch.int32))
+
+
+def test_bitwise_repeatable_and_index_forms():
+    inp = make_case(batch=400, top_k=8, G=16, K=16, N=1024, dtype="bf16", seed=43, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs)
+    for _ in range(2):
+        pg2, qg2 = run(inp, d_out, probs)
+        assert torch.equal(pg.view(torch.int16), pg2.view(torch.int16))
+        assert torch.equal(qg.view(torch.int16), qg2.view(torch.int16))
+    pg3, qg3 = run(with_row_idx_type(inp, 1), d_out, probs)
+    assert torch.equal(pg.view(torch.int16), pg3.view(torch.int16))
+    assert torch.equal(qg.view(torch.int16), qg3.view(torch.int16))
+
+
+def test_misaligned_pointers_use_the_scalar_path():
+    inp = make_case(batch=200, top_k=4, G=6, K=16, N=512, dtype="bf16", seed=44, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs)
+    buf = torch.empty(d_out.numel() + 1, dtype=d_out.dtype, device="cuda")
+    d_shift = buf[1:].view(d_out.shape)
+    d_shift.copy_(d_out)
+    pg2, qg2, ws = pgg.unpermute_grad(inp.grad_y, d_shift, probs, inp.expanded_row_idx,
+                                      inp.top_k, 0)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(pg.view(torch.int16), pg2.view(torch.int16))
+    rpg, rqg = ref_of(inp, d_out, probs)
+    check_qg(qg2, rqg)
+
+
+def test_index_errors_zero_the_outputs():
+    inp = make_case(batch=64, top_k=2, G=4, K=16, N=64, dtype="bf16", seed=45, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    for name, mutate in (("PGG_ERR_NOT_PERM", lambda i: i.__setitem__(5, int(i[6]))),
+                         ("PGG_ERR_INDEX", lambda i: i.__setitem__(5, 128))):
+        idx = inp.expanded_row_idx.clone()
+        mutate(idx)
+        pg = torch.full((128, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+        qg = torch.full((64, 2), 7.0, dtype=torch.bfloat16, device="cuda")
+        _, _, ws = pgg.unpermute_grad(inp.grad_y, d_out, probs, idx, 2, 0, perm_grad=pg,
+                                      probs_grad=qg)
+        torch.cuda.synchronize()
+        assert pgg.STATUS[pgg.status(ws)] == name
+        assert torch.count_nonzero(pg) == 0 and torch.count_nonzero(qg) == 0
+
+
+def test_chained_into_the_fused_input_gradient():
+    # perm_grad is the gradY of the fused d_x backward
+    inp = make_case(batch=256, top_k=4, G=8, K=384, N=256, dtype="bf16", seed=46, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, _ = run(inp, d_out, probs)
+    dx, ws = pgg.dx(pg, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k, 0)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    ref = oracle.dx(pg, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k, 0)
+    got = dx.double().cpu().numpy()
+    assert np.abs(got - ref).max() <= TOL * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("name", ["uniform-bf16", "large-bf16", "skewed-fp16"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs)
+    # the oracle on a token sample: rebuild a small problem from those tokens
+    toks = np.sort(np.random.default_rng(5).choice(w.batch, 32, replace=False))
+    pos = (toks[:, None] * w.top_k + np.arange(w.top_k)[None, :]).reshape(-1)
+    gather = inp.gather.numpy()
+    row_of = np.empty_like(gather)
+    row_of[gather] = np.arange(gather.shape[0])
+    rows = row_of[pos]
+    d = d_out.double().cpu().numpy()[toks]
+    pr = probs.double().cpu().numpy()[toks]
+    perm = inp.grad_y[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    want_pg = d[np.arange(32).repeat(w.top_k)] * pr.reshape(-1)[:, None]
+    want_qg = np.einsum("ph,ph->p", d[np.arange(32).repeat(w.top_k)], perm).reshape(32, w.top_k)
+    check_pg(pg[torch.as_tensor(rows, device="cuda")], want_pg)
+    got_q = qg[torch.as_tensor(toks, device="cuda")]
+    check_qg(got_q, want_qg)
