@@ -64,9 +64,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--op", default="dx", choices=["dx", "dw", "fwd"],
+    ap.add_argument("--op", default="dx", choices=["dx", "dw", "fwd", "unperm"],
                     help="dx: the fused input gradient (default); dw: the weight gradient; "
-                         "fwd: the forward")
+                         "fwd: the forward; unperm: the probs-weighted unpermute backward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -377,7 +377,68 @@ class FwdOp(DxOp):
         return self.inp.workload.M
 
 
-OPS = {"dx": DxOp, "dw": DwOp, "fwd": FwdOp}
+class UnpermOp(DxOp):
+    """The probs-weighted unpermute backward (perm_grad and probs_grad)."""
+    name = "unperm"
+    metric = ("probs-weighted unpermute backward GB/s (algorithmic bytes / s) & % of HBM roofline, "
+              "1xGB300")
+    unit = "GB/s"
+
+    def __init__(self, inp, pgg, dev):
+        import torch
+        from workloads.moe import unpermute_inputs
+        self.inp, self.pgg = inp, pgg
+        w = inp.workload
+        self.dt = pgg.dtype_code(inp.grad_y.dtype)
+        self.sizes = (w.M, w.N, w.batch, w.top_k)
+        self.plan = {"variant": 0, "threads": 256, "ctas_per_token": 1}
+        self.ws_bytes = pgg.pgg_unpermute_grad_workspace_size(w.M, w.batch, w.top_k)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.d_out, self.probs = unpermute_inputs(inp, dev)
+        self.out = torch.empty(w.M, w.N, dtype=inp.grad_y.dtype, device=dev)
+        self.qg = torch.empty(w.batch, w.top_k, dtype=inp.grad_y.dtype, device=dev)
+        self.kernel = "unpermute_grad_kernel"
+
+    def values(self):
+        return self.inp.grad_y, self.d_out
+
+    def stage1(self, idx, gl, sp):
+        return 0  # index validation runs inside the call
+
+    def stage2(self, a, b, idx, gl, out, sp):
+        w = self.inp.workload
+        return self.pgg.pgg_unpermute_grad(a.data_ptr(), b.data_ptr(), self.probs.data_ptr(),
+                                           idx.data_ptr(), w.M, w.N, w.batch, w.top_k,
+                                           w.row_idx_type, self.dt, self.dt, self.ws.data_ptr(),
+                                           self.ws_bytes, out.data_ptr(), self.qg.data_ptr(), sp)
+
+    def execute(self, a, b, idx, gl, out, sp):
+        return self.stage2(a, b, idx, gl, out, sp)
+
+    def algorithmic(self):
+        """(flops, bytes): 3*M*N (scale + dot); bytes: d_out once, permuted once,
+        perm_grad written once, probs and probs_grad, the index."""
+        w = self.inp.workload
+        es = {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+        flops = 3 * w.M * w.N
+        nbytes = (w.batch * w.N * es + 2 * w.M * w.N * es + 2 * w.M * es + w.M * 8)
+        return flops, nbytes
+
+    def oracle_sample(self, host, rng, n):
+        import oracle
+        w = host.workload
+        if not hasattr(self, "_host"):
+            self._host = (self.d_out.cpu(), self.probs.cpu())
+        oracle.unpermute_grad(host.grad_y, self._host[0], self._host[1], host.expanded_row_idx,
+                              w.batch, w.top_k, w.row_idx_type)
+        _, nbytes = self.algorithmic()
+        return nbytes, f"all {w.batch} tokens (whole problem: the oracle has no token sample)"
+
+    def units(self):
+        return 1
+
+
+OPS = {"dx": DxOp, "dw": DwOp, "fwd": FwdOp, "unperm": UnpermOp}
 
 
 def cpu_baseline(op, target_s: float):
@@ -396,7 +457,11 @@ def cpu_baseline(op, target_s: float):
         t0 = time.perf_counter()
         flops, desc = op.oracle_sample(host, rng, n)
         dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, n),
+    if getattr(op, "unit", "TFLOP/s") == "GB/s":
+        value, unit = flops / dt / 1e9, "GB/s"  # oracle_sample returns bytes for this op
+    else:
+        value, unit = flops / dt / 1e12, "TFLOP/s"
+    return {"value": value, "unit": unit, "cores": min(cores, n),
             "kind": "oracle", "sample": f"{desc}, fp64 C++ loops, {dt:.1f} s"}
 
 
@@ -415,6 +480,9 @@ def run_reference(args):
     if args.op in ("dw", "fwd"):
         from workloads.moe import forward_input
         op.x = forward_input(inp, "cpu")
+    if args.op == "unperm":
+        from workloads.moe import unpermute_inputs
+        op.d_out, op.probs = unpermute_inputs(inp, "cpu")
     cores = oracle.host_cores()
     # size each step to ~ (a few minutes) / (steps + warmup)
     budget = 150.0 / max(1, args.steps + args.warmup)
@@ -432,17 +500,20 @@ def run_reference(args):
             times.append(time.perf_counter() - t0)
             flops += flops_s
     dt = sum(times)
-    value = flops / dt / 1e12
+    if getattr(op, "unit", "TFLOP/s") == "GB/s":
+        value, unit = flops / dt / 1e9, "GB/s"  # oracle_sample returns bytes for this op
+    else:
+        value, unit = flops / dt / 1e12, "TFLOP/s"
     sample = f"{desc} per step, fp64 C++ loops"
     line = {
-        "impl": "reference", "metric": op.metric, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": op.metric, "value": value, "unit": unit,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / max(1, len(times)) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {**w.describe(), "op": args.op, "sample_units": n},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(cores, n),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": min(cores, n),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -527,7 +598,11 @@ def run_ours(args):
         mean_step, mean_gemm = float(t[0]), float(t[1])
 
     flops, nbytes = op.algorithmic()
-    value = world * flops / (mean_step * 1e-3) / 1e12
+    if getattr(op, "unit", "TFLOP/s") == "GB/s":
+        value = world * nbytes / (mean_step * 1e-3) / 1e9
+    else:
+        value = world * flops / (mean_step * 1e-3) / 1e12
+    value_unit = getattr(op, "unit", "TFLOP/s")
 
     peaks, peak_src = load_peaks()
     clocks = clk.summary()
@@ -561,10 +636,10 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(op, pgg, w, dev, stream, flops, world, dist)
+        e2e = measure_e2e(op, pgg, w, dev, stream, flops, nbytes, world, dist)
 
     line = {
-        "metric": op.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": op.metric, "value": value, "unit": value_unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded; routing and value recipe in DESIGN.md)",
@@ -593,7 +668,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_e2e(op, pgg, w, dev, stream, flops, world, dist):
+def measure_e2e(op, pgg, w, dev, stream, flops, nbytes, world, dist):
     """Same metric through the public call with host buffers: every step copies
     the inputs from pinned host memory, runs the execute call and copies the
     result back."""
@@ -635,7 +710,11 @@ def measure_e2e(op, pgg, w, dev, stream, flops, world, dist):
         ms = float(t[0])
     if not torch.equal(h_out, d_out.cpu()):
         raise RuntimeError("e2e readback mismatch")
-    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    if getattr(op, "unit", "TFLOP/s") == "GB/s":
+        value, unit = world * nbytes / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        value, unit = world * flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    return {"value": value, "unit": unit,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
