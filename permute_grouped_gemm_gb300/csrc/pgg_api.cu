@@ -49,8 +49,8 @@ cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_ti
                             cudaStream_t stream);
 cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, int32_t* inv,
                               WsHeader* hdr, int num_sms, cudaStream_t stream);
-cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, int num_sms,
-                                  cudaStream_t stream);
+cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, bool pairs,
+                                  int num_sms, cudaStream_t stream);
 
 namespace {
 
@@ -807,8 +807,11 @@ int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* prob
     return PGG_ERR_CUDA;
   const bool vec = (H * static_cast<int64_t>(es)) % 16 == 0 && aligned(d_out, 16) &&
                    aligned(perm_grad, 16) && (!probs || aligned(permuted, 16));
-  return launch_unpermute_grad(dtype, a, vec, di.num_sms, s) == cudaSuccess ? PGG_OK
-                                                                             : PGG_ERR_CUDA;
+  const bool pairs = H % 2 == 0 && aligned(d_out, 4) && aligned(perm_grad, 4) &&
+                     (!probs || aligned(permuted, 4));
+  return launch_unpermute_grad(dtype, a, vec, pairs, di.num_sms, s) == cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
 }
 
 const char* pgg_status_string(int status) {

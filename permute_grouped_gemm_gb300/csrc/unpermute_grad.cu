@@ -8,11 +8,11 @@
 //
 // perm_grad is the d_y that the fused d_x backward and the weight gradient
 // take. Bound by HBM: d_out is read once per token (its re-reads for the
-// token's topK rows hit L1), permuted is read once and perm_grad written
-// once. One 256-thread CTA per token (grid-stride); 16-byte loads and stores
-// along h when the rows allow it; the dot product in fp32, each thread over
-// its own positions in increasing order, then a fixed shuffle and
-// shared-memory tree, so that it is bitwise repeatable.
+// token's topK rows hit L1 or L2), permuted is read once and perm_grad
+// written once. One warp per original position (grid-stride), four 16-byte
+// loads per lane in flight when the rows allow 16-byte access; the dot
+// product in fp32, each lane over its own positions in increasing order, then
+// a fixed shuffle tree, so that it is bitwise repeatable.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -101,24 +101,11 @@ __device__ __forceinline__ uint4 pack16(const float* f) {
   }
 }
 
-// Sum over the block in a fixed order: shuffle tree in each warp, then the
-// warps' sums added by thread 0 in warp order.
-__device__ __forceinline__ float block_sum(float v, float* s_part) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
-  __syncthreads();  // s_part of the previous call has been read
-  if (lane == 0) s_part[warp] = v;
-  __syncthreads();
-  float t = 0.0f;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < kUThreads / 32; ++w) t += s_part[w];
-  return t;
-}
-
-template <int DT, bool PROBS, bool VEC>
+// One warp per original position p = b * topK + j: it reads d_out[b] (shared
+// with the token's other positions through L1), permuted[row], writes
+// perm_grad[row] and reduces the dot product with a fixed shuffle tree.
+template <int DT, bool PROBS, bool VEC, bool PAIRS>
 __global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermArgs a) {
-  __shared__ float s_part[kUThreads / 32];
   using E = Elem<DT>;
   const uint32_t st = a.hdr->status;
   if (st == kStIndex || st == kStGroupSum || st == kStNotPerm) {
@@ -135,81 +122,147 @@ __global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermA
       }
     return;
   }
+  const int lane = threadIdx.x & 31;
   const int64_t H = a.H;
-  for (int64_t b = blockIdx.x; b < a.batch; b += gridDim.x) {
-    for (int64_t j = 0; j < a.topK; ++j) {
-      const int64_t p = b * a.topK + j;
-      const int64_t row = a.row_idx_type == 0 ? static_cast<int64_t>(a.inv[p]) : a.idx[p];
-      const float pr = PROBS ? E::get(a.probs, p) : 1.0f;
-      float dot = 0.0f;
-      if constexpr (VEC) {
-        constexpr int kE = E::kPer16;
-        constexpr int64_t kEs = DT == PGG_F32 ? 4 : 2;  // bytes per element
-        const uint4* d4 =
-            reinterpret_cast<const uint4*>(static_cast<const char*>(a.dout) + b * H * kEs);
-        const uint4* p4 = PROBS ? reinterpret_cast<const uint4*>(
-                                      static_cast<const char*>(a.perm) + row * H * kEs)
-                                : nullptr;
-        uint4* g4 = reinterpret_cast<uint4*>(static_cast<char*>(a.perm_grad) + row * H * kEs);
-        for (int64_t v = threadIdx.x; v < H / kE; v += kUThreads) {
-          float d[kE], o[kE];
-          unpack16<DT>(d4[v], d);
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kUThreads / 32);
+  for (int64_t p = static_cast<int64_t>(blockIdx.x) * (kUThreads / 32) + (threadIdx.x >> 5);
+       p < a.M; p += warps) {
+    const int64_t b = p / a.topK;
+    const int64_t row = a.row_idx_type == 0 ? static_cast<int64_t>(a.inv[p]) : a.idx[p];
+    const float pr = PROBS ? E::get(a.probs, p) : 1.0f;
+    float dot = 0.0f;
+    if constexpr (VEC) {
+      constexpr int kE = E::kPer16;
+      constexpr int64_t kEs = DT == PGG_F32 ? 4 : 2;  // bytes per element
+      const uint4* d4 =
+          reinterpret_cast<const uint4*>(static_cast<const char*>(a.dout) + b * H * kEs);
+      const uint4* p4 =
+          PROBS ? reinterpret_cast<const uint4*>(static_cast<const char*>(a.perm) + row * H * kEs)
+                : nullptr;
+      uint4* g4 = reinterpret_cast<uint4*>(static_cast<char*>(a.perm_grad) + row * H * kEs);
+      const int64_t nv = H / kE;
+      constexpr int kU = 4;  // vectors per lane in flight
+      for (int64_t v0 = lane; v0 < nv; v0 += 32 * kU) {
+        uint4 dq[kU], pq[kU];
 #pragma unroll
-          for (int i = 0; i < kE; ++i) o[i] = d[i] * pr;
-          g4[v] = pack16<DT>(o);
-          if constexpr (PROBS) {
-            float x[kE];
-            unpack16<DT>(__ldg(p4 + v), x);
-#pragma unroll
-            for (int i = 0; i < kE; ++i) dot = fmaf(d[i], x[i], dot);
+        for (int u = 0; u < kU; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            dq[u] = __ldg(d4 + v);
+            if constexpr (PROBS) pq[u] = __ldg(p4 + v);
           }
         }
-      } else {
-        for (int64_t h = threadIdx.x; h < H; h += kUThreads) {
-          const float d = E::get(a.dout, b * H + h);
-          E::put(a.perm_grad, row * H + h, d * pr);
-          if constexpr (PROBS) dot = fmaf(d, E::get(a.perm, row * H + h), dot);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            float d[kE], o[kE];
+            unpack16<DT>(dq[u], d);
+#pragma unroll
+            for (int i = 0; i < kE; ++i) o[i] = d[i] * pr;
+            g4[v] = pack16<DT>(o);
+            if constexpr (PROBS) {
+              float x[kE];
+              unpack16<DT>(pq[u], x);
+#pragma unroll
+              for (int i = 0; i < kE; ++i) dot = fmaf(d[i], x[i], dot);
+            }
+          }
         }
       }
-      if constexpr (PROBS) {
-        const float t = block_sum(dot, s_part);
-        if (threadIdx.x == 0 && a.probs_grad) {
-          if (a.probs_grad_f32)
-            static_cast<float*>(a.probs_grad)[p] = t;
-          else
-            E::put(a.probs_grad, p, t);
+    } else if (PAIRS) {
+      // 16-bit rows of even length, 4-byte aligned: two elements per access
+      const uint32_t* d2 = reinterpret_cast<const uint32_t*>(
+          static_cast<const uint16_t*>(a.dout) + b * H);
+      const uint32_t* p2 = PROBS ? reinterpret_cast<const uint32_t*>(
+                                       static_cast<const uint16_t*>(a.perm) + row * H)
+                                 : nullptr;
+      uint32_t* g2 = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.perm_grad) + row * H);
+      const int64_t nv = H / 2;
+      constexpr int kU = 8;
+      for (int64_t v0 = lane; v0 < nv; v0 += 32 * kU) {
+        uint32_t dq[kU], pq[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            dq[u] = __ldg(d2 + v);
+            if constexpr (PROBS) pq[u] = __ldg(p2 + v);
+          }
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            const uint4 dd = make_uint4(dq[u], 0, 0, 0);
+            float d[8];
+            unpack16<DT>(dd, d);
+            float o[8] = {d[0] * pr, d[1] * pr, 0, 0, 0, 0, 0, 0};
+            g2[v] = pack16<DT>(o).x;
+            if constexpr (PROBS) {
+              float x[8];
+              unpack16<DT>(make_uint4(pq[u], 0, 0, 0), x);
+              dot = fmaf(d[0], x[0], dot);
+              dot = fmaf(d[1], x[1], dot);
+            }
+          }
+        }
+      }
+    } else {
+      for (int64_t h = lane; h < H; h += 32) {
+        const float d = E::get(a.dout, b * H + h);
+        E::put(a.perm_grad, row * H + h, d * pr);
+        if constexpr (PROBS) dot = fmaf(d, E::get(a.perm, row * H + h), dot);
+      }
+    }
+    if constexpr (PROBS) {
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, d);
+      if (lane == 0 && a.probs_grad) {
+        if (a.probs_grad_f32)
+          static_cast<float*>(a.probs_grad)[p] = dot;
+        else
+          E::put(a.probs_grad, p, dot);
       }
     }
   }
 }
 
-template <int DT>
-cudaError_t launch_t(const UnpermArgs& a, bool probs, bool vec, int grid, cudaStream_t s) {
-  if (probs && vec)
-    unpermute_grad_kernel<DT, true, true><<<grid, kUThreads, 0, s>>>(a);
-  else if (probs)
-    unpermute_grad_kernel<DT, true, false><<<grid, kUThreads, 0, s>>>(a);
-  else if (vec)
-    unpermute_grad_kernel<DT, false, true><<<grid, kUThreads, 0, s>>>(a);
+template <int DT, bool PROBS>
+void launch_p(const UnpermArgs& a, bool vec, bool pairs, int grid, cudaStream_t s) {
+  if (vec)
+    unpermute_grad_kernel<DT, PROBS, true, false><<<grid, kUThreads, 0, s>>>(a);
+  else if (pairs && DT != PGG_F32)
+    unpermute_grad_kernel<DT, PROBS, false, DT != PGG_F32><<<grid, kUThreads, 0, s>>>(a);
   else
-    unpermute_grad_kernel<DT, false, false><<<grid, kUThreads, 0, s>>>(a);
+    unpermute_grad_kernel<DT, PROBS, false, false><<<grid, kUThreads, 0, s>>>(a);
+}
+
+template <int DT>
+cudaError_t launch_t(const UnpermArgs& a, bool probs, bool vec, bool pairs, int grid,
+                     cudaStream_t s) {
+  if (probs)
+    launch_p<DT, true>(a, vec, pairs, grid, s);
+  else
+    launch_p<DT, false>(a, vec, pairs, grid, s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// vec: H * sizeof(dtype) a multiple of 16 and perm, d_out, perm_grad 16-byte aligned.
-cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, int num_sms,
-                                  cudaStream_t stream) {
-  int64_t grid = a.batch;
+// vec: H * sizeof(dtype) a multiple of 16 and perm, d_out, perm_grad 16-byte
+// aligned; pairs (16-bit dtypes): H even and those pointers 4-byte aligned.
+cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, bool pairs,
+                                  int num_sms, cudaStream_t stream) {
+  int64_t grid = (a.M + kUThreads / 32 - 1) / (kUThreads / 32);
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   const bool probs = a.probs != nullptr;
-  if (dtype == PGG_F32) return launch_t<PGG_F32>(a, probs, vec, static_cast<int>(grid), stream);
-  if (dtype == PGG_F16) return launch_t<PGG_F16>(a, probs, vec, static_cast<int>(grid), stream);
-  if (dtype == PGG_BF16) return launch_t<PGG_BF16>(a, probs, vec, static_cast<int>(grid), stream);
+  const int g = static_cast<int>(grid);
+  if (dtype == PGG_F32) return launch_t<PGG_F32>(a, probs, vec, false, g, stream);
+  if (dtype == PGG_F16) return launch_t<PGG_F16>(a, probs, vec, pairs, g, stream);
+  if (dtype == PGG_BF16) return launch_t<PGG_BF16>(a, probs, vec, pairs, g, stream);
   return cudaErrorInvalidValue;
 }
 

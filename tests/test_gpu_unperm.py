@@ -98,12 +98,14 @@ def test_bitwise_repeatable_and_index_forms():
     assert torch.equal(qg.view(torch.int16), qg3.view(torch.int16))
 
 
-def test_misaligned_pointers_use_the_scalar_path():
+@pytest.mark.parametrize("shift", [1, 2])
+def test_misaligned_pointers_use_the_narrower_paths(shift):
+    # shift 1 element: 2-byte accesses; 2 elements: 4-byte pairs
     inp = make_case(batch=200, top_k=4, G=6, K=16, N=512, dtype="bf16", seed=44, device="cuda")
     d_out, probs = unpermute_inputs(inp)
     pg, qg = run(inp, d_out, probs)
-    buf = torch.empty(d_out.numel() + 1, dtype=d_out.dtype, device="cuda")
-    d_shift = buf[1:].view(d_out.shape)
+    buf = torch.empty(d_out.numel() + shift, dtype=d_out.dtype, device="cuda")
+    d_shift = buf[shift:].view(d_out.shape)
     d_shift.copy_(d_out)
     pg2, qg2, ws = pgg.unpermute_grad(inp.grad_y, d_shift, probs, inp.expanded_row_idx,
                                       inp.top_k, 0)
