@@ -1,6 +1,6 @@
 """Builds libpgg.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Nine translation units compiled in parallel, then linked as a shared
+Ten translation units compiled in parallel, then linked as a shared
 library with the CUDA runtime linked statically; the driver API is reached at
 run time through cudaGetDriverEntryPointByVersion, so loading the library
 needs no libcuda.
@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libpgg.so")
 SOURCES = ["pgg_api.cu", "route_prep.cu", "gmm_dx.cu", "gmm_dx_simt.cu", "gmm_dw.cu",
-           "gmm_dw_simt.cu", "gmm_fwd.cu", "gmm_fwd_simt.cu", "unpermute_grad.cu"]
+           "gmm_dw_simt.cu", "gmm_fwd.cu", "gmm_fwd_simt.cu", "unpermute_grad.cu",
+           "gmm_dx_owner.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -729,6 +729,8 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
       args.out[q] = 0.0f;
     return;
   }
+  // After the owner kernel: nothing to do unless it had to leave the work here.
+  if (args.only_if_unsorted && args.hdr->unsorted == 0) return;
   const uint32_t total = args.hdr->n_row_blocks * static_cast<uint32_t>(args.k_units);
 
   if (threadIdx.x == 0) {

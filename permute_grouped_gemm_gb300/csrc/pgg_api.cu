@@ -47,6 +47,10 @@ void fwd_simt_tiles(int64_t N, int* n_blocks);
 int fwd_simt_smem_bytes();
 cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
                             cudaStream_t stream);
+int owner_smem_bytes();
+int owner_threads();
+cudaError_t launch_owner(int dtype, const DyMaps& dy, const CUtensorMap& tw, const OwnerArgs& a,
+                         int num_sms, cudaStream_t stream);
 cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, int32_t* inv,
                               WsHeader* hdr, int num_sms, cudaStream_t stream);
 cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, bool pairs,
@@ -61,7 +65,18 @@ std::atomic<int> g_force_variant{-1};
 std::atomic<int> g_band_k_blocks{0};
 
 constexpr int64_t kInt32Max = 2147483647;
-constexpr int kVariantSimt = 3;  // FP32-pipe kernel (gmm_dx_simt.cu)
+constexpr int kVariantSimt = 3;   // FP32-pipe kernel (gmm_dx_simt.cu)
+constexpr int kVariantOwner = 4;  // slab-owner kernel (gmm_dx_owner.cu), ticketed fallback
+
+// The owner variant pays off when a 256-token slab holds about 96 or more
+// rows of each expert (so its MMAs are wide), for 16-bit inputs, and when
+// there are enough (slab, 256-k) units to fill the GPU.
+bool owner_fits(int64_t K, int64_t G, int64_t batch, int64_t topK, int dtype) {
+  if (dtype == PGG_F32) return false;
+  const int64_t slabs = (batch + kSlabTokens - 1) / kSlabTokens;
+  const int64_t k_units = (K + 255) / 256;
+  return G * 96 <= kSlabTokens * topK && slabs * k_units >= 128;
+}
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -90,15 +105,23 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   std::memset(p, 0, sizeof(*p));
   p->dtype = dtype;
   int variant = g_force_variant.load();
-  if (variant < 0) variant = (M / G < 64) ? 1 : 0;
+  if (variant < 0) {
+    variant = (M / G < 64) ? 1 : 0;
+    if (owner_fits(K, G, batch, topK, dtype)) variant = kVariantOwner;
+  }
+  if (variant == kVariantOwner && dtype == PGG_F32) variant = 0;
   if (!rows_streamable(N, dtype)) variant = kVariantSimt;
   p->variant = variant;
   if (variant == kVariantSimt) {
     simt_config(&p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes);
-  } else if (!kernel_config(dtype, variant, &p->rows_per_block, &p->stages, &p->threads,
-                            &p->smem_bytes, &p->pair)) {
+  } else if (!kernel_config(dtype, variant == kVariantOwner ? 0 : variant, &p->rows_per_block,
+                            &p->stages, &p->threads, &p->smem_bytes, &p->pair)) {
+    // the owner variant keeps the ticketed kernel's (variant 0) row blocks for its fallback
     return PGG_ERR_DTYPE;
   }
+  p->n_slabs = variant == kVariantOwner
+                   ? static_cast<int>((batch + kSlabTokens - 1) / kSlabTokens)
+                   : 0;
   if (rows_override > 0) p->rows_per_block = rows_override;
   p->M = M;
   p->N = N;
@@ -132,6 +155,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
   L.rowinfo = take(sizeof(RowInfo) * static_cast<size_t>(M));
   L.n_tickets = (batch * p->k_blocks + 3) / 4 * 4;
   L.tickets = take(sizeof(uint32_t) * static_cast<size_t>(L.n_tickets));
+  L.seg = take(sizeof(int32_t) * static_cast<size_t>(G) * static_cast<size_t>(p->n_slabs + 1));
   L.total = a;
   return PGG_OK;
 }
@@ -277,6 +301,7 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   if (plan.variant == kVariantSimt || !aligned(gradY, 16) || !aligned(weight, 16))
     return run_simt(plan, gradY, weight, ws, out, di, stream);
   DyMaps tdy;
+  const bool owner = plan.variant == kVariantOwner;
   CUtensorMap tw;
   int rc = encode_maps(plan, gradY, weight, &tdy, &tw);
   if (rc != PGG_OK) return rc;
@@ -295,10 +320,32 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   a.nk = plan.nk;
   a.ticket_bias = g_ticket_bias.load();
   a.vec_rows = (plan.K % 4 == 0 && aligned(out, 16)) ? 1 : 0;
+  a.only_if_unsorted = owner ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
+  if (owner) {
+    OwnerArgs o;
+    o.off = reinterpret_cast<const int64_t*>(w + plan.layout.off);
+    o.seg = reinterpret_cast<const int32_t*>(w + plan.layout.seg);
+    o.rowinfo = a.rowinfo;
+    o.hdr = a.hdr;
+    o.out = out;
+    o.M = plan.M;
+    o.K = plan.K;
+    o.G = plan.G;
+    o.batch = plan.batch;
+    o.n_slabs = plan.n_slabs;
+    o.k_units = static_cast<int32_t>((plan.K + 255) / 256);
+    o.nk = plan.nk;
+    o.wait_limit_ns = a.wait_limit_ns;
+    if (launch_owner(plan.dtype, tdy, tw, o, di.num_sms, stream) != cudaSuccess)
+      return PGG_ERR_CUDA;
+  }
+  // the ticketed kernel; after the owner kernel it works only when that one
+  // could not (some expert's rows not in increasing original position)
   const int64_t max_ctas = plan.max_row_blocks * plan.k_units * (plan.pair ? 2 : 1);
   const int grid = static_cast<int>(max_ctas < di.num_sms ? max_ctas : di.num_sms);
-  return launch_grouped_gemm(plan.dtype, plan.variant, tdy, tw, a, grid, stream) == cudaSuccess
+  return launch_grouped_gemm(plan.dtype, owner ? 0 : plan.variant, tdy, tw, a, grid, stream) ==
+                 cudaSuccess
              ? PGG_OK
              : PGG_ERR_CUDA;
 }
@@ -540,16 +587,16 @@ int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
   if (rc != PGG_OK) return rc;
   info->variant = p.variant;
-  info->rows_per_block = p.rows_per_block;
+  info->rows_per_block = p.variant == kVariantOwner ? kSlabTokens : p.rows_per_block;
   info->k_per_block = kKBlock;
   info->stages = p.stages;
   info->k_blocks = p.k_blocks;
   info->band_k_blocks = p.band_k_blocks;
   info->max_row_blocks = p.max_row_blocks;
   info->workspace_bytes = p.layout.total;
-  info->threads = p.threads;
-  info->smem_bytes = p.smem_bytes;
-  info->cta_pair = p.pair;
+  info->threads = p.variant == kVariantOwner ? owner_threads() : p.threads;
+  info->smem_bytes = p.variant == kVariantOwner ? owner_smem_bytes() : p.smem_bytes;
+  info->cta_pair = p.variant == kVariantOwner ? 1 : p.pair;
   return PGG_OK;
 }
 

@@ -37,14 +37,18 @@ struct alignas(16) WsHeader {
   uint32_t sched_next;    // dynamic tile counter of the grouped-GEMM kernel
   uint32_t n_row_blocks;  // number of non-empty row blocks
   uint32_t timeout_site;  // where a bounded wait ran out (diagnostic)
-  uint32_t pad[12];
+  uint32_t unsorted;      // 1: some expert's rows are not in increasing original position
+  uint32_t pad[11];
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
 
 struct Layout {
-  size_t hdr, off, rbstart, rblist, inv, rowinfo, tickets, total;
+  size_t hdr, off, rbstart, rblist, inv, rowinfo, tickets, seg, total;
   int64_t n_tickets;  // batch * k_blocks, rounded up to a multiple of 4
 };
+
+// Token slabs of the owner variant of the d_x kernel (gmm_dx_owner.cu).
+constexpr int kSlabTokens = 256;
 
 struct Plan {
   int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single
@@ -63,6 +67,7 @@ struct Plan {
   int64_t M, N, K, G, batch, topK;
   int row_idx_type;
   int nk;  // reduction steps: ceil(N / elements per 128-byte row)
+  int n_slabs;  // owner variant: ceil(batch / kSlabTokens); 0 otherwise
   Layout layout;
 };
 
@@ -88,6 +93,21 @@ struct GemmArgs {
   uint32_t ticket_bias;
   int32_t vec_rows;  // 1: epilogue writes 512-byte row segments with v4 stores / reductions
                      // (needs K % 4 == 0); 0: one 128-byte scalar store / reduction per warp
+  int32_t only_if_unsorted;  // 1: the owner kernel ran first; do the work only if it could not
+  uint64_t wait_limit_ns;
+};
+
+// Arguments of the owner variant of the d_x kernel (gmm_dx_owner.cu).
+struct OwnerArgs {
+  const int64_t* off;     // [G + 1] first expanded row of each expert
+  const int32_t* seg;     // [G][n_slabs + 1] first row of expert g with token >= slab * 256
+  const RowInfo* rowinfo; // [M]
+  WsHeader* hdr;
+  float* out;             // [batch, K]
+  int64_t M, K, G, batch;
+  int32_t n_slabs;
+  int32_t k_units;  // ceil(K / 256): k ranges of a CTA pair
+  int32_t nk;       // ceil(N / 64): reduction steps
   uint64_t wait_limit_ns;
 };
 

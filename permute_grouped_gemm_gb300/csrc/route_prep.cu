@@ -3,7 +3,8 @@
 // list of blocks over all non-empty experts, and the inverse of the routing
 // index for rowIdxType 1).
 //
-// Three small launches, in stream order:
+// Three small launches (four for the owner variant of the d_x kernel), in
+// stream order:
 //   route_scan     (1 CTA)  exclusive scan of groupList -> off[G+1]; row-block
 //                           counts and their scan -> rbstart[G+1]; the row-block
 //                           list {expert, first row, rows}; header reset; the
@@ -13,6 +14,9 @@
 //   route_rank     (grid)   per token b: its topK expanded rows, the check that
 //                           the index is a permutation, and each row's rank
 //                           among the token's rows (increasing expanded index).
+//   route_owner    (grid)   owner variant only: whether each expert's rows are
+//                           in increasing original position, and where each
+//                           256-token slab starts inside each expert.
 //
 // The index is read as the constraint table and note 1 of section "输入输出"
 // state: rowIdxType 0 maps expanded row -> original position, rowIdxType 1
@@ -104,6 +108,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int64_t* __restr
     hdr->sched_next = 0;
     hdr->n_row_blocks = static_cast<uint32_t>(n_rb);
     hdr->timeout_site = 0;
+    hdr->unsorted = 0;
   }
   __syncthreads();
   for (int64_t e = tid; e < n_rb; e += blockDim.x) {
@@ -196,6 +201,56 @@ __global__ void header_reset_kernel(WsHeader* hdr) {
   hdr->sched_next = 0;
   hdr->n_row_blocks = 0;
   hdr->timeout_site = 0;
+  hdr->unsorted = 0;
+}
+
+// Original position of expanded row i (valid once the index is a permutation).
+__device__ __forceinline__ int64_t position_of_row(const int64_t* idx, const int32_t* inv,
+                                                   int64_t i, int row_idx_type) {
+  return row_idx_type == 0 ? idx[i] : static_cast<int64_t>(inv[i]);
+}
+
+// Owner variant: (1) whether every expert's rows are in increasing original
+// position (then the rows of a token slab form one contiguous range inside
+// each expert); (2) seg[g][s] = first row of expert g whose position is at
+// least s * kSlabTokens * topK (binary search, meaningful when sorted).
+__global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                                   const int64_t* __restrict__ off, int64_t M, int64_t G,
+                                   int64_t top_k, int row_idx_type, int n_slabs,
+                                   int32_t* __restrict__ seg, WsHeader* hdr) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
+  bool unsorted = false;
+  for (int64_t i = t0; i + 1 < M; i += stride) {
+    // expert of row i: largest g with off[g] <= i
+    int64_t lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (off[mid] <= i)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    if (i + 1 < off[lo + 1] &&
+        position_of_row(idx, inv, i, row_idx_type) > position_of_row(idx, inv, i + 1, row_idx_type))
+      unsorted = true;
+  }
+  if (unsorted) atomicOr(&hdr->unsorted, 1u);
+  const int64_t n_seg = G * (n_slabs + 1);
+  for (int64_t q = t0; q < n_seg; q += stride) {
+    const int64_t g = q / (n_slabs + 1), s = q - g * (n_slabs + 1);
+    const int64_t p0 = s * kSlabTokens * top_k;
+    int64_t lo = off[g], hi = off[g + 1];  // first row in [lo, hi) with position >= p0
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (position_of_row(idx, inv, mid, row_idx_type) < p0)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    seg[q] = static_cast<int32_t>(lo);
+  }
 }
 
 // Every original position must have an expanded row (see row_of_position).
@@ -252,6 +307,14 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
   if (rblocks < 1) rblocks = 1;
   route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
       idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+  if (plan.n_slabs > 0) {
+    int64_t oblocks = (plan.M + 255) / 256;
+    if (oblocks > cap) oblocks = cap;
+    if (oblocks < 1) oblocks = 1;
+    route_owner_kernel<<<static_cast<int>(oblocks), 256, 0, stream>>>(
+        idx, inv, off, plan.M, plan.G, plan.topK, plan.row_idx_type, plan.n_slabs,
+        reinterpret_cast<int32_t*>(ws + L.seg), hdr);
+  }
   return cudaGetLastError();
 }
 

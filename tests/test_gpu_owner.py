@@ -1,0 +1,140 @@
+"""GPU parity of the slab-owner variant of the fused d_x backward (plan variant 4).
+
+The owner kernel adds each token's rows in the same order as the ticketed
+kernel (increasing expanded index), so the two agree bit for bit; both match
+the fp64 oracle within 1e-4 * max |d_x_ref|. When some expert's rows are not in
+increasing original position the ticketed kernel launched after it does the
+work.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_case, make_inputs
+from workloads.moe import Inputs, with_row_idx_type
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from permute_grouped_gemm_gb300 import build as pbuild
+    pbuild.build()
+    oracle.build()
+    pgg.load()
+    yield
+    pgg.pgg_debug_force_variant(-1)
+
+
+def run(inp, variant=-1):
+    try:
+        pgg.pgg_debug_force_variant(variant)
+        out, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                         inp.top_k, inp.row_idx_type)
+        torch.cuda.synchronize()
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert pgg.status(ws) == 0, pgg.STATUS.get(pgg.status(ws))
+    return out
+
+
+def check(inp, out, tokens=None, what=""):
+    ref = oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                    inp.top_k, inp.row_idx_type, tokens=tokens)
+    got = out.double().cpu().numpy()
+    if tokens is not None:
+        got = got[np.asarray(tokens)]
+    err = np.abs(got - ref).max()
+    assert err <= TOL * np.abs(ref).max(), f"{what}: {err:.3e}"
+
+
+def test_uniform_workload_plans_the_owner_variant():
+    w = WORKLOADS["uniform-bf16"]
+    p = pgg.pgg_dx_plan(w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k, 0, pgg.PGG_BF16)
+    assert p["variant"] == 4 and p["rows_per_block"] == 256 and p["cta_pair"] == 1
+
+
+CASES = {
+    "uniform_small": dict(batch=1024, top_k=8, G=16, K=512, N=256),
+    "ragged_k_n_batch": dict(batch=700, top_k=4, G=7, K=400, N=328),
+    "empty_experts": dict(batch=600, top_k=3, G=9, K=256, N=192, routing="zipf", zipf_zero=3),
+    "same_expert_twice": dict(batch=500, top_k=4, G=3, K=384, N=128, routing="replacement"),
+    "top1": dict(batch=900, top_k=1, G=4, K=256, N=256),
+    "k_is_1": dict(batch=300, top_k=3, G=4, K=1, N=256),
+    "many_rows_per_expert": dict(batch=2000, top_k=2, G=2, K=256, N=128),
+}
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_owner_matches_oracle_and_ticketed_kernel_bitwise(case, dtype):
+    inp = make_case(dtype=dtype, seed=51, device="cuda", **CASES[case])
+    owner = run(inp, 4)
+    check(inp, owner, what=case)
+    ticketed = run(inp, 0)
+    assert torch.equal(owner.view(torch.int32), ticketed.view(torch.int32)), case
+
+
+def test_index_forms_and_repeat_bitwise():
+    inp = make_case(batch=1024, top_k=8, G=16, K=512, N=256, dtype="bf16", seed=52,
+                    device="cuda")
+    a = run(inp, 4)
+    for _ in range(3):
+        assert torch.equal(run(inp, 4).view(torch.int32), a.view(torch.int32))
+    b = run(with_row_idx_type(inp, 1), 4)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def _unsorted(inp):
+    """The same problem with two rows of expert 0 swapped in the expanded order
+    (still a valid routing; the expert's rows no longer in increasing position)."""
+    gather = inp.gather.clone()
+    i, j = 0, 1  # rows 0 and 1 both belong to expert 0 (its count is large here)
+    assert int(inp.group_list[0]) >= 2
+    gather[i], gather[j] = gather[j].clone(), gather[i].clone()
+    dy = inp.grad_y.clone()
+    dy[[i, j]] = dy[[j, i]]
+    idx = gather if inp.row_idx_type == 0 else torch.argsort(gather)
+    return Inputs(inp.workload, dy, inp.weight, idx.to(dy.device), inp.group_list, inp.experts,
+                  gather)
+
+
+@pytest.mark.parametrize("row_idx_type", [0, 1])
+def test_unsorted_rows_fall_back_to_the_ticketed_kernel(row_idx_type):
+    base = make_case(batch=1024, top_k=8, G=16, K=512, N=256, dtype="bf16", seed=53,
+                     row_idx_type=row_idx_type, device="cuda")
+    inp = _unsorted(base)
+    out = run(inp, 4)
+    check(inp, out, what="unsorted")
+    assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
+
+
+def test_device_errors_zero_the_output_in_owner_mode():
+    base = make_case(batch=512, top_k=8, G=16, K=256, N=128, dtype="bf16", seed=54, device="cuda")
+    idx = base.expanded_row_idx.clone()
+    idx[5] = idx[6]
+    out = torch.full((512, 256), 7.0, device="cuda")
+    try:
+        pgg.pgg_debug_force_variant(4)
+        _, ws = pgg.dx(base.grad_y, base.weight, idx, base.group_list, 512, 8, 0, out=out)
+        torch.cuda.synchronize()
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_NOT_PERM"
+    assert torch.count_nonzero(out) == 0
+
+
+def test_uniform_workload_full_size():
+    w = WORKLOADS["uniform-bf16"]
+    inp = make_inputs(w, device="cuda")
+    out = run(inp)
+    toks = np.sort(np.random.default_rng(7).choice(w.batch, 64, replace=False))
+    check(inp, out, tokens=toks, what=w.name)
+    assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
