@@ -2,30 +2,32 @@
 // design", section "数学定义和公式": d_x[b, k] = sum over the token's rows i of
 // sum_n d_y[i, n] * weight[g(i), k, n]), for problems with few experts.
 //
-// A CTA pair owns a block of d_x outright: 256 tokens (a slab) x 256 k (128
-// per CTA). It walks the experts in increasing order; for each expert it
+// A CTA pair owns a block of d_x outright: a slab of T tokens (T <= 256, set
+// by the host so that a slab holds about 112 rows of each expert) x 256 k
+// (128 per CTA). It walks the experts in increasing order; for each expert it
 // takes the expert's rows whose tokens lie in the slab (one contiguous range
 // when each expert's rows are in increasing original position, which the
-// routing step checks), computes C = d_y[rows] @ weight[g]^T for its 256 k
-// on the tensor cores (cta_group::2, M = 256 k, N = rows rounded up to 32,
-// TMA for both operands, accumulators in tensor memory), and adds each row
-// into d_x with plain loads and stores. Every d_x element is then written by
-// one thread only, in program order, in increasing expanded index (increasing
-// expert, then increasing row within the expert): the same order of
-// additions as the ticketed kernel, with no tickets, no waits on other CTAs
-// and no atomics. A token's first row stores, later rows load, add and store;
-// two rows of one token inside one expert are adjacent and carried in a
-// register.
+// routing step checks), computes C = weight[g] d_y[rows]^T for its 256 k on
+// the tensor cores (cta_group::2, M = 256 k, N = rows rounded up to 32 and at
+// most 128, TMA for both operands, accumulators in tensor memory), and adds
+// each row into a shared-memory copy of the slab's d_x block. Each epilogue
+// thread owns one d_x column k of the slab, for every token: it alone reads,
+// adds and writes that column, in program order, in increasing expanded index
+// (increasing expert, then increasing row within the expert), which is the
+// order of additions of the ticketed kernel, with no tickets, no barriers
+// between threads and no atomics. A token's first row (rank 0) stores, later
+// rows load, add and store; two rows of one token inside one expert are
+// adjacent and carried in a register. When the slab is done each thread
+// writes its column to d_x once.
 //
 // When some expert's rows are not in increasing original position the kernel
 // leaves at once and the ticketed kernel, launched after it, does the work.
 //
 // Warp roles per CTA: 0 TMA; 1 tensor-memory allocation and (even CTA) MMA
-// issue; 2-5 epilogue (one group, so that one thread owns each d_x column
-// through all of the slab's rows). Units (slab, k range) are statically
-// interleaved over the clusters. Waits are bounded; when one runs out the
-// kernel records PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor
-// memory and returns.
+// issue; 2-5 epilogue. Units (slab, k range) are statically interleaved over
+// the clusters. Waits are bounded; when one runs out the kernel records
+// PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
+// returns.
 
 #include <cstdint>
 
@@ -36,14 +38,18 @@ namespace pgg {
 namespace {
 
 constexpr int kOK = 128;          // k per CTA (the pair's MMA M is 256)
-constexpr int kMaxRows = 256;     // rows per chunk (MMA N)
-constexpr int kStages = 6;
+constexpr int kMaxRows = 128;     // rows per chunk (MMA N)
+constexpr int kStages = 4;
 constexpr int kABytes = kOK * kRowBytes;              // weight: 128 k x 128 bytes
 constexpr int kBBytes = (kMaxRows / 2) * kRowBytes;   // this CTA's half of the rows
 constexpr int kStageBytes = kABytes + kBBytes;
+// slab accumulators: per epilogue warp [kMaxSlabTokens + 1 tokens][32 k] fp32;
+// the last row takes the stores of the padding rows of a chunk
+constexpr int kAccRows = kMaxSlabTokens + 1;
+constexpr int kAccBytes = 4 * kAccRows * 32 * 4;
 constexpr int kThreads = 32 * 6;
-constexpr int kTmemCols = 512;
-constexpr int kAccCols = 256;
+constexpr int kTmemCols = 256;
+constexpr int kAccCols = 128;
 
 struct OwnCtl {
   uint64_t full[kStages];
@@ -55,7 +61,8 @@ struct OwnCtl {
   int abort;
 };
 
-constexpr int kSmemBytes = kStages * kStageBytes + static_cast<int>(sizeof(OwnCtl)) + 1024;
+constexpr int kSmemBytes =
+    kStages * kStageBytes + kAccBytes + static_cast<int>(sizeof(OwnCtl)) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint32_t site) {
@@ -67,13 +74,6 @@ __device__ __forceinline__ uint32_t n_clusters() { return gridDim.x >> 1; }
 
 // MMA N for a chunk of R rows: a multiple of 32 (each CTA stages half).
 __device__ __forceinline__ int mma_n(int R) { return (R + 31) / 32 * 32; }
-
-// Smallest d_y box (16 << j rows) that covers `rows`.
-__device__ __forceinline__ int box_of(int rows) {
-  int j = 0;
-  while ((kDyMinRows << j) < rows && j < kDyMaps - 1) ++j;
-  return j;
-}
 
 // Walks the chunks of one unit (slab s, k range): experts in increasing
 // order, each expert's slab rows in pieces of at most 256.
@@ -122,9 +122,9 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const DyMaps* dy, const CUt
     ChunkIt c;
     for (c.start(&a, slab); c.valid() && !failed; c.next()) {
       const int nm = mma_n(c.rows());
-      const int j = box_of(nm / 2);
-      const uint32_t tx = 2u * static_cast<uint32_t>(kABytes + (kDyMinRows << j) * kRowBytes);
-      const int32_t brow = static_cast<int32_t>(c.r0 + rank * (nm / 2));
+      const int half = nm / 2;  // this CTA's rows: 16, 32, 48 or 64
+      const uint32_t tx = 2u * static_cast<uint32_t>(kABytes + half * kRowBytes);
+      const int32_t brow = static_cast<int32_t>(c.r0 + rank * half);
       for (int ks = 0; ks < a.nk; ++ks) {
         if (!ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
           failed = true;
@@ -134,7 +134,13 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const DyMaps* dy, const CUt
         const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
         if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
         ptx::tma_load_3d_pair(sa, tw, fb, ks * 64, k0, static_cast<int32_t>(c.g));
-        ptx::tma_load_2d_pair(sa + kABytes, &dy->box[j], fb, ks * 64, brow);
+        // the rows in boxes of 64, 32 and 16 rows (each box lands on a
+        // 1024-byte boundary, so the 128-byte swizzle stays in phase)
+        for (int r = 0; r < half;) {
+          const int j = half - r >= 64 ? 2 : (half - r >= 32 ? 1 : 0);
+          ptx::tma_load_2d_pair(sa + kABytes + r * kRowBytes, &dy->box[j], fb, ks * 64, brow + r);
+          r += kDyMinRows << j;
+        }
         outstanding |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -213,10 +219,17 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
   }
 }
 
+// Row flags of the epilogue: bits 0-8 the accumulator row (the token within
+// the slab, or kMaxSlabTokens for a padding row).
+constexpr int kRowMask = 0x1FF;
+constexpr int kRowFirst = 1 << 9;  // the token's first row: store, no load
+constexpr int kRowDup = 1 << 10;   // same token as the row before, in this batch: carry
+
 // Epilogue warp q (of 4) owns accumulator lanes 32 q .. 32 q + 31: one d_x
-// column k each, for every row of every chunk of the CTA's units.
-__device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, uint32_t n_units,
-                         uint32_t rank) {
+// column k each, for every token of the slab. Its accumulator block acc_q is
+// [kAccRows][32 k] fp32 in shared memory.
+__device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const OwnerArgs& a,
+                         uint32_t n_units, uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,16 +237,35 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
   const uint32_t tempty0 = ptx::mapa(&ctl->tempty[0], 0);
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   const int64_t K = a.K;
+  const int T = a.slab_tokens;
   int acc = 0;
   uint32_t aph = 0;
   bool stop = false;
   for (uint32_t u = cluster_id(); u < n_units && !stop; u += n_clusters()) {
+    const int64_t slab = u / a.k_units;
+    const int64_t tok0 = slab * T;
     const int64_t k =
         static_cast<int64_t>(u % a.k_units) * 2 * kOK + kOK * rank + 32 * quarter + lane;
-    const bool k_ok = k < K;
     ChunkIt c;
-    for (c.start(&a, u / a.k_units); c.valid(); c.next()) {
+    for (c.start(&a, slab); c.valid(); c.next()) {
       const int R = c.rows();
+      // lane j of info[b] describes row 32 b + j of the chunk (read before the
+      // accumulator is ready: it does not depend on the MMA)
+      int info[kMaxRows / 32];
+#pragma unroll
+      for (int b = 0; b < kMaxRows / 32; ++b) {
+        int f = kMaxSlabTokens;
+        const int r = 32 * b + lane;
+        if (r < R) {
+          const RowInfo ri = a.rowinfo[c.r0 + r];
+          const int64_t t = static_cast<int64_t>(ri.token) - tok0;
+          if (t >= 0 && t < T) f = static_cast<int>(t) | (ri.rank == 0 ? kRowFirst : 0);
+        }
+        const int before = __shfl_up_sync(0xFFFFFFFFu, f, 1);
+        if (lane > 0 && (f & kRowMask) != kMaxSlabTokens && ((before ^ f) & kRowMask) == 0)
+          f |= kRowDup;
+        info[b] = f;
+      }
       const bool ok = ptx::mbar_wait_cluster(&ctl->tfull[acc], aph, lim, abort);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         if (lane == 0) {
@@ -246,38 +278,35 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
       ptx::tc_fence_after_sync();
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
                               static_cast<uint32_t>(acc * kAccCols);
-      for (int b0 = 0; b0 < R; b0 += 32) {
+#pragma unroll
+      for (int b = 0; b < kMaxRows / 32; ++b) {
+        if (32 * b >= R) break;
         uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(b0), v);
-        ptx::tmem_ld_wait();
-        int tok_l = -1, rank_l = 0;
-        if (b0 + lane < R) {
-          const RowInfo ri = a.rowinfo[c.r0 + b0 + lane];
-          tok_l = ri.token;
-          rank_l = ri.rank;
-        }
-        const int n = R - b0 < 32 ? R - b0 : 32;
-        // loads of the rows that add onto an earlier row stored before this batch
+        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(32 * b), v);
+        int row[32];
         float old[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int tok = __shfl_sync(0xFFFFFFFFu, tok_l, j);
-          const int rk = __shfl_sync(0xFFFFFFFFu, rank_l, j);
-          const int prev = __shfl_sync(0xFFFFFFFFu, tok_l, j > 0 ? j - 1 : 0);
-          old[j] = 0.0f;
-          if (j < n && k_ok && rk > 0 && (j == 0 || prev != tok)) old[j] = a.out[tok * K + k];
+          row[j] = __shfl_sync(0xFFFFFFFFu, info[b], j);
+          old[j] = acc_q[(row[j] & kRowMask) * 32 + lane];
         }
-        float carry = 0.0f;
+        ptx::tmem_ld_wait();
+        if (!__any_sync(0xFFFFFFFFu, info[b] & kRowDup)) {
+          // distinct tokens: independent updates (-0 + x == x for every x)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int tok = __shfl_sync(0xFFFFFFFFu, tok_l, j);
-          const int rk = __shfl_sync(0xFFFFFFFFu, rank_l, j);
-          const int prev = __shfl_sync(0xFFFFFFFFu, tok_l, j > 0 ? j - 1 : 0);
-          if (j < n) {
+          for (int j = 0; j < 32; ++j) {
+            const float base = (row[j] & kRowFirst) ? -0.0f : old[j];
+            acc_q[(row[j] & kRowMask) * 32 + lane] = base + __uint_as_float(v[j]);
+          }
+        } else {
+          // a token twice in a row: carry its running sum
+          float carry = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
             const float x = __uint_as_float(v[j]);
             const float val =
-                rk == 0 ? x : ((j > 0 && prev == tok) ? carry + x : old[j] + x);
-            if (k_ok) a.out[tok * K + k] = val;
+                (row[j] & kRowFirst) ? x : ((row[j] & kRowDup) ? carry + x : old[j] + x);
+            acc_q[(row[j] & kRowMask) * 32 + lane] = val;
             carry = val;
           }
         }
@@ -287,6 +316,16 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
       if (lane == 0) ptx::mbar_arrive_remote(acc ? tempty1 : tempty0);
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
+    }
+    if (stop) break;
+    // the slab is done: this thread's column to d_x (every token of the
+    // slab has at least one row, so every element was stored above)
+    int64_t nt = a.batch - tok0;
+    if (nt > T) nt = T;
+    if (k < K) {
+      float* dst = a.out + tok0 * K + k;
+#pragma unroll 8
+      for (int t = 0; t < static_cast<int>(nt); ++t) dst[t * K] = acc_q[t * 32 + lane];
     }
   }
 }
@@ -298,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  auto* ctl = reinterpret_cast<OwnCtl*>(smem + kStages * kStageBytes);
+  float* accs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+  auto* ctl = reinterpret_cast<OwnCtl*>(smem + kStages * kStageBytes + kAccBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
@@ -348,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_issuer<DT>(smem, ctl, tmem_base, a, n_units);
   } else {
-    epilogue(ctl, tmem_base, a, n_units, rank);
+    epilogue(ctl, accs + (warp & 3) * (kAccRows * 32), tmem_base, a, n_units, rank);
   }
 
   ptx::tc_fence_before_sync();

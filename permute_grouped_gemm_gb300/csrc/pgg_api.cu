@@ -68,14 +68,26 @@ constexpr int64_t kInt32Max = 2147483647;
 constexpr int kVariantSimt = 3;   // FP32-pipe kernel (gmm_dx_simt.cu)
 constexpr int kVariantOwner = 4;  // slab-owner kernel (gmm_dx_owner.cu), ticketed fallback
 
-// The owner variant pays off when a 256-token slab holds about 96 or more
-// rows of each expert (so its MMAs are wide), for 16-bit inputs, and when
-// there are enough (slab, 256-k) units to fill the GPU.
+// Token slab of the owner variant: about 112 rows of each expert per slab
+// when the routing is even (G * T / topK rows), so that most experts take one
+// MMA of N <= 128; a multiple of 32 in [32, 256].
+int owner_slab_tokens(int64_t G, int64_t topK) {
+  int64_t t = 112 * G / topK / 32 * 32;
+  if (t < 32) t = 32;
+  if (t > kMaxSlabTokens) t = kMaxSlabTokens;
+  return static_cast<int>(t);
+}
+
+// The owner variant pays off when its slabs hold about 112 rows of each
+// expert (so its MMAs are wide: few experts per token), for 16-bit inputs,
+// and when there are enough (slab, 256-k) units to fill the GPU.
 bool owner_fits(int64_t K, int64_t G, int64_t batch, int64_t topK, int dtype) {
   if (dtype == PGG_F32) return false;
-  const int64_t slabs = (batch + kSlabTokens - 1) / kSlabTokens;
+  if (112 * G > static_cast<int64_t>(kMaxSlabTokens) * topK) return false;
+  const int64_t T = owner_slab_tokens(G, topK);
+  const int64_t slabs = (batch + T - 1) / T;
   const int64_t k_units = (K + 255) / 256;
-  return G * 96 <= kSlabTokens * topK && slabs * k_units >= 128;
+  return slabs * k_units >= 128;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -119,8 +131,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
     // the owner variant keeps the ticketed kernel's (variant 0) row blocks for its fallback
     return PGG_ERR_DTYPE;
   }
+  p->slab_tokens = variant == kVariantOwner ? owner_slab_tokens(G, topK) : 0;
   p->n_slabs = variant == kVariantOwner
-                   ? static_cast<int>((batch + kSlabTokens - 1) / kSlabTokens)
+                   ? static_cast<int>((batch + p->slab_tokens - 1) / p->slab_tokens)
                    : 0;
   if (rows_override > 0) p->rows_per_block = rows_override;
   p->M = M;
@@ -334,6 +347,7 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
     o.G = plan.G;
     o.batch = plan.batch;
     o.n_slabs = plan.n_slabs;
+    o.slab_tokens = plan.slab_tokens;
     o.k_units = static_cast<int32_t>((plan.K + 255) / 256);
     o.nk = plan.nk;
     o.wait_limit_ns = a.wait_limit_ns;
@@ -587,7 +601,7 @@ int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   rc = make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
   if (rc != PGG_OK) return rc;
   info->variant = p.variant;
-  info->rows_per_block = p.variant == kVariantOwner ? kSlabTokens : p.rows_per_block;
+  info->rows_per_block = p.variant == kVariantOwner ? p.slab_tokens : p.rows_per_block;
   info->k_per_block = kKBlock;
   info->stages = p.stages;
   info->k_blocks = p.k_blocks;

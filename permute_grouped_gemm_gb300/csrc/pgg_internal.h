@@ -47,8 +47,8 @@ struct Layout {
   int64_t n_tickets;  // batch * k_blocks, rounded up to a multiple of 4
 };
 
-// Token slabs of the owner variant of the d_x kernel (gmm_dx_owner.cu).
-constexpr int kSlabTokens = 256;
+// Largest token slab of the owner variant of the d_x kernel (gmm_dx_owner.cu).
+constexpr int kMaxSlabTokens = 256;
 
 struct Plan {
   int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single
@@ -67,7 +67,8 @@ struct Plan {
   int64_t M, N, K, G, batch, topK;
   int row_idx_type;
   int nk;  // reduction steps: ceil(N / elements per 128-byte row)
-  int n_slabs;  // owner variant: ceil(batch / kSlabTokens); 0 otherwise
+  int slab_tokens;  // owner variant: tokens per slab (<= kMaxSlabTokens); 0 otherwise
+  int n_slabs;      // owner variant: ceil(batch / slab_tokens); 0 otherwise
   Layout layout;
 };
 
@@ -100,12 +101,13 @@ struct GemmArgs {
 // Arguments of the owner variant of the d_x kernel (gmm_dx_owner.cu).
 struct OwnerArgs {
   const int64_t* off;     // [G + 1] first expanded row of each expert
-  const int32_t* seg;     // [G][n_slabs + 1] first row of expert g with token >= slab * 256
+  const int32_t* seg;     // [G][n_slabs + 1] first row of expert g with token >= slab * T
   const RowInfo* rowinfo; // [M]
   WsHeader* hdr;
   float* out;             // [batch, K]
   int64_t M, K, G, batch;
   int32_t n_slabs;
+  int32_t slab_tokens;  // T
   int32_t k_units;  // ceil(K / 256): k ranges of a CTA pair
   int32_t nk;       // ceil(N / 64): reduction steps
   uint64_t wait_limit_ns;

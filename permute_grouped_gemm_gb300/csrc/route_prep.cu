@@ -16,7 +16,7 @@
 //                           among the token's rows (increasing expanded index).
 //   route_owner    (grid)   owner variant only: whether each expert's rows are
 //                           in increasing original position, and where each
-//                           256-token slab starts inside each expert.
+//                           token slab starts inside each expert.
 //
 // The index is read as the constraint table and note 1 of section "输入输出"
 // state: rowIdxType 0 maps expanded row -> original position, rowIdxType 1
@@ -213,11 +213,11 @@ __device__ __forceinline__ int64_t position_of_row(const int64_t* idx, const int
 // Owner variant: (1) whether every expert's rows are in increasing original
 // position (then the rows of a token slab form one contiguous range inside
 // each expert); (2) seg[g][s] = first row of expert g whose position is at
-// least s * kSlabTokens * topK (binary search, meaningful when sorted).
+// least s * slab_tokens * topK (binary search, meaningful when sorted).
 __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
                                    const int64_t* __restrict__ off, int64_t M, int64_t G,
                                    int64_t top_k, int row_idx_type, int n_slabs,
-                                   int32_t* __restrict__ seg, WsHeader* hdr) {
+                                   int slab_tokens, int32_t* __restrict__ seg, WsHeader* hdr) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
@@ -240,7 +240,7 @@ __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_
   const int64_t n_seg = G * (n_slabs + 1);
   for (int64_t q = t0; q < n_seg; q += stride) {
     const int64_t g = q / (n_slabs + 1), s = q - g * (n_slabs + 1);
-    const int64_t p0 = s * kSlabTokens * top_k;
+    const int64_t p0 = s * slab_tokens * top_k;
     int64_t lo = off[g], hi = off[g + 1];  // first row in [lo, hi) with position >= p0
     while (lo < hi) {
       const int64_t mid = (lo + hi) >> 1;
@@ -313,7 +313,7 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
     if (oblocks < 1) oblocks = 1;
     route_owner_kernel<<<static_cast<int>(oblocks), 256, 0, stream>>>(
         idx, inv, off, plan.M, plan.G, plan.topK, plan.row_idx_type, plan.n_slabs,
-        reinterpret_cast<int32_t*>(ws + L.seg), hdr);
+        plan.slab_tokens, reinterpret_cast<int32_t*>(ws + L.seg), hdr);
   }
   return cudaGetLastError();
 }

@@ -58,7 +58,7 @@ def check(inp, out, tokens=None, what=""):
 def test_uniform_workload_plans_the_owner_variant():
     w = WORKLOADS["uniform-bf16"]
     p = pgg.pgg_dx_plan(w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k, 0, pgg.PGG_BF16)
-    assert p["variant"] == 4 and p["rows_per_block"] == 256 and p["cta_pair"] == 1
+    assert p["variant"] == 4 and p["rows_per_block"] == 224 and p["cta_pair"] == 1
 
 
 CASES = {
@@ -69,6 +69,10 @@ CASES = {
     "top1": dict(batch=900, top_k=1, G=4, K=256, N=256),
     "k_is_1": dict(batch=300, top_k=3, G=4, K=1, N=256),
     "many_rows_per_expert": dict(batch=2000, top_k=2, G=2, K=256, N=128),
+    # 32-token slabs of 256 rows over two experts: chunks of 128 rows and a tail
+    "chunk_split": dict(batch=1000, top_k=8, G=2, K=512, N=192, routing="replacement"),
+    # many experts: 256-token slabs with a few rows of each expert
+    "wide_slabs": dict(batch=800, top_k=2, G=40, K=300, N=256),
 }
 
 
