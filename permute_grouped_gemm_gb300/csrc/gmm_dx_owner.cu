@@ -9,10 +9,12 @@
 // when each expert's rows are in increasing original position, which the
 // routing step checks), computes C = weight[g] d_y[rows]^T for its 256 k on
 // the tensor cores (cta_group::2, M = 256 k, N = rows rounded up to 32 and at
-// most 128, TMA for both operands, accumulators in tensor memory), and adds
-// each row into a shared-memory copy of the slab's d_x block. Each epilogue
-// thread owns one d_x column k of the slab, for every token: it alone reads,
-// adds and writes that column, in program order, in increasing expanded index
+// most 128, TMA for both operands, two accumulators in tensor memory), and
+// adds each row into the slab's d_x block, which also lives in tensor memory
+// (columns 256 .. 256 + T: one column per token, one lane per k), so that all
+// of shared memory goes to the operand pipeline. Each epilogue thread owns one
+// d_x column k of the slab (its tensor-memory lane), for every token: it alone
+// reads, adds and writes that column, in program order, in increasing expanded index
 // (increasing expert, then increasing row within the expert), which is the
 // order of additions of the ticketed kernel, with no tickets, no barriers
 // between threads and no atomics. A token's first row (rank 0) stores, later
@@ -23,8 +25,10 @@
 // When some expert's rows are not in increasing original position the kernel
 // leaves at once and the ticketed kernel, launched after it, does the work.
 //
-// Warp roles per CTA: 0 TMA; 1 tensor-memory allocation and (even CTA) MMA
-// issue; 2-5 epilogue. Units (slab, k range) are statically interleaved over
+// Pipeline stages: when N is a multiple of 64, each stage covers 128 n as two
+// 64-n panels, loaded by one 4-D weight copy and one 3-D d_y copy (4 stages);
+// otherwise 64 n (9 stages). Warp roles per CTA: 0 TMA; 1 tensor-memory
+// allocation and (even CTA) MMA issue; 2-5 epilogue. Units (slab, k range) are statically interleaved over
 // the clusters. Waits are bounded; when one runs out the kernel records
 // PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
 // returns.
@@ -39,21 +43,27 @@ namespace {
 
 constexpr int kOK = 128;          // k per CTA (the pair's MMA M is 256)
 constexpr int kMaxRows = 128;     // rows per chunk (MMA N)
-constexpr int kStages = 4;
-constexpr int kABytes = kOK * kRowBytes;              // weight: 128 k x 128 bytes
-constexpr int kBBytes = (kMaxRows / 2) * kRowBytes;   // this CTA's half of the rows
-constexpr int kStageBytes = kABytes + kBBytes;
-// slab accumulators: per epilogue warp [kMaxSlabTokens + 1 tokens][32 k] fp32;
-// the last row takes the stores of the padding rows of a chunk
-constexpr int kAccRows = kMaxSlabTokens + 1;
-constexpr int kAccBytes = 4 * kAccRows * 32 * 4;
+constexpr int kABytes = kOK * kRowBytes;              // weight panel: 128 k x 128 bytes
+constexpr int kBBytes = (kMaxRows / 2) * kRowBytes;   // rows panel: this CTA's half of the rows
+constexpr int kMaxStages = 9;
+
+// Stage geometry: one or two 64-n panels per stage.
+template <bool WIDE>
+struct Geo {
+  static constexpr int kPanels = WIDE ? 2 : 1;
+  static constexpr int kA = kPanels * kABytes;
+  static constexpr int kStageBytes = kPanels * (kABytes + kBBytes);
+  static constexpr int kStages = WIDE ? 4 : kMaxStages;
+};
 constexpr int kThreads = 32 * 6;
-constexpr int kTmemCols = 256;
-constexpr int kAccCols = 128;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 128;              // per MMA accumulator
+constexpr int kSlabCol = 2 * kAccCols;     // the slab block: columns 256 .. 256 + T
+static_assert(kSlabCol + kMaxSlabTokens <= kTmemCols, "tensor memory columns");
 
 struct OwnCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -61,9 +71,12 @@ struct OwnCtl {
   int abort;
 };
 
-constexpr int kSmemBytes =
-    kStages * kStageBytes + kAccBytes + static_cast<int>(sizeof(OwnCtl)) + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+template <bool WIDE>
+constexpr int smem_bytes() {
+  return Geo<WIDE>::kStages * Geo<WIDE>::kStageBytes + static_cast<int>(sizeof(OwnCtl)) + 1024;
+}
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024,
+              "shared memory per CTA");
 
 __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint32_t site) {
   if (atomicCAS(&hdr->status, 0u, code) == 0u) hdr->timeout_site = site;
@@ -76,26 +89,40 @@ __device__ __forceinline__ uint32_t n_clusters() { return gridDim.x >> 1; }
 __device__ __forceinline__ int mma_n(int R) { return (R + 31) / 32 * 32; }
 
 // Walks the chunks of one unit (slab s, k range): experts in increasing
-// order, each expert's slab rows in pieces of at most 256.
+// order, each expert's slab rows in pieces of at most kMaxRows. The bounds of
+// the next expert are loaded one expert ahead, so that moving on does not wait
+// for memory.
 struct ChunkIt {
   const OwnerArgs* a;
   int64_t s;
-  int64_t g;
-  int64_t r0, r_end;
+  int64_t g, r0, r_end;
+  int64_t ng;          // next expert, its bounds in flight
+  int32_t nlo, nhi;
+  __device__ void load_next() {
+    ng = g + 1;
+    if (ng < a->G) {
+      const int32_t* row = a->seg + ng * (a->n_slabs + 1);
+      nlo = row[s];
+      nhi = row[s + 1];
+    }
+  }
+  __device__ void next_expert() {
+    while (true) {
+      g = ng;
+      if (g >= a->G) return;
+      r0 = nlo;
+      r_end = nhi;
+      load_next();
+      if (r0 < r_end) return;
+    }
+  }
   __device__ void start(const OwnerArgs* args, int64_t slab) {
     a = args;
     s = slab;
     g = -1;
     r0 = r_end = 0;
+    load_next();
     next_expert();
-  }
-  __device__ void next_expert() {
-    while (++g < a->G) {
-      const int32_t* row = a->seg + g * (a->n_slabs + 1);
-      r0 = row[s];
-      r_end = row[s + 1];
-      if (r0 < r_end) return;
-    }
   }
   __device__ bool valid() const { return g < a->G; }
   __device__ int rows() const {
@@ -108,8 +135,10 @@ struct ChunkIt {
   }
 };
 
-__device__ void producer(uint8_t* smem, OwnCtl* ctl, const DyMaps* dy, const CUtensorMap* tw,
-                         const OwnerArgs& a, uint32_t n_units, uint32_t rank) {
+template <bool WIDE>
+__device__ void producer(uint8_t* smem, OwnCtl* ctl, const OwnerMaps* m, const OwnerArgs& a,
+                         uint32_t n_units, uint32_t rank) {
+  using Gm = Geo<WIDE>;
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const bool leader = rank == 0;
@@ -123,27 +152,36 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const DyMaps* dy, const CUt
     for (c.start(&a, slab); c.valid() && !failed; c.next()) {
       const int nm = mma_n(c.rows());
       const int half = nm / 2;  // this CTA's rows: 16, 32, 48 or 64
-      const uint32_t tx = 2u * static_cast<uint32_t>(kABytes + half * kRowBytes);
+      // wide stages load whole 64-row boxes (the MMA reads the first half rows)
+      const uint32_t tx = WIDE ? 2u * static_cast<uint32_t>(Gm::kStageBytes)
+                               : 2u * static_cast<uint32_t>(kABytes + half * kRowBytes);
       const int32_t brow = static_cast<int32_t>(c.r0 + rank * half);
       for (int ks = 0; ks < a.nk; ++ks) {
         if (!ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
           failed = true;
           break;
         }
-        uint8_t* sa = smem + stage * kStageBytes;
+        uint8_t* sa = smem + stage * Gm::kStageBytes;
         const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
         if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
-        ptx::tma_load_3d_pair(sa, tw, fb, ks * 64, k0, static_cast<int32_t>(c.g));
-        // the rows in boxes of 64, 32 and 16 rows (each box lands on a
-        // 1024-byte boundary, so the 128-byte swizzle stays in phase)
-        for (int r = 0; r < half;) {
-          const int j = half - r >= 64 ? 2 : (half - r >= 32 ? 1 : 0);
-          ptx::tma_load_2d_pair(sa + kABytes + r * kRowBytes, &dy->box[j], fb, ks * 64, brow + r);
-          r += kDyMinRows << j;
+        if constexpr (WIDE) {
+          // panels 2 ks and 2 ks + 1 of 64 n (past N / 64 they read as zero)
+          ptx::tma_load_4d_pair(sa, &m->tw4, fb, 0, k0, 2 * ks, static_cast<int32_t>(c.g));
+          ptx::tma_load_3d_pair(sa + Gm::kA, &m->dy3, fb, 0, brow, 2 * ks);
+        } else {
+          ptx::tma_load_3d_pair(sa, &m->tw, fb, ks * 64, k0, static_cast<int32_t>(c.g));
+          // the rows in boxes of 64, 32 and 16 rows (each box lands on a
+          // 1024-byte boundary, so the 128-byte swizzle stays in phase)
+          for (int r = 0; r < half;) {
+            const int j = half - r >= 64 ? 2 : (half - r >= 32 ? 1 : 0);
+            ptx::tma_load_2d_pair(sa + kABytes + r * kRowBytes, &m->dy.box[j], fb, ks * 64,
+                                  brow + r);
+            r += kDyMinRows << j;
+          }
         }
         outstanding |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
+        if (++stage == Gm::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -156,15 +194,16 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const DyMaps* dy, const CUt
   }
   if (leader) {
     int no_abort = 0;
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < Gm::kStages; ++s)
       if (outstanding & (1u << s))
         ptx::mbar_wait_cluster(&ctl->full[s], (last_parity >> s) & 1u, lim, &no_abort);
   }
 }
 
-template <int DT>
+template <int DT, bool WIDE>
 __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a,
                            uint32_t n_units) {
+  using Gm = Geo<WIDE>;
   constexpr uint32_t kFmt = DT == PGG_BF16 ? 1u : 0u;
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
@@ -187,17 +226,20 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
           break;
         }
         ptx::tc_fence_after_sync();
-        const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
-        const uint64_t da = ptx::sdesc_sw128(sa);
-        const uint64_t db = ptx::sdesc_sw128(sa + kABytes);
+        const uint32_t sa = ptx::smem_addr(smem + stage * Gm::kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kRowBytes / 32; ++kk) {
-          const uint64_t koff = static_cast<uint64_t>((kk * 32) >> 4);
-          ptx::mma_f16_pair(d_tmem, da + koff, db + koff, idesc, (ks | kk) != 0 ? 1u : 0u);
+        for (int p = 0; p < Gm::kPanels; ++p) {
+          const uint64_t da = ptx::sdesc_sw128(sa + p * kABytes);
+          const uint64_t db = ptx::sdesc_sw128(sa + Gm::kA + p * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+            const uint64_t koff = static_cast<uint64_t>((kk * 32) >> 4);
+            ptx::mma_f16_pair(d_tmem, da + koff, db + koff, idesc, (ks | p | kk) != 0 ? 1u : 0u);
+          }
         }
         issued = true;
         ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
-        if (++stage == kStages) {
+        if (++stage == Gm::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -219,17 +261,22 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
   }
 }
 
-// Row flags of the epilogue: bits 0-8 the accumulator row (the token within
-// the slab, or kMaxSlabTokens for a padding row).
-constexpr int kRowMask = 0x1FF;
+// Row flags of the epilogue: bits 0-7 the token within the slab.
+constexpr int kRowPad = 1 << 8;    // no row (past the chunk's end)
 constexpr int kRowFirst = 1 << 9;  // the token's first row: store, no load
 constexpr int kRowDup = 1 << 10;   // same token as the row before, in this batch: carry
 
-// Epilogue warp q (of 4) owns accumulator lanes 32 q .. 32 q + 31: one d_x
-// column k each, for every token of the slab. Its accumulator block acc_q is
-// [kAccRows][32 k] fp32 in shared memory.
-__device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const OwnerArgs& a,
-                         uint32_t n_units, uint32_t rank) {
+// Tensor-memory column that row j of a batch reads and writes: its token's
+// slab column, or for a padding row its own accumulator column (already read,
+// and cleared by the next MMA into that accumulator).
+__device__ __forceinline__ uint32_t row_col(int row, uint32_t own) {
+  return (row & kRowPad) ? own : static_cast<uint32_t>(kSlabCol + (row & 0xFF));
+}
+
+// Epilogue warp q (of 4) owns tensor-memory lanes 32 q .. 32 q + 31: one d_x
+// column k each, for every token of the slab.
+__device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, uint32_t n_units,
+                         uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -238,6 +285,7 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   const int64_t K = a.K;
   const int T = a.slab_tokens;
+  const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
   int acc = 0;
   uint32_t aph = 0;
   bool stop = false;
@@ -254,7 +302,7 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
       int info[kMaxRows / 32];
 #pragma unroll
       for (int b = 0; b < kMaxRows / 32; ++b) {
-        int f = kMaxSlabTokens;
+        int f = kRowPad;
         const int r = 32 * b + lane;
         if (r < R) {
           const RowInfo ri = a.rowinfo[c.r0 + r];
@@ -262,7 +310,7 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
           if (t >= 0 && t < T) f = static_cast<int>(t) | (ri.rank == 0 ? kRowFirst : 0);
         }
         const int before = __shfl_up_sync(0xFFFFFFFFu, f, 1);
-        if (lane > 0 && (f & kRowMask) != kMaxSlabTokens && ((before ^ f) & kRowMask) == 0)
+        if (lane > 0 && !(f & kRowPad) && !(before & kRowPad) && ((before ^ f) & 0xFF) == 0)
           f |= kRowDup;
         info[b] = f;
       }
@@ -276,27 +324,27 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
         break;
       }
       ptx::tc_fence_after_sync();
-      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
-                              static_cast<uint32_t>(acc * kAccCols);
+      const uint32_t acc_col = static_cast<uint32_t>(acc * kAccCols);
 #pragma unroll
       for (int b = 0; b < kMaxRows / 32; ++b) {
         if (32 * b >= R) break;
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(32 * b), v);
+        uint32_t v[32], old[32];
+        ptx::tmem_ld_32x32b_x32(t_lane + acc_col + static_cast<uint32_t>(32 * b), v);
         int row[32];
-        float old[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           row[j] = __shfl_sync(0xFFFFFFFFu, info[b], j);
-          old[j] = acc_q[(row[j] & kRowMask) * 32 + lane];
+          old[j] = ptx::tmem_ld_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j));
         }
-        ptx::tmem_ld_wait();
+        ptx::tmem_ld_wait_regs(v);
+        ptx::tmem_ld_wait_regs(old);
         if (!__any_sync(0xFFFFFFFFu, info[b] & kRowDup)) {
           // distinct tokens: independent updates (-0 + x == x for every x)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float base = (row[j] & kRowFirst) ? -0.0f : old[j];
-            acc_q[(row[j] & kRowMask) * 32 + lane] = base + __uint_as_float(v[j]);
+            const float base = (row[j] & kRowFirst) ? -0.0f : __uint_as_float(old[j]);
+            ptx::tmem_st_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j),
+                                   __float_as_uint(base + __uint_as_float(v[j])));
           }
         } else {
           // a token twice in a row: carry its running sum
@@ -304,12 +352,16 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float x = __uint_as_float(v[j]);
-            const float val =
-                (row[j] & kRowFirst) ? x : ((row[j] & kRowDup) ? carry + x : old[j] + x);
-            acc_q[(row[j] & kRowMask) * 32 + lane] = val;
+            const float val = (row[j] & kRowFirst)
+                                  ? x
+                                  : ((row[j] & kRowDup) ? carry + x : __uint_as_float(old[j]) + x);
+            ptx::tmem_st_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j),
+                                   __float_as_uint(val));
             carry = val;
           }
         }
+        // the next batch may read what this one wrote
+        ptx::tmem_st_wait();
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -322,23 +374,28 @@ __device__ void epilogue(OwnCtl* ctl, float* acc_q, uint32_t tmem_base, const Ow
     // slab has at least one row, so every element was stored above)
     int64_t nt = a.batch - tok0;
     if (nt > T) nt = T;
-    if (k < K) {
-      float* dst = a.out + tok0 * K + k;
-#pragma unroll 8
-      for (int t = 0; t < static_cast<int>(nt); ++t) dst[t * K] = acc_q[t * 32 + lane];
+    for (int t0 = 0; t0 < static_cast<int>(nt); t0 += 32) {
+      uint32_t w[32];
+      ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(kSlabCol + t0), w);
+      ptx::tmem_ld_wait_regs(w);
+      if (k < K) {
+        float* dst = a.out + (tok0 + t0) * K + k;
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t0 + t < nt) dst[t * K] = __uint_as_float(w[t]);
+      }
     }
   }
 }
 
-template <int DT>
+template <int DT, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
-    gmm_dx_owner_kernel(const __grid_constant__ DyMaps dy, const __grid_constant__ CUtensorMap tw,
-                        const OwnerArgs a) {
+    gmm_dx_owner_kernel(const __grid_constant__ OwnerMaps m, const OwnerArgs a) {
+  using Gm = Geo<WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  float* accs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  auto* ctl = reinterpret_cast<OwnCtl*>(smem + kStages * kStageBytes + kAccBytes);
+  auto* ctl = reinterpret_cast<OwnCtl*>(smem + Gm::kStages * Gm::kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
@@ -357,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t n_units = static_cast<uint32_t>(a.n_slabs) * static_cast<uint32_t>(a.k_units);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Gm::kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
     }
@@ -370,8 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int j = 0; j < kDyMaps; ++j) ptx::tma_prefetch_desc(&dy.box[j]);
-    ptx::tma_prefetch_desc(&tw);
+    if constexpr (WIDE) {
+      ptx::tma_prefetch_desc(&m.tw4);
+      ptx::tma_prefetch_desc(&m.dy3);
+    } else {
+      for (int j = 0; j < kDyMaps; ++j) ptx::tma_prefetch_desc(&m.dy.box[j]);
+      ptx::tma_prefetch_desc(&m.tw);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
@@ -384,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer(smem, ctl, &dy, &tw, a, n_units, rank);
+    if (lane == 0) producer<WIDE>(smem, ctl, &m, a, n_units, rank);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_issuer<DT>(smem, ctl, tmem_base, a, n_units);
+    if (lane == 0 && rank == 0) mma_issuer<DT, WIDE>(smem, ctl, tmem_base, a, n_units);
   } else {
-    epilogue(ctl, accs + (warp & 3) * (kAccRows * 32), tmem_base, a, n_units, rank);
+    epilogue(ctl, tmem_base, a, n_units, rank);
   }
 
   ptx::tc_fence_before_sync();
@@ -402,20 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int owner_smem_bytes() { return kSmemBytes; }
+int owner_smem_bytes(bool wide) { return wide ? smem_bytes<true>() : smem_bytes<false>(); }
 int owner_threads() { return kThreads; }
 
-cudaError_t launch_owner(int dtype, const DyMaps& dy, const CUtensorMap& tw, const OwnerArgs& a,
-                         int num_sms, cudaStream_t stream) {
-  void (*kern)(const DyMaps, const CUtensorMap, const OwnerArgs) = nullptr;
+// m.tw4 / m.dy3 are read when a.wide is set (N a multiple of 64), m.dy / m.tw otherwise.
+cudaError_t launch_owner(int dtype, const OwnerMaps& m, const OwnerArgs& a, int num_sms,
+                         cudaStream_t stream) {
+  void (*kern)(const OwnerMaps, const OwnerArgs) = nullptr;
+  const bool wide = a.wide != 0;
   if (dtype == PGG_BF16)
-    kern = gmm_dx_owner_kernel<PGG_BF16>;
+    kern = wide ? gmm_dx_owner_kernel<PGG_BF16, true> : gmm_dx_owner_kernel<PGG_BF16, false>;
   else if (dtype == PGG_F16)
-    kern = gmm_dx_owner_kernel<PGG_F16>;
+    kern = wide ? gmm_dx_owner_kernel<PGG_F16, true> : gmm_dx_owner_kernel<PGG_F16, false>;
   else
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+  const int smem = owner_smem_bytes(wide);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -424,7 +488,7 @@ cudaError_t launch_owner(int dtype, const DyMaps& dy, const CUtensorMap& tw, con
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -437,7 +501,7 @@ cudaError_t launch_owner(int dtype, const DyMaps& dy, const CUtensorMap& tw, con
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, dy, tw, a);
+  return cudaLaunchKernelEx(&cfg, kern, m, a);
 }
 
 }  // namespace pgg

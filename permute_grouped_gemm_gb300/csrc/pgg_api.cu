@@ -47,10 +47,10 @@ void fwd_simt_tiles(int64_t N, int* n_blocks);
 int fwd_simt_smem_bytes();
 cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
                             cudaStream_t stream);
-int owner_smem_bytes();
+int owner_smem_bytes(bool wide);
 int owner_threads();
-cudaError_t launch_owner(int dtype, const DyMaps& dy, const CUtensorMap& tw, const OwnerArgs& a,
-                         int num_sms, cudaStream_t stream);
+cudaError_t launch_owner(int dtype, const OwnerMaps& m, const OwnerArgs& a, int num_sms,
+                         cudaStream_t stream);
 cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, int32_t* inv,
                               WsHeader* hdr, int num_sms, cudaStream_t stream);
 cudaError_t launch_unpermute_grad(int dtype, const UnpermArgs& a, bool vec, bool pairs,
@@ -252,6 +252,36 @@ int encode_maps(const Plan& p, const void* dy, const void* w, DyMaps* tdy, CUten
   return PGG_OK;
 }
 
+// Owner kernel stages of two 64-n panels (16-bit dtypes, N a multiple of 64):
+// weight {64, K, N / 64, G} in boxes {64, 128, 2, 1}, d_y {64, M, N / 64} in
+// boxes {64, 64, 2}; panels past N / 64 read as zero.
+int encode_owner_wide_maps(const Plan& p, const void* dy, const void* w, OwnerMaps* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PGG_ERR_CUDA;
+  const cuuint64_t N = static_cast<cuuint64_t>(p.N), K = static_cast<cuuint64_t>(p.K);
+  {
+    cuuint64_t dims[4] = {64, K, N / 64, static_cast<cuuint64_t>(p.G)};
+    cuuint64_t strides[3] = {N * 2, 128, N * K * 2};
+    cuuint32_t box[4] = {64, 128, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(&m->tw4, tmap_type(p.dtype), 4, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PGG_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(p.M), N / 64};
+    cuuint64_t strides[2] = {N * 2, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&m->dy3, tmap_type(p.dtype), 3, const_cast<void*>(dy), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PGG_ERR_CUDA;
+  }
+  return PGG_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Common front half of every entry point that enqueues work.
@@ -350,9 +380,20 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
     o.slab_tokens = plan.slab_tokens;
     o.k_units = static_cast<int32_t>((plan.K + 255) / 256);
     o.nk = plan.nk;
+    o.wide = 0;
     o.wait_limit_ns = a.wait_limit_ns;
-    if (launch_owner(plan.dtype, tdy, tw, o, di.num_sms, stream) != cudaSuccess)
-      return PGG_ERR_CUDA;
+    OwnerMaps om;
+    om.dy = tdy;
+    om.tw = tw;
+    std::memset(&om.tw4, 0, sizeof(om.tw4));
+    std::memset(&om.dy3, 0, sizeof(om.dy3));
+    if (plan.N % 64 == 0) {
+      rc = encode_owner_wide_maps(plan, gradY, weight, &om);
+      if (rc != PGG_OK) return rc;
+      o.wide = 1;
+      o.nk = static_cast<int32_t>((plan.N + 127) / 128);
+    }
+    if (launch_owner(plan.dtype, om, o, di.num_sms, stream) != cudaSuccess) return PGG_ERR_CUDA;
   }
   // the ticketed kernel; after the owner kernel it works only when that one
   // could not (some expert's rows not in increasing original position)
@@ -609,7 +650,8 @@ int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   info->max_row_blocks = p.max_row_blocks;
   info->workspace_bytes = p.layout.total;
   info->threads = p.variant == kVariantOwner ? owner_threads() : p.threads;
-  info->smem_bytes = p.variant == kVariantOwner ? owner_smem_bytes() : p.smem_bytes;
+  info->smem_bytes =
+      p.variant == kVariantOwner ? owner_smem_bytes(p.N % 64 == 0) : p.smem_bytes;
   info->cta_pair = p.variant == kVariantOwner ? 1 : p.pair;
   return PGG_OK;
 }
