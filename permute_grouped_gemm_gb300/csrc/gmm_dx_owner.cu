@@ -8,8 +8,8 @@
 // takes the expert's rows whose tokens lie in the slab (one contiguous range
 // when each expert's rows are in increasing original position, which the
 // routing step checks), computes C = weight[g] d_y[rows]^T for its 256 k on
-// the tensor cores (cta_group::2, M = 256 k, N = rows rounded up to 32 and at
-// most 128, TMA for both operands, two accumulators in tensor memory), and
+// the tensor cores (cta_group::2, M = 256 k, N = rows rounded up to 16 or 32
+// and at most 128, TMA for both operands, two accumulators in tensor memory), and
 // adds each row into the slab's d_x block, which also lives in tensor memory
 // (columns 256 .. 256 + T: one column per token, one lane per k), so that all
 // of shared memory goes to the operand pipeline. Each epilogue thread owns one
@@ -27,7 +27,7 @@
 //
 // Pipeline stages: when N is a multiple of 64, each stage covers 128 n as two
 // 64-n panels, loaded by one 4-D weight copy and one 3-D d_y copy (4 stages);
-// otherwise 64 n (9 stages). Warp roles per CTA: 0 TMA; 1 tensor-memory
+// otherwise 64 n (8 stages). Warp roles per CTA: 0 TMA; 1 tensor-memory
 // allocation and (even CTA) MMA issue; 2-5 epilogue. Units (slab, k range) are statically interleaved over
 // the clusters. Waits are bounded; when one runs out the kernel records
 // PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
@@ -45,7 +45,7 @@ constexpr int kOK = 128;          // k per CTA (the pair's MMA M is 256)
 constexpr int kMaxRows = 128;     // rows per chunk (MMA N)
 constexpr int kABytes = kOK * kRowBytes;              // weight panel: 128 k x 128 bytes
 constexpr int kBBytes = (kMaxRows / 2) * kRowBytes;   // rows panel: this CTA's half of the rows
-constexpr int kMaxStages = 9;
+constexpr int kMaxStages = 8;
 
 // Stage geometry: one or two 64-n panels per stage.
 template <bool WIDE>
@@ -55,6 +55,11 @@ struct Geo {
   static constexpr int kStageBytes = kPanels * (kABytes + kBBytes);
   static constexpr int kStages = WIDE ? 4 : kMaxStages;
 };
+
+// Write-out staging: per epilogue warp two buffers of 32 tokens x 32 k fp32,
+// stored to d_x by TMA.
+constexpr int kOutBuf = 32 * 32;  // floats
+constexpr int kOutBytes = 4 * 2 * kOutBuf * 4;
 constexpr int kThreads = 32 * 6;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;              // per MMA accumulator
@@ -73,7 +78,8 @@ struct OwnCtl {
 
 template <bool WIDE>
 constexpr int smem_bytes() {
-  return Geo<WIDE>::kStages * Geo<WIDE>::kStageBytes + static_cast<int>(sizeof(OwnCtl)) + 1024;
+  return Geo<WIDE>::kStages * Geo<WIDE>::kStageBytes + kOutBytes +
+         static_cast<int>(sizeof(OwnCtl)) + 1024;
 }
 static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024,
               "shared memory per CTA");
@@ -85,8 +91,12 @@ __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint3
 __device__ __forceinline__ uint32_t cluster_id() { return blockIdx.x >> 1; }
 __device__ __forceinline__ uint32_t n_clusters() { return gridDim.x >> 1; }
 
-// MMA N for a chunk of R rows: a multiple of 32 (each CTA stages half).
-__device__ __forceinline__ int mma_n(int R) { return (R + 31) / 32 * 32; }
+// MMA N for a chunk of R rows (each CTA stages half): a multiple of 16 with
+// wide stages (whole 64-row boxes), of 32 otherwise (boxes of 16 rows or more).
+template <bool WIDE>
+__device__ __forceinline__ int mma_n(int R) {
+  return WIDE ? (R + 15) / 16 * 16 : (R + 31) / 32 * 32;
+}
 
 // Walks the chunks of one unit (slab s, k range): experts in increasing
 // order, each expert's slab rows in pieces of at most kMaxRows. The bounds of
@@ -150,8 +160,8 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const OwnerMaps* m, const O
     const int32_t k0 = static_cast<int32_t>((u % a.k_units) * 2 * kOK + kOK * rank);
     ChunkIt c;
     for (c.start(&a, slab); c.valid() && !failed; c.next()) {
-      const int nm = mma_n(c.rows());
-      const int half = nm / 2;  // this CTA's rows: 16, 32, 48 or 64
+      const int nm = mma_n<WIDE>(c.rows());
+      const int half = nm / 2;  // this CTA's rows: a multiple of 8 (WIDE) or 16, at most 64
       // wide stages load whole 64-row boxes (the MMA reads the first half rows)
       const uint32_t tx = WIDE ? 2u * static_cast<uint32_t>(Gm::kStageBytes)
                                : 2u * static_cast<uint32_t>(kABytes + half * kRowBytes);
@@ -213,7 +223,8 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
   for (uint32_t u = cluster_id(); u < n_units && !failed; u += n_clusters()) {
     ChunkIt c;
     for (c.start(&a, u / a.k_units); c.valid() && !failed; c.next()) {
-      const uint32_t idesc = ptx::idesc_make(kFmt, 2 * kOK, static_cast<uint32_t>(mma_n(c.rows())));
+      const uint32_t idesc =
+          ptx::idesc_make(kFmt, 2 * kOK, static_cast<uint32_t>(mma_n<WIDE>(c.rows())));
       if (!ptx::mbar_wait_cluster(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
         failed = true;
         break;
@@ -275,8 +286,8 @@ __device__ __forceinline__ uint32_t row_col(int row, uint32_t own) {
 
 // Epilogue warp q (of 4) owns tensor-memory lanes 32 q .. 32 q + 31: one d_x
 // column k each, for every token of the slab.
-__device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, uint32_t n_units,
-                         uint32_t rank) {
+__device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
+                         uint32_t tmem_base, const OwnerArgs& a, uint32_t n_units, uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,7 +297,7 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
   const int64_t K = a.K;
   const int T = a.slab_tokens;
   const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16);
-  int acc = 0;
+  int acc = 0, obuf = 0;
   uint32_t aph = 0;
   bool stop = false;
   for (uint32_t u = cluster_id(); u < n_units && !stop; u += n_clusters()) {
@@ -371,14 +382,31 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
     }
     if (stop) break;
     // the slab is done: this thread's column to d_x (every token of the
-    // slab has at least one row, so every element was stored above)
+    // slab has at least one row, so every element was stored above), 32
+    // tokens at a time: through a shared-memory buffer and a TMA store when
+    // d_x rows allow it, else with 128-byte warp stores
     int64_t nt = a.batch - tok0;
     if (nt > T) nt = T;
     for (int t0 = 0; t0 < static_cast<int>(nt); t0 += 32) {
       uint32_t w[32];
       ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(kSlabCol + t0), w);
       ptx::tmem_ld_wait_regs(w);
-      if (k < K) {
+      if (a.tma_out) {
+        float* sb = out_stage + obuf * kOutBuf;
+        // the store that last read this buffer (two groups ago) is done
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) sb[t * 32 + lane] = __uint_as_float(w[t]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        // (a warp whose 32 columns all lie past K has nothing to store)
+        if (lane == 0 && k < K) {
+          ptx::tma_store_2d(tout, sb, static_cast<int32_t>(k), static_cast<int32_t>(tok0 + t0));
+          ptx::bulk_commit();
+        }
+        obuf ^= 1;
+      } else if (k < K) {
         float* dst = a.out + (tok0 + t0) * K + k;
 #pragma unroll
         for (int t = 0; t < 32; ++t)
@@ -386,6 +414,9 @@ __device__ void epilogue(OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a, ui
       }
     }
   }
+  // the stores have read shared memory and written d_x before the CTA exits
+  if (lane == 0) ptx::bulk_wait<0>();
+  __syncwarp();
 }
 
 template <int DT, bool WIDE>
@@ -395,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  auto* ctl = reinterpret_cast<OwnCtl*>(smem + Gm::kStages * Gm::kStageBytes);
+  float* out_stage = reinterpret_cast<float*>(smem + Gm::kStages * Gm::kStageBytes);
+  auto* ctl = reinterpret_cast<OwnCtl*>(smem + Gm::kStages * Gm::kStageBytes + kOutBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
@@ -434,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kDyMaps; ++j) ptx::tma_prefetch_desc(&m.dy.box[j]);
       ptx::tma_prefetch_desc(&m.tw);
     }
+    if (a.tma_out) ptx::tma_prefetch_desc(&m.tout);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
@@ -450,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_issuer<DT, WIDE>(smem, ctl, tmem_base, a, n_units);
   } else {
-    epilogue(ctl, tmem_base, a, n_units, rank);
+    epilogue(ctl, out_stage + (warp & 3) * 2 * kOutBuf, &m.tout, tmem_base, a, n_units, rank);
   }
 
   ptx::tc_fence_before_sync();

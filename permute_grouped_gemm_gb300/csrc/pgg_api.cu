@@ -282,6 +282,22 @@ int encode_owner_wide_maps(const Plan& p, const void* dy, const void* w, OwnerMa
   return PGG_OK;
 }
 
+// d_x [batch, K] fp32 for the owner kernel's write-out: boxes of 32 k x 32
+// tokens, no swizzle; stores past K or batch are clipped.
+int encode_owner_out_map(const Plan& p, float* out, CUtensorMap* m) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PGG_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.batch)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Common front half of every entry point that enqueues work.
@@ -387,6 +403,13 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
     om.tw = tw;
     std::memset(&om.tw4, 0, sizeof(om.tw4));
     std::memset(&om.dy3, 0, sizeof(om.dy3));
+    std::memset(&om.tout, 0, sizeof(om.tout));
+    o.tma_out = 0;
+    if (plan.K % 4 == 0 && aligned(out, 16)) {
+      rc = encode_owner_out_map(plan, out, &om.tout);
+      if (rc != PGG_OK) return rc;
+      o.tma_out = 1;
+    }
     if (plan.N % 64 == 0) {
       rc = encode_owner_wide_maps(plan, gradY, weight, &om);
       if (rc != PGG_OK) return rc;

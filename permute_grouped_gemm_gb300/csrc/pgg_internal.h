@@ -111,17 +111,20 @@ struct OwnerArgs {
   int32_t k_units;  // ceil(K / 256): k ranges of a CTA pair
   int32_t nk;       // reduction steps: ceil(N / 128) when wide, else ceil(N / 64)
   int32_t wide;     // 1: stages of two 64-n panels (N a multiple of 64)
+  int32_t tma_out;  // 1: d_x written by TMA stores (K % 4 == 0, out 16-byte aligned)
   uint64_t wait_limit_ns;
 };
 
 // Tensor maps of the owner kernel: the d_x kernel's (d_y boxes of 16 << j rows,
-// weight {N, K, G}) and, for wide stages, weight {64, K, N / 64, G} with boxes
-// {64, 128, 2, 1} and d_y {64, M, N / 64} with boxes {64, 64, 2}.
+// weight {N, K, G}); for wide stages, weight {64, K, N / 64, G} with boxes
+// {64, 128, 2, 1} and d_y {64, M, N / 64} with boxes {64, 64, 2}; for TMA
+// write-out, d_x {K, batch} fp32 with boxes {32, 32}.
 struct OwnerMaps {
   DyMaps dy;
   CUtensorMap tw;
   CUtensorMap tw4;
   CUtensorMap dy3;
+  CUtensorMap tout;
 };
 
 // Arguments of the FP32-pipe kernel used when the operands cannot be streamed

@@ -95,6 +95,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
 
 // TMA store of a shared-memory box to a 3-D tensor (elements outside the
 // tensor are not written), tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int32_t c0,
                                              int32_t c1, int32_t c2) {
   asm volatile(
