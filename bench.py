@@ -47,12 +47,15 @@ _COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh"]
 KERNEL_SOURCES = {
     "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", *_COMMON],
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
+    "gmm_dx_owner_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_owner.cu", *_COMMON],
+    "unpermute_grad_kernel": ["permute_grouped_gemm_gb300/csrc/unpermute_grad.cu"],
     "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", *_COMMON],
     "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],
     "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", *_COMMON],
     "gmm_fwd_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd_simt.cu", *_COMMON],
 }
 SIMT_VARIANT = 3
+OWNER_VARIANT = 4
 FP32_LANES_PER_SM = 128    # FP32 fused multiply-add lanes per SM
 NOMINAL_SM_MHZ = 2070.0    # maximum SM clock of the part
 
@@ -193,7 +196,13 @@ class DxOp:
         self.ws_bytes = pgg.pgg_dx_workspace_size(*self.sizes, w.row_idx_type, self.dt)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.out = torch.empty(w.batch, w.K, dtype=torch.float32, device=dev)
-        self.kernel = "gmm_dx_simt_kernel" if self.plan["variant"] == SIMT_VARIANT else "gmm_dx_kernel"
+        v = self.plan["variant"]
+        self.kernel = {SIMT_VARIANT: "gmm_dx_simt_kernel",
+                       OWNER_VARIANT: "gmm_dx_owner_kernel"}.get(v, "gmm_dx_kernel")
+        # routing step: scan, inverse, ranks (+ slab bounds for the owner
+        # kernel); grouped GEMM: one kernel (+ the ticketed kernel after the
+        # owner kernel, which works only when the rows are not sorted)
+        self.launches = 6 if v == OWNER_VARIANT else 4
 
     def values(self):
         return self.inp.grad_y, self.inp.weight
@@ -655,7 +664,7 @@ def run_ours(args):
                      "kernel": kernel, "algorithmic_flops": flops,
                      "algorithmic_bytes": nbytes},
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": getattr(op, "launches", 4) * args.steps,
         "wall_s_timed_region": t_wall,
     }
     if e2e:

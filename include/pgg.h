@@ -153,9 +153,13 @@ typedef struct {
   int32_t variant;          /* 0 = wide row blocks on CTA pairs (tensor-bound), 1 = narrow row
                                blocks (weight streaming), 2 = wide row blocks on single CTAs,
                                3 = FP32-pipe kernel (rows of N * sizeof(dtype) bytes that are
-                               not a multiple of 16); pgg_dx_execute also takes variant 3 when
-                               gradY or weight is not 16-byte aligned */
-  int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent */
+                               not a multiple of 16), 4 = owner kernel (each CTA pair owns a
+                               block of d_x: few experts per token, 16-bit dtypes; falls back
+                               to variant 0 when an expert's rows are not in increasing original
+                               position); pgg_dx_execute also takes variant 3 when gradY or
+                               weight is not 16-byte aligned */
+  int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent (variant 4: tokens per
+                               slab) */
   int32_t k_per_block;      /* output columns per CTA and tile (128; a CTA pair covers 256) */
   int32_t stages;           /* shared-memory pipeline depth */
   int32_t k_blocks;         /* ceil(K / k_per_block) */
@@ -180,9 +184,9 @@ const char* pgg_status_string(int status);
  * pgg_debug_set_ticket_bias: added to the ticket count each ordered
  *   scatter-add waits for; a positive bias makes every wait of a row with
  *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
- * pgg_debug_force_variant: -1 = automatic (default), 0, 1, 2 or 3 = force the
- *   variant reported by pgg_dx_plan (2 exists for the 16-bit dtypes only;
- *   rows that are not a multiple of 16 bytes always take variant 3).
+ * pgg_debug_force_variant: -1 = automatic (default), 0, 1, 2, 3 or 4 = force
+ *   the variant reported by pgg_dx_plan (2 and 4 exist for the 16-bit dtypes
+ *   only; rows that are not a multiple of 16 bytes always take variant 3).
  * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
  *   automatic). The result does not depend on it, bit for bit: only the time
  *   order of the tiles changes, never the order of the additions.

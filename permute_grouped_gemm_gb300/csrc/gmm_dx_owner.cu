@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int owner_smem_bytes(bool wide) { return wide ? smem_bytes<true>() : smem_bytes<false>(); }
+int owner_stages(bool wide) { return wide ? Geo<true>::kStages : Geo<false>::kStages; }
 int owner_threads() { return kThreads; }
 
 // m.tw4 / m.dy3 are read when a.wide is set (N a multiple of 64), m.dy / m.tw otherwise.

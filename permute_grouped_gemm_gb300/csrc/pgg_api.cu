@@ -48,6 +48,7 @@ int fwd_simt_smem_bytes();
 cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
                             cudaStream_t stream);
 int owner_smem_bytes(bool wide);
+int owner_stages(bool wide);
 int owner_threads();
 cudaError_t launch_owner(int dtype, const OwnerMaps& m, const OwnerArgs& a, int num_sms,
                          cudaStream_t stream);
@@ -667,7 +668,7 @@ int pgg_dx_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   info->variant = p.variant;
   info->rows_per_block = p.variant == kVariantOwner ? p.slab_tokens : p.rows_per_block;
   info->k_per_block = kKBlock;
-  info->stages = p.stages;
+  info->stages = p.variant == kVariantOwner ? owner_stages(p.N % 64 == 0) : p.stages;
   info->k_blocks = p.k_blocks;
   info->band_k_blocks = p.band_k_blocks;
   info->max_row_blocks = p.max_row_blocks;
