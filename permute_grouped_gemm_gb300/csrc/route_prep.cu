@@ -13,7 +13,8 @@
 //                           inv[idx[q]] = q; zeroes the scatter-add tickets.
 //   route_rank     (grid)   per token b: its topK expanded rows, the check that
 //                           the index is a permutation, and each row's rank
-//                           among the token's rows (increasing expanded index).
+//                           among the token's rows (increasing expanded index);
+//                           one lane per position when topK <= 32.
 //   route_owner    (grid)   owner variant only: whether each expert's rows are
 //                           in increasing original position, and where each
 //                           token slab starts inside each expert.
@@ -196,6 +197,43 @@ __global__ void route_rank_kernel(const int64_t* __restrict__ idx, const int32_t
   if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
 }
 
+// The same, one lane per original position for topK <= 32: a token's topK
+// positions sit in consecutive lanes of one warp, and each lane counts the
+// token's rows below its own through shuffles.
+__global__ void route_rank_lanes_kernel(const int64_t* __restrict__ idx,
+                                        const int32_t* __restrict__ inv, int64_t batch,
+                                        int top_k, int64_t M, int row_idx_type,
+                                        RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+  const int lane = threadIdx.x & 31;
+  const int per_warp = 32 / top_k;  // tokens per warp
+  const int slot = lane / top_k, j = lane - slot * top_k;
+  const int base = slot * top_k;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  bool bad = false;
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       w * per_warp < batch; w += warps) {
+    const int64_t b = w * per_warp + slot;
+    const bool valid = slot < per_warp && b < batch;
+    const int64_t i = valid ? row_of_position(idx, inv, b * top_k + j, M, row_idx_type) : -1;
+    int32_t rank = 0;
+    for (int j2 = 0; j2 < top_k; ++j2) {
+      const int64_t i2 = __shfl_sync(0xFFFFFFFFu, i, valid ? base + j2 : lane);
+      if (i2 >= 0 && i2 < i) ++rank;
+    }
+    if (valid) {
+      if (i < 0) {
+        bad = true;
+      } else {
+        RowInfo r;
+        r.token = static_cast<int32_t>(b);
+        r.rank = rank;
+        rowinfo[i] = r;
+      }
+    }
+  }
+  if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
+}
+
 __global__ void header_reset_kernel(WsHeader* hdr) {
   hdr->status = 0;
   hdr->sched_next = 0;
@@ -213,44 +251,55 @@ __device__ __forceinline__ int64_t position_of_row(const int64_t* idx, const int
 // Owner variant: (1) whether every expert's rows are in increasing original
 // position (then the rows of a token slab form one contiguous range inside
 // each expert); (2) seg[g][s] = first row of expert g whose position is at
-// least s * slab_tokens * topK (binary search, meaningful when sorted).
+// least s * slab_tokens * topK. Each row i of expert g writes the entries from
+// its predecessor's slab (exclusive) to its own (inclusive); the expert's last
+// row writes the rest with the expert's end, and empty experts write their
+// offset everywhere. Meaningful when sorted; every write stays inside seg.
+constexpr int kOffSmem = 2048;  // experts whose offsets fit in shared memory
+
 __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
                                    const int64_t* __restrict__ off, int64_t M, int64_t G,
                                    int64_t top_k, int row_idx_type, int n_slabs,
                                    int slab_tokens, int32_t* __restrict__ seg, WsHeader* hdr) {
+  __shared__ int64_t s_off[kOffSmem];
+  if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
+  const bool in_smem = G + 1 <= kOffSmem;
+  if (in_smem)
+    for (int64_t g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = off[g];
+  __syncthreads();
+  const int64_t* offs = in_smem ? s_off : off;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
+  const int64_t slab_rows = static_cast<int64_t>(slab_tokens) * top_k;
+  const int64_t ns = n_slabs;
   bool unsorted = false;
-  for (int64_t i = t0; i + 1 < M; i += stride) {
+  for (int64_t i = t0; i < M; i += stride) {
     // expert of row i: largest g with off[g] <= i
     int64_t lo = 0, hi = G;
     while (hi - lo > 1) {
       const int64_t mid = (lo + hi) >> 1;
-      if (off[mid] <= i)
+      if (offs[mid] <= i)
         lo = mid;
       else
         hi = mid;
     }
-    if (i + 1 < off[lo + 1] &&
-        position_of_row(idx, inv, i, row_idx_type) > position_of_row(idx, inv, i + 1, row_idx_type))
-      unsorted = true;
+    int32_t* row = seg + lo * (ns + 1);
+    const int64_t p = position_of_row(idx, inv, i, row_idx_type);
+    const int64_t sl = p / slab_rows;
+    int64_t prev = -1;
+    if (i > offs[lo]) {
+      const int64_t pp = position_of_row(idx, inv, i - 1, row_idx_type);
+      if (pp > p) unsorted = true;
+      prev = pp / slab_rows;
+    }
+    for (int64_t t = prev + 1; t <= sl && t <= ns; ++t) row[t] = static_cast<int32_t>(i);
+    if (i + 1 == offs[lo + 1])
+      for (int64_t t = sl + 1; t <= ns; ++t) row[t] = static_cast<int32_t>(i + 1);
   }
   if (unsorted) atomicOr(&hdr->unsorted, 1u);
-  const int64_t n_seg = G * (n_slabs + 1);
-  for (int64_t q = t0; q < n_seg; q += stride) {
-    const int64_t g = q / (n_slabs + 1), s = q - g * (n_slabs + 1);
-    const int64_t p0 = s * slab_tokens * top_k;
-    int64_t lo = off[g], hi = off[g + 1];  // first row in [lo, hi) with position >= p0
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (position_of_row(idx, inv, mid, row_idx_type) < p0)
-        lo = mid + 1;
-      else
-        hi = mid;
-    }
-    seg[q] = static_cast<int32_t>(lo);
-  }
+  for (int64_t g = t0; g < G; g += stride)
+    if (offs[g] == offs[g + 1])
+      for (int64_t t = 0; t <= ns; ++t) seg[g * (ns + 1) + t] = static_cast<int32_t>(offs[g]);
 }
 
 // Every original position must have an expanded row (see row_of_position).
@@ -302,11 +351,21 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
   route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, plan.M, inv, hdr,
                                                                      tickets4,
                                                                      plan.layout.n_tickets / 4);
-  int64_t rblocks = (plan.batch + 127) / 128;
-  if (rblocks > cap) rblocks = cap;
-  if (rblocks < 1) rblocks = 1;
-  route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
-      idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+  if (plan.topK <= 32) {
+    const int64_t per_block = 8 * (32 / plan.topK);  // tokens per 256-thread block
+    int64_t rblocks = (plan.batch + per_block - 1) / per_block;
+    if (rblocks > cap) rblocks = cap;
+    if (rblocks < 1) rblocks = 1;
+    route_rank_lanes_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
+        idx, inv, plan.batch, static_cast<int>(plan.topK), plan.M, plan.row_idx_type, rowinfo,
+        hdr);
+  } else {
+    int64_t rblocks = (plan.batch + 127) / 128;
+    if (rblocks > cap) rblocks = cap;
+    if (rblocks < 1) rblocks = 1;
+    route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
+        idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+  }
   if (plan.n_slabs > 0) {
     int64_t oblocks = (plan.M + 255) / 256;
     if (oblocks > cap) oblocks = cap;
