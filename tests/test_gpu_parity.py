@@ -180,6 +180,34 @@ def test_gather_and_scatter_forms_agree_bitwise(n):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+# The routing step ranks a token's rows with one lane per position when
+# topK <= 32 (topK lanes per token, 32 // topK tokens per warp, idle lanes when
+# topK does not divide 32) and with one thread per token above that.
+@pytest.mark.parametrize("top_k", [5, 32, 40])
+@pytest.mark.parametrize("row_idx_type", [0, 1])
+def test_many_experts_per_token(top_k, row_idx_type):
+    inp = make_case(batch=97, top_k=top_k, G=48, K=256, N=128, dtype="bf16", seed=17,
+                    row_idx_type=row_idx_type, device="cuda")
+    a = check(inp, what=f"topK {top_k}")
+    b, _ = run(inp)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    try:  # the owner kernel adds the same rows in the same order
+        pgg.pgg_debug_force_variant(4)
+        c, ws = run(inp)
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert pgg.status(ws) == 0
+    assert torch.equal(a.view(torch.int32), c.view(torch.int32))
+    # a position without an expanded row is still detected
+    idx = inp.expanded_row_idx.clone()
+    idx[3] = idx[4]
+    out = torch.full((97, 256), 7.0, device="cuda")
+    _, ws = pgg.dx(inp.grad_y, inp.weight, idx, inp.group_list, 97, top_k, row_idx_type, out=out)
+    torch.cuda.synchronize()
+    assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_NOT_PERM"
+    assert torch.count_nonzero(out) == 0
+
+
 @pytest.mark.parametrize("n", [64, 63])
 def test_device_detected_errors_zero_the_output(n):
     base = make_case(batch=64, top_k=2, G=4, K=128, N=n, dtype="bf16", seed=9, device="cuda")
