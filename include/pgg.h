@@ -398,6 +398,28 @@ int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* prob
                        void* workspace, size_t workspace_bytes, void* perm_grad, void* probs_grad,
                        pgg_stream_t stream);
 
+/*
+ * The same call in two stream-ordered stages, for callers that validate the
+ * routing once and apply it to several tensors, and for timing the kernel
+ * alone. pgg_unpermute_grad is exactly prep followed by apply.
+ *   pgg_unpermute_grad_prep   index validation and the inverse map, into the
+ *                             workspace (status word at offset 0).
+ *   pgg_unpermute_grad_apply  the unpermute kernel; reads the workspace that a
+ *                             prep of the same expandedRowIdx (same M, batch,
+ *                             topK, rowIdxType) filled earlier on the stream.
+ *                             Its arguments and checks are those of
+ *                             pgg_unpermute_grad.
+ */
+int pgg_unpermute_grad_prep(const int64_t* expandedRowIdx, int64_t M, int64_t batch, int64_t topK,
+                            int rowIdxType, void* workspace, size_t workspace_bytes,
+                            pgg_stream_t stream);
+
+int pgg_unpermute_grad_apply(const void* permuted, const void* d_out, const void* probs,
+                             const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
+                             int64_t topK, int rowIdxType, pgg_dtype dtype,
+                             pgg_dtype probs_grad_dtype, void* workspace, size_t workspace_bytes,
+                             void* perm_grad, void* probs_grad, pgg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

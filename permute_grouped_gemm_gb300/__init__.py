@@ -14,7 +14,8 @@ from ._lib import (  # noqa: F401
     pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
     pgg_dw_execute, pgg_dw_grouped_gemm, pgg_dw_plan, pgg_dw_workspace_size,
     pgg_fwd_execute, pgg_fwd_grouped_gemm, pgg_fwd_plan, pgg_fwd_route_prep,
-    pgg_fwd_workspace_size, pgg_unpermute_grad, pgg_unpermute_grad_workspace_size,
+    pgg_fwd_workspace_size, pgg_unpermute_grad, pgg_unpermute_grad_apply,
+    pgg_unpermute_grad_prep, pgg_unpermute_grad_workspace_size,
     pgg_dx_execute, pgg_dx_execute_static_scratch, pgg_dx_grouped_gemm, pgg_dx_plan,
     pgg_dx_route_prep,
     pgg_dx_workspace_size, pgg_status_string,

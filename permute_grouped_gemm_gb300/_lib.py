@@ -81,8 +81,11 @@ def load(path: str | None = None):
                 ctypes.POINTER(sz)]
             lib.pgg_unpermute_grad.argtypes = [vp, vp, vp, vp] + [ctypes.c_int64] * 4 + [
                 i32, i32, i32, vp, sz, vp, vp, vp]
-            lib.pgg_unpermute_grad_workspace_size.restype = ctypes.c_int
-            lib.pgg_unpermute_grad.restype = ctypes.c_int
+            lib.pgg_unpermute_grad_apply.argtypes = lib.pgg_unpermute_grad.argtypes
+            lib.pgg_unpermute_grad_prep.argtypes = [vp] + [ctypes.c_int64] * 3 + [i32, vp, sz, vp]
+            for f in ("pgg_unpermute_grad_workspace_size", "pgg_unpermute_grad",
+                      "pgg_unpermute_grad_prep", "pgg_unpermute_grad_apply"):
+                getattr(lib, f).restype = ctypes.c_int
             for f in ("pgg_fwd_workspace_size", "pgg_fwd_plan", "pgg_fwd_execute",
                       "pgg_fwd_grouped_gemm", "pgg_fwd_route_prep"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -235,6 +238,23 @@ def pgg_unpermute_grad(permuted, d_out, probs, expandedRowIdx, M, H, batch, topK
                                      H, batch, topK, rowIdxType, dtype, probs_grad_dtype,
                                      workspace, workspace_bytes, perm_grad, probs_grad or None,
                                      stream)
+
+
+def pgg_unpermute_grad_prep(expandedRowIdx, M, batch, topK, rowIdxType, workspace,
+                            workspace_bytes, stream) -> int:
+    """Raw call: index validation and inverse map into the workspace."""
+    return load().pgg_unpermute_grad_prep(expandedRowIdx, M, batch, topK, rowIdxType, workspace,
+                                          workspace_bytes, stream)
+
+
+def pgg_unpermute_grad_apply(permuted, d_out, probs, expandedRowIdx, M, H, batch, topK,
+                             rowIdxType, dtype, probs_grad_dtype, workspace, workspace_bytes,
+                             perm_grad, probs_grad, stream) -> int:
+    """Raw call: the unpermute kernel on a workspace filled by the prep step."""
+    return load().pgg_unpermute_grad_apply(permuted or None, d_out, probs or None,
+                                           expandedRowIdx, M, H, batch, topK, rowIdxType, dtype,
+                                           probs_grad_dtype, workspace, workspace_bytes,
+                                           perm_grad, probs_grad or None, stream)
 
 
 def pgg_status_string(code: int) -> str:

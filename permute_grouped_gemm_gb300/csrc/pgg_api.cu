@@ -889,26 +889,57 @@ int pgg_unpermute_grad_workspace_size(int64_t M, int64_t batch, int64_t topK,
   return PGG_OK;
 }
 
-int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* probs,
-                       const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
-                       int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_dtype probs_grad_dtype,
-                       void* workspace, size_t workspace_bytes, void* perm_grad, void* probs_grad,
-                       pgg_stream_t stream) {
-  if (!d_out || !expandedRowIdx || !workspace || !perm_grad) return PGG_ERR_NULL;
+namespace {
+
+// Host checks shared by the unpermute entry points: sizes, attributes and the
+// workspace (pointers of the values are checked by the apply step).
+int unperm_check(const int64_t* idx, int64_t M, int64_t batch, int64_t topK, int rowIdxType,
+                 const void* workspace, size_t workspace_bytes) {
+  if (!idx || !workspace) return PGG_ERR_NULL;
+  if (rowIdxType != 0 && rowIdxType != 1) return PGG_ERR_ATTR;
+  size_t need = 0;
+  const int rc = pgg_unpermute_grad_workspace_size(M, batch, topK, &need);
+  if (rc != PGG_OK) return rc;
+  if (!aligned(workspace, 256) || !aligned(idx, 8)) return PGG_ERR_ALIGN;
+  if (workspace_bytes < need) return PGG_ERR_WORKSPACE;
+  return PGG_OK;
+}
+
+}  // namespace
+
+int pgg_unpermute_grad_prep(const int64_t* expandedRowIdx, int64_t M, int64_t batch, int64_t topK,
+                            int rowIdxType, void* workspace, size_t workspace_bytes,
+                            pgg_stream_t stream) {
+  int rc = unperm_check(expandedRowIdx, M, batch, topK, rowIdxType, workspace, workspace_bytes);
+  if (rc != PGG_OK) return rc;
+  DeviceInfo di;
+  if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
+  char* w = static_cast<char*>(workspace);
+  return launch_index_prep(expandedRowIdx, M, rowIdxType,
+                           reinterpret_cast<int32_t*>(w + unperm_inv_offset()),
+                           reinterpret_cast<WsHeader*>(w), di.num_sms,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PGG_OK
+             : PGG_ERR_CUDA;
+}
+
+int pgg_unpermute_grad_apply(const void* permuted, const void* d_out, const void* probs,
+                             const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
+                             int64_t topK, int rowIdxType, pgg_dtype dtype,
+                             pgg_dtype probs_grad_dtype, void* workspace, size_t workspace_bytes,
+                             void* perm_grad, void* probs_grad, pgg_stream_t stream) {
+  if (!d_out || !perm_grad) return PGG_ERR_NULL;
   if (probs && (!permuted || !probs_grad)) return PGG_ERR_NULL;
   if (dtype != PGG_F32 && dtype != PGG_F16 && dtype != PGG_BF16) return PGG_ERR_DTYPE;
   if (probs_grad_dtype != dtype && probs_grad_dtype != PGG_F32) return PGG_ERR_DTYPE;
-  if (rowIdxType != 0 && rowIdxType != 1) return PGG_ERR_ATTR;
-  if (H <= 0 || H > kInt32Max) return PGG_ERR_SHAPE;
-  size_t need = 0;
-  int rc = pgg_unpermute_grad_workspace_size(M, batch, topK, &need);
+  int rc = unperm_check(expandedRowIdx, M, batch, topK, rowIdxType, workspace, workspace_bytes);
   if (rc != PGG_OK) return rc;
+  if (H <= 0 || H > kInt32Max) return PGG_ERR_SHAPE;
   const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
-  if (!aligned(workspace, 256) || !aligned(expandedRowIdx, 8) || !aligned(d_out, es) ||
-      !aligned(perm_grad, es) || (probs && (!aligned(permuted, es) || !aligned(probs, es) ||
-                                            !aligned(probs_grad, elem_size(probs_grad_dtype)))))
+  if (!aligned(d_out, es) || !aligned(perm_grad, es) ||
+      (probs && (!aligned(permuted, es) || !aligned(probs, es) ||
+                 !aligned(probs_grad, elem_size(probs_grad_dtype)))))
     return PGG_ERR_ALIGN;
-  if (workspace_bytes < need) return PGG_ERR_WORKSPACE;
   DeviceInfo di;
   if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
   char* w = static_cast<char*>(workspace);
@@ -927,18 +958,40 @@ int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* prob
   a.topK = topK;
   a.row_idx_type = rowIdxType;
   a.probs_grad_f32 = probs_grad_dtype == PGG_F32 ? 1 : 0;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_index_prep(expandedRowIdx, M, rowIdxType,
-                        reinterpret_cast<int32_t*>(w + unperm_inv_offset()), a.hdr, di.num_sms,
-                        s) != cudaSuccess)
-    return PGG_ERR_CUDA;
   const bool vec = (H * static_cast<int64_t>(es)) % 16 == 0 && aligned(d_out, 16) &&
                    aligned(perm_grad, 16) && (!probs || aligned(permuted, 16));
   const bool pairs = H % 2 == 0 && aligned(d_out, 4) && aligned(perm_grad, 4) &&
                      (!probs || aligned(permuted, 4));
-  return launch_unpermute_grad(dtype, a, vec, pairs, di.num_sms, s) == cudaSuccess
+  return launch_unpermute_grad(dtype, a, vec, pairs, di.num_sms,
+                               reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PGG_OK
              : PGG_ERR_CUDA;
+}
+
+int pgg_unpermute_grad(const void* permuted, const void* d_out, const void* probs,
+                       const int64_t* expandedRowIdx, int64_t M, int64_t H, int64_t batch,
+                       int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_dtype probs_grad_dtype,
+                       void* workspace, size_t workspace_bytes, void* perm_grad, void* probs_grad,
+                       pgg_stream_t stream) {
+  // every host check before anything is enqueued
+  if (!d_out || !expandedRowIdx || !workspace || !perm_grad) return PGG_ERR_NULL;
+  if (probs && (!permuted || !probs_grad)) return PGG_ERR_NULL;
+  if (dtype != PGG_F32 && dtype != PGG_F16 && dtype != PGG_BF16) return PGG_ERR_DTYPE;
+  if (probs_grad_dtype != dtype && probs_grad_dtype != PGG_F32) return PGG_ERR_DTYPE;
+  int rc = unperm_check(expandedRowIdx, M, batch, topK, rowIdxType, workspace, workspace_bytes);
+  if (rc != PGG_OK) return rc;
+  if (H <= 0 || H > kInt32Max) return PGG_ERR_SHAPE;
+  const uintptr_t es = static_cast<uintptr_t>(elem_size(dtype));
+  if (!aligned(d_out, es) || !aligned(perm_grad, es) ||
+      (probs && (!aligned(permuted, es) || !aligned(probs, es) ||
+                 !aligned(probs_grad, elem_size(probs_grad_dtype)))))
+    return PGG_ERR_ALIGN;
+  rc = pgg_unpermute_grad_prep(expandedRowIdx, M, batch, topK, rowIdxType, workspace,
+                               workspace_bytes, stream);
+  if (rc != PGG_OK) return rc;
+  return pgg_unpermute_grad_apply(permuted, d_out, probs, expandedRowIdx, M, H, batch, topK,
+                                  rowIdxType, dtype, probs_grad_dtype, workspace, workspace_bytes,
+                                  perm_grad, probs_grad, stream);
 }
 
 const char* pgg_status_string(int status) {

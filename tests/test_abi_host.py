@@ -211,3 +211,32 @@ def test_unpermute_grad_host_errors(lib):
     assert code(d_out=fake + 1) == "PGG_ERR_ALIGN"
     assert code(rowIdxType=2) == "PGG_ERR_ATTR"
     assert code(M=999) == "PGG_ERR_SHAPE"
+
+
+def test_unpermute_grad_two_stage_host_errors(lib):
+    fake = 1 << 20
+    need = pgg.pgg_unpermute_grad_workspace_size(1000, 250, 4)
+    prep = dict(expandedRowIdx=fake, M=1000, batch=250, topK=4, rowIdxType=0, workspace=fake,
+                workspace_bytes=need, stream=None)
+
+    def prep_code(**o):
+        return pgg.STATUS[pgg.pgg_unpermute_grad_prep(**dict(prep, **o))]
+
+    assert prep_code(expandedRowIdx=0) == "PGG_ERR_NULL"
+    assert prep_code(workspace_bytes=need - 1) == "PGG_ERR_WORKSPACE"
+    assert prep_code(rowIdxType=2) == "PGG_ERR_ATTR"
+    assert prep_code(M=999) == "PGG_ERR_SHAPE"
+    assert prep_code(workspace=fake + 128) == "PGG_ERR_ALIGN"
+    apply = dict(permuted=fake, d_out=fake, probs=fake, expandedRowIdx=fake, M=1000, H=512,
+                 batch=250, topK=4, rowIdxType=0, dtype=pgg.PGG_BF16,
+                 probs_grad_dtype=pgg.PGG_BF16, workspace=fake, workspace_bytes=need,
+                 perm_grad=fake, probs_grad=fake, stream=None)
+
+    def apply_code(**o):
+        return pgg.STATUS[pgg.pgg_unpermute_grad_apply(**dict(apply, **o))]
+
+    assert apply_code(probs_grad_dtype=pgg.PGG_F16) == "PGG_ERR_DTYPE"
+    assert apply_code(workspace_bytes=need - 1) == "PGG_ERR_WORKSPACE"
+    assert apply_code(probs_grad=0) == "PGG_ERR_NULL"
+    assert apply_code(perm_grad=fake + 1) == "PGG_ERR_ALIGN"
+    assert apply_code(H=0) == "PGG_ERR_SHAPE"

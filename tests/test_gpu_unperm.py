@@ -98,6 +98,31 @@ def test_bitwise_repeatable_and_index_forms():
     assert torch.equal(qg.view(torch.int16), qg3.view(torch.int16))
 
 
+
+def test_prep_then_apply_equals_the_one_call():
+    inp = make_case(batch=300, top_k=6, G=8, K=16, N=520, dtype="fp16", seed=44,
+                    row_idx_type=1, device="cuda")
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs)
+    M, H = inp.grad_y.shape
+    need = pgg.pgg_unpermute_grad_workspace_size(M, inp.batch, inp.top_k)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pg2 = torch.empty_like(pg)
+    qg2 = torch.empty_like(qg)
+    dt = pgg.dtype_code(inp.grad_y.dtype)
+    sp = torch.cuda.current_stream().cuda_stream
+    idx = inp.expanded_row_idx
+    assert pgg.pgg_unpermute_grad_prep(idx.data_ptr(), M, inp.batch, inp.top_k,
+                                       inp.row_idx_type, ws.data_ptr(), need, sp) == 0
+    assert pgg.pgg_unpermute_grad_apply(inp.grad_y.data_ptr(), d_out.data_ptr(), probs.data_ptr(),
+                                        idx.data_ptr(), M, H, inp.batch, inp.top_k,
+                                        inp.row_idx_type, dt, dt, ws.data_ptr(), need,
+                                        pg2.data_ptr(), qg2.data_ptr(), sp) == 0
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(pg.view(torch.int16), pg2.view(torch.int16))
+    assert torch.equal(qg.view(torch.int16), qg2.view(torch.int16))
+
 @pytest.mark.parametrize("shift", [1, 2])
 def test_misaligned_pointers_use_the_narrower_paths(shift):
     # shift 1 element: 2-byte accesses; 2 elements: 4-byte pairs
