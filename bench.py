@@ -201,10 +201,14 @@ class DxOp:
         v = self.plan["variant"]
         self.kernel = {SIMT_VARIANT: "gmm_dx_simt_kernel",
                        OWNER_VARIANT: "gmm_dx_owner_kernel"}.get(v, "gmm_dx_kernel")
-        # routing step: scan, inverse, ranks (+ slab bounds for the owner
-        # kernel); grouped GEMM: one kernel (+ the ticketed kernel after the
-        # owner kernel, which works only when the rows are not sorted)
-        self.launches = 6 if v == OWNER_VARIANT else 4
+        # routing step: scan, inverse, ranks (the owner kernel's slab bounds
+        # in the same launch for topK <= 32, in a fourth above); grouped GEMM:
+        # one kernel (+ the ticketed kernel after the owner kernel, which works
+        # only when the rows are not sorted)
+        if v == OWNER_VARIANT:
+            self.launches = 5 if w.top_k <= 32 else 6
+        else:
+            self.launches = 4
 
     def values(self):
         return self.inp.grad_y, self.inp.weight

@@ -3,8 +3,9 @@
 // list of blocks over all non-empty experts, and the inverse of the routing
 // index for rowIdxType 1).
 //
-// Three small launches (four for the owner variant of the d_x kernel), in
-// stream order:
+// Three small launches, in stream order (for the owner variant of the d_x
+// kernel the rank launch also writes the slab bounds; a fourth launch does it
+// when topK > 32):
 //   route_scan     (1 CTA)  exclusive scan of groupList -> off[G+1]; row-block
 //                           counts and their scan -> rbstart[G+1]; the row-block
 //                           list {expert, first row, rows}; header reset; the
@@ -200,10 +201,9 @@ __global__ void route_rank_kernel(const int64_t* __restrict__ idx, const int32_t
 // The same, one lane per original position for topK <= 32: a token's topK
 // positions sit in consecutive lanes of one warp, and each lane counts the
 // token's rows below its own through shuffles.
-__global__ void route_rank_lanes_kernel(const int64_t* __restrict__ idx,
-                                        const int32_t* __restrict__ inv, int64_t batch,
-                                        int top_k, int64_t M, int row_idx_type,
-                                        RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+__device__ void rank_lanes(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                           int64_t batch, int top_k, int64_t M, int row_idx_type,
+                           RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
   const int lane = threadIdx.x & 31;
   const int per_warp = 32 / top_k;  // tokens per warp
   const int slot = lane / top_k, j = lane - slot * top_k;
@@ -234,6 +234,13 @@ __global__ void route_rank_lanes_kernel(const int64_t* __restrict__ idx,
   if (bad) atomicCAS(&hdr->status, 0u, kStNotPerm);
 }
 
+__global__ void route_rank_lanes_kernel(const int64_t* __restrict__ idx,
+                                        const int32_t* __restrict__ inv, int64_t batch,
+                                        int top_k, int64_t M, int row_idx_type,
+                                        RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+  rank_lanes(idx, inv, batch, top_k, M, row_idx_type, rowinfo, hdr);
+}
+
 __global__ void header_reset_kernel(WsHeader* hdr) {
   hdr->status = 0;
   hdr->sched_next = 0;
@@ -257,19 +264,14 @@ __device__ __forceinline__ int64_t position_of_row(const int64_t* idx, const int
 // offset everywhere. Meaningful when sorted; every write stays inside seg.
 constexpr int kOffSmem = 2048;  // experts whose offsets fit in shared memory
 
-__global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
-                                   const int64_t* __restrict__ off, int64_t M, int64_t G,
-                                   int64_t top_k, int row_idx_type, int n_slabs,
-                                   int slab_tokens, int32_t* __restrict__ seg, WsHeader* hdr) {
-  __shared__ int64_t s_off[kOffSmem];
-  if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
-  const bool in_smem = G + 1 <= kOffSmem;
-  if (in_smem)
-    for (int64_t g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = off[g];
-  __syncthreads();
-  const int64_t* offs = in_smem ? s_off : off;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+// The owner work over rows t0, t0 + stride, ... and experts likewise. Robust
+// to an index that is not a permutation (its check may run concurrently):
+// positions outside [0, M) only mark the rows unsorted, and every write stays
+// inside seg.
+__device__ void owner_rows(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                           const int64_t* offs, int64_t M, int64_t G, int64_t top_k,
+                           int row_idx_type, int n_slabs, int slab_tokens,
+                           int32_t* __restrict__ seg, WsHeader* hdr, int64_t t0, int64_t stride) {
   const int64_t slab_rows = static_cast<int64_t>(slab_tokens) * top_k;
   const int64_t ns = n_slabs;
   bool unsorted = false;
@@ -285,12 +287,16 @@ __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_
     }
     int32_t* row = seg + lo * (ns + 1);
     const int64_t p = position_of_row(idx, inv, i, row_idx_type);
+    if (p < 0 || p >= M) {
+      unsorted = true;
+      continue;
+    }
     const int64_t sl = p / slab_rows;
     int64_t prev = -1;
     if (i > offs[lo]) {
       const int64_t pp = position_of_row(idx, inv, i - 1, row_idx_type);
-      if (pp > p) unsorted = true;
-      prev = pp / slab_rows;
+      if (pp < 0 || pp >= M || pp > p) unsorted = true;
+      prev = (pp < 0 || pp >= M) ? sl : pp / slab_rows;
     }
     for (int64_t t = prev + 1; t <= sl && t <= ns; ++t) row[t] = static_cast<int32_t>(i);
     if (i + 1 == offs[lo + 1])
@@ -300,6 +306,45 @@ __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_
   for (int64_t g = t0; g < G; g += stride)
     if (offs[g] == offs[g + 1])
       for (int64_t t = 0; t <= ns; ++t) seg[g * (ns + 1) + t] = static_cast<int32_t>(offs[g]);
+}
+
+// Expert offsets in shared memory when they fit (the caller syncs).
+__device__ const int64_t* stage_offsets(const int64_t* off, int64_t G, int64_t* s_off) {
+  if (G + 1 > kOffSmem) return off;
+  for (int64_t g = threadIdx.x; g <= G; g += blockDim.x) s_off[g] = off[g];
+  return s_off;
+}
+
+__global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
+                                   const int64_t* __restrict__ off, int64_t M, int64_t G,
+                                   int64_t top_k, int row_idx_type, int n_slabs,
+                                   int slab_tokens, int32_t* __restrict__ seg, WsHeader* hdr) {
+  __shared__ int64_t s_off[kOffSmem];
+  if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
+  const int64_t* offs = stage_offsets(off, G, s_off);
+  __syncthreads();
+  owner_rows(idx, inv, offs, M, G, top_k, row_idx_type, n_slabs, slab_tokens, seg, hdr,
+             static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+             static_cast<int64_t>(gridDim.x) * blockDim.x);
+}
+
+// The lane-per-position ranks and, in the same launch, the owner work (for
+// the owner variant with topK <= 32).
+__global__ void route_rank_owner_kernel(const int64_t* __restrict__ idx,
+                                        const int32_t* __restrict__ inv,
+                                        const int64_t* __restrict__ off, int64_t batch, int top_k,
+                                        int64_t M, int64_t G, int row_idx_type, int n_slabs,
+                                        int slab_tokens, RowInfo* __restrict__ rowinfo,
+                                        int32_t* __restrict__ seg, WsHeader* hdr) {
+  __shared__ int64_t s_off[kOffSmem];
+  const uint32_t st = hdr->status;  // index range or group sum already wrong: no order
+  const int64_t* offs = stage_offsets(off, G, s_off);
+  __syncthreads();
+  rank_lanes(idx, inv, batch, top_k, M, row_idx_type, rowinfo, hdr);
+  if (st == 0)
+    owner_rows(idx, inv, offs, M, G, top_k, row_idx_type, n_slabs, slab_tokens, seg, hdr,
+               static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+               static_cast<int64_t>(gridDim.x) * blockDim.x);
 }
 
 // Every original position must have an expanded row (see row_of_position).
@@ -351,14 +396,28 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
   route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, plan.M, inv, hdr,
                                                                      tickets4,
                                                                      plan.layout.n_tickets / 4);
+  bool owner_done = false;
   if (plan.topK <= 32) {
     const int64_t per_block = 8 * (32 / plan.topK);  // tokens per 256-thread block
     int64_t rblocks = (plan.batch + per_block - 1) / per_block;
+    if (plan.n_slabs > 0) {
+      // ranks and slab bounds in one launch: enough blocks for the rows too
+      const int64_t oblocks = (plan.M + 255) / 256;
+      if (oblocks > rblocks) rblocks = oblocks;
+    }
     if (rblocks > cap) rblocks = cap;
     if (rblocks < 1) rblocks = 1;
-    route_rank_lanes_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
-        idx, inv, plan.batch, static_cast<int>(plan.topK), plan.M, plan.row_idx_type, rowinfo,
-        hdr);
+    if (plan.n_slabs > 0) {
+      route_rank_owner_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
+          idx, inv, off, plan.batch, static_cast<int>(plan.topK), plan.M, plan.G,
+          plan.row_idx_type, plan.n_slabs, plan.slab_tokens, rowinfo,
+          reinterpret_cast<int32_t*>(ws + L.seg), hdr);
+      owner_done = true;
+    } else {
+      route_rank_lanes_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
+          idx, inv, plan.batch, static_cast<int>(plan.topK), plan.M, plan.row_idx_type, rowinfo,
+          hdr);
+    }
   } else {
     int64_t rblocks = (plan.batch + 127) / 128;
     if (rblocks > cap) rblocks = cap;
@@ -366,7 +425,7 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
     route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
         idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
   }
-  if (plan.n_slabs > 0) {
+  if (plan.n_slabs > 0 && !owner_done) {
     int64_t oblocks = (plan.M + 255) / 256;
     if (oblocks > cap) oblocks = cap;
     if (oblocks < 1) oblocks = 1;
