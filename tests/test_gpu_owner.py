@@ -142,3 +142,17 @@ def test_uniform_workload_full_size():
     toks = np.sort(np.random.default_rng(7).choice(w.batch, 64, replace=False))
     check(inp, out, tokens=toks, what=w.name)
     assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
+
+
+def test_large_few_expert_problem_plans_and_matches_the_owner_kernel():
+    # 16384 tokens, topK 4, 8 experts: 224-token slabs (74) x 4 k ranges = 296 units,
+    # some experts' slab rows above 128 (chunk splits), N a multiple of 64 (two-panel stages)
+    inp = make_case(batch=16384, top_k=4, G=8, K=1024, N=512, dtype="bf16", seed=55,
+                    device="cuda")
+    M = inp.grad_y.shape[0]
+    p = pgg.pgg_dx_plan(M, 512, 1024, 8, M, 16384, 4, 0, pgg.PGG_BF16)
+    assert p["variant"] == 4 and p["rows_per_block"] == 224
+    out = run(inp)
+    toks = np.sort(np.random.default_rng(9).choice(inp.batch, 64, replace=False))
+    check(inp, out, tokens=toks, what="large few-expert")
+    assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
