@@ -62,6 +62,28 @@ def test_static_scratch_matches_workspace_entry_point(dtype, row_idx_type):
         assert err <= TOL * scale, f"max|diff| {err:.3e} > {TOL} * {scale:.3e}"
 
 
+def test_static_scratch_with_the_owner_plan():
+    # few experts per token: the automatic plan is the owner kernel, whose workspace also
+    # holds the slab bounds; both entry points run the same plan, so they agree bit for bit
+    inp = make_case(batch=2048, top_k=8, G=16, K=4096, N=128, dtype="bf16", seed=22,
+                    device="cuda")
+    w = inp.workload
+    assert pgg.pgg_dx_plan(w.M, w.N, w.K, w.G, w.M, w.batch, w.top_k, 0,
+                           pgg.PGG_BF16)["variant"] == 4
+    ref, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                     inp.batch, inp.top_k, inp.row_idx_type)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out = torch.full((inp.batch, w.K), float("nan"), device="cuda")
+        rc = call_static(inp, out, status)
+        assert rc == 0, pgg.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+
+
 def test_sizes_beyond_the_scratch_are_rejected():
     # batch 1M tokens x topK 8 at K = 7168 needs far more than 8 MiB of index
     # tables; the call is refused on the host before any pointer is used
