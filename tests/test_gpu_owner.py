@@ -73,6 +73,10 @@ CASES = {
     "chunk_split": dict(batch=1000, top_k=8, G=2, K=512, N=192, routing="replacement"),
     # many experts: 256-token slabs with a few rows of each expert
     "wide_slabs": dict(batch=800, top_k=2, G=40, K=300, N=256),
+    # one two-panel stage whose second panel is past N (read as zero)
+    "n_is_64": dict(batch=600, top_k=4, G=4, K=256, N=64),
+    # one 64-n stage whose box reaches past the 16 values of a row
+    "n_is_16": dict(batch=600, top_k=4, G=4, K=256, N=16),
 }
 
 
