@@ -674,7 +674,7 @@ def run_ours(args):
         "metric": op.metric, "value": value, "unit": value_unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded; routing and value recipe in DESIGN.md)",
+        "dtype": w.dtype, "data": "synthetic (seeded; routing and value recipe in workloads/moe.py)",
         "config": {**w.describe(), "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                    "plan": plan, **({"op": op.name} if op.name != "dx" else {})},
