@@ -24,6 +24,10 @@ Recipe (the same for every workload, seed 0 unless stated):
    expert at a time so that the fp32 staging stays small. For the weight
    gradient, the forward input x ~ N(0, 1) with shape [batch, K] (seed + 2,
    ``forward_input``).
+4. Unpermute backward (``unpermute_inputs``): grad_y [M, N] stands for the
+   expert outputs being combined; d_out ~ N(0, 1) with shape [batch, N]
+   (seed + 3); probs uniform in (0, 1] plus 1e-3, normalised per token
+   (seed + 4); both rounded to the workload dtype.
 
 The pages' shapes: M ~ 108K expanded tokens, K = 7168, G = 60, N = 2048
 ("MoeInitRoutingGroupedMatmulGrad design", section 1.2 and the d_weight
