@@ -160,3 +160,33 @@ def test_large_few_expert_problem_plans_and_matches_the_owner_kernel():
     toks = np.sort(np.random.default_rng(9).choice(inp.batch, 64, replace=False))
     check(inp, out, tokens=toks, what="large few-expert")
     assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        top_k = int(rng.integers(1, 9))
+        G = int(rng.integers(top_k, 25))
+        cases.append(dict(batch=int(rng.integers(1, 3000)), top_k=top_k, G=G,
+                          K=int(rng.integers(1, 1000)),
+                          N=int(rng.choice([16, 48, 64, 96, 128, 200, 256, 320])),
+                          dtype=str(rng.choice(["bf16", "fp16"])),
+                          row_idx_type=int(rng.integers(0, 2)), seed=100 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(24, 2026),
+                         ids=lambda c: "b{batch}k{top_k}g{G}K{K}N{N}".format(**c))
+def test_random_shapes_owner_equals_ticketed(case):
+    # random sizes cross every slab size, partial last slab, chunk split, K tail,
+    # N tail and both stage kinds; the owner kernel must match the ticketed one
+    # bit for bit, and both the oracle
+    inp = make_case(device="cuda", **case)
+    owner = run(inp, 4)
+    ticketed = run(inp, 0)
+    assert torch.equal(owner.view(torch.int32), ticketed.view(torch.int32))
+    toks = None
+    if inp.batch > 256:
+        toks = np.sort(np.random.default_rng(case["seed"]).choice(inp.batch, 64, replace=False))
+    check(inp, owner, tokens=toks, what=str(case))
