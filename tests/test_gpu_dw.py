@@ -218,3 +218,29 @@ def test_workload_full_size_sampled(name):
     assert_close(out[torch.as_tensor(g), torch.as_tensor(k)], ref, name)
     again = run(inp, x)
     assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        top_k = int(rng.integers(1, 7))
+        cases.append(dict(batch=int(rng.integers(1, 600)), top_k=top_k,
+                          G=int(rng.integers(top_k, 17)), K=int(rng.integers(1, 400)),
+                          N=int(rng.integers(1, 400)),
+                          dtype=str(rng.choice(["bf16", "fp16", "fp32"])),
+                          row_idx_type=int(rng.integers(0, 2)), seed=300 + i,
+                          out_f32=bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(16, 4343),
+                         ids=lambda c: "b{batch}k{top_k}g{G}K{K}N{N}{dtype}".format(**c))
+def test_random_shapes(case):
+    # random sizes, dtypes and index forms: tensor-core and FP32-pipe plans alike
+    c = dict(case)
+    out_f32 = c.pop("out_f32")
+    inp = make_case(device="cuda", **c)
+    x = forward_input(inp)
+    got = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert_close(got, ref_of(inp, x), what=str(case))

@@ -191,3 +191,30 @@ def test_workload_full_size_sampled(name):
     check_pg(pg[torch.as_tensor(rows, device="cuda")], want_pg)
     got_q = qg[torch.as_tensor(toks, device="cuda")]
     check_qg(got_q, want_qg)
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        top_k = int(rng.integers(1, 9))
+        cases.append(dict(batch=int(rng.integers(1, 800)), top_k=top_k,
+                          G=int(rng.integers(top_k, 17)), K=16, N=int(rng.integers(1, 700)),
+                          dtype=str(rng.choice(["bf16", "fp16", "fp32"])),
+                          row_idx_type=int(rng.integers(0, 2)), seed=500 + i,
+                          qg_f32=bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(16, 4444),
+                         ids=lambda c: "b{batch}k{top_k}H{N}{dtype}".format(**c))
+def test_random_shapes(case):
+    # random hidden sizes cross the 16-byte, 4-byte-pair and element paths
+    c = dict(case)
+    qg_f32 = c.pop("qg_f32")
+    inp = make_case(device="cuda", **c)
+    d_out, probs = unpermute_inputs(inp)
+    pg, qg = run(inp, d_out, probs, probs_grad_dtype=torch.float32 if qg_f32 else None)
+    rpg, rqg = ref_of(inp, d_out, probs)
+    check_pg(pg, rpg)
+    check_qg(qg, rqg)
