@@ -349,3 +349,30 @@ def test_workload_full_size_sampled(name):
     assert torch.equal(out.view(torch.int32), again.view(torch.int32))
     # every row was written: no row left at its initial content
     assert torch.isfinite(out).all()
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        top_k = int(rng.integers(1, 9))
+        cases.append(dict(batch=int(rng.integers(1, 2500)), top_k=top_k,
+                          G=int(rng.integers(top_k, 40)), K=int(rng.integers(1, 700)),
+                          N=int(rng.integers(1, 400)),
+                          dtype=str(rng.choice(["bf16", "fp16", "fp32"])),
+                          row_idx_type=int(rng.integers(0, 2)), seed=700 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(20, 4545),
+                         ids=lambda c: "b{batch}k{top_k}g{G}K{K}N{N}{dtype}".format(**c))
+def test_random_shapes(case):
+    # random sizes, dtypes and index forms through the automatic plan (ticketed,
+    # narrow, FP32-pipe or owner kernel), against the oracle, and repeatable
+    inp = make_case(device="cuda", **case)
+    toks = None
+    if inp.batch > 256:
+        toks = np.sort(np.random.default_rng(case["seed"]).choice(inp.batch, 64, replace=False))
+    a = check(inp, tokens=toks, what=str(case))
+    b, _ = run(inp)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
