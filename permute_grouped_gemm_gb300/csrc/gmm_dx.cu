@@ -719,6 +719,9 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
 
+  // Launched with programmatic serialization: the routing (or the owner
+  // kernel) before this one has finished and its memory is visible past here.
+  ptx::griddep_wait();
   // Routing validation failed: the result is defined as zeros. (Both CTAs of
   // a pair see the same status and leave before any cluster operation.)
   const uint32_t st = args.hdr->status;
@@ -801,8 +804,8 @@ cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& a
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   if constexpr (!PAIR) {
-    kern<<<max_ctas, C::kThreads, smem, stream>>>(tdy, tw, args);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(max_ctas)), dim3(C::kThreads), smem, stream,
+                      1, tdy, tw, args);
   } else {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -821,8 +824,8 @@ cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& a
     if (err != cudaSuccess) return err;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     const int want = (max_ctas + 1) / 2;
-    cfg.gridDim = dim3(2 * (clusters < want ? clusters : want), 1, 1);
-    return cudaLaunchKernelEx(&cfg, kern, tdy, tw, args);
+    return launch_pdl(kern, dim3(2 * static_cast<unsigned>(clusters < want ? clusters : want)),
+                      dim3(C::kThreads), smem, stream, 2, tdy, tw, args);
   }
 }
 

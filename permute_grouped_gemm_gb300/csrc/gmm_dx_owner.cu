@@ -431,6 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
+  // Launched with programmatic serialization: the routing step before this
+  // kernel has finished and its memory is visible past here.
+  ptx::griddep_wait();
   // Routing validation failed: the result is defined as zeros. Rows not in
   // increasing position: the ticketed kernel that follows does the work.
   // (Both CTAs of a pair see the same header.)
@@ -534,8 +537,8 @@ cudaError_t launch_owner(int dtype, const OwnerMaps& m, const OwnerArgs& a, int 
   err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, m, a);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want))),
+                    dim3(kThreads), static_cast<size_t>(smem), stream, 2, m, a);
 }
 
 }  // namespace pgg

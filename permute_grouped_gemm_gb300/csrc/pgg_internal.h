@@ -9,6 +9,8 @@
 
 #include "pgg.h"
 
+#include <utility>
+
 namespace pgg {
 
 // Output columns (problem K) per tile. They are the 128 accumulator lanes of
@@ -191,5 +193,35 @@ struct UnpermArgs {
   int32_t row_idx_type;
   int32_t probs_grad_f32;  // 1: probs_grad is fp32; 0: it has the input dtype
 };
+
+// Launches `kern` with the programmatic-serialization attribute: its CTAs may
+// be scheduled while the previous kernel in the stream drains, and every such
+// kernel calls griddepcontrol.wait (ptx::griddep_wait) before it reads
+// anything, so the previous kernel's results are complete and visible by then.
+// cluster_x > 1 adds that cluster dimension.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace pgg

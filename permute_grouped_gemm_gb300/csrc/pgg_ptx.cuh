@@ -69,6 +69,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// (the previous kernel in the stream, when this one was launched with the
+// programmatic-serialization attribute) have completed and their memory is
+// visible. A no-op for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "pgg_internal.h"
+#include "pgg_ptx.cuh"
 
 namespace pgg {
 
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int64_t* __restr
 __global__ void route_scatter_kernel(const int64_t* __restrict__ idx, int64_t M,
                                      int32_t* __restrict__ inv, WsHeader* hdr,
                                      uint4* __restrict__ tickets4, int64_t n_tickets4) {
+  ptx::griddep_wait();  // the header reset of the previous launch
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   bool bad = false;
@@ -173,6 +175,7 @@ __device__ __forceinline__ int64_t row_of_position(const int64_t* idx, const int
 __global__ void route_rank_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
                                   int64_t batch, int64_t top_k, int64_t M, int row_idx_type,
                                   RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+  ptx::griddep_wait();  // inv of the previous launch
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < batch;
@@ -238,6 +241,7 @@ __global__ void route_rank_lanes_kernel(const int64_t* __restrict__ idx,
                                         const int32_t* __restrict__ inv, int64_t batch,
                                         int top_k, int64_t M, int row_idx_type,
                                         RowInfo* __restrict__ rowinfo, WsHeader* hdr) {
+  ptx::griddep_wait();  // inv of the previous launch
   rank_lanes(idx, inv, batch, top_k, M, row_idx_type, rowinfo, hdr);
 }
 
@@ -320,6 +324,7 @@ __global__ void route_owner_kernel(const int64_t* __restrict__ idx, const int32_
                                    int64_t top_k, int row_idx_type, int n_slabs,
                                    int slab_tokens, int32_t* __restrict__ seg, WsHeader* hdr) {
   __shared__ int64_t s_off[kOffSmem];
+  ptx::griddep_wait();  // ranks and status of the previous launch
   if (hdr->status != 0) return;  // the index is not a permutation: nothing to order
   const int64_t* offs = stage_offsets(off, G, s_off);
   __syncthreads();
@@ -337,6 +342,7 @@ __global__ void route_rank_owner_kernel(const int64_t* __restrict__ idx,
                                         int slab_tokens, RowInfo* __restrict__ rowinfo,
                                         int32_t* __restrict__ seg, WsHeader* hdr) {
   __shared__ int64_t s_off[kOffSmem];
+  ptx::griddep_wait();  // inv, off and the status of the previous launches
   const uint32_t st = hdr->status;  // index range or group sum already wrong: no order
   const int64_t* offs = stage_offsets(off, G, s_off);
   __syncthreads();
@@ -350,6 +356,7 @@ __global__ void route_rank_owner_kernel(const int64_t* __restrict__ idx,
 // Every original position must have an expanded row (see row_of_position).
 __global__ void perm_check_kernel(const int64_t* __restrict__ idx, const int32_t* __restrict__ inv,
                                   int64_t M, int row_idx_type, WsHeader* hdr) {
+  ptx::griddep_wait();  // inv of the previous launch
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
   for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < M; p += stride)
@@ -369,9 +376,12 @@ cudaError_t launch_index_prep(const int64_t* idx, int64_t M, int row_idx_type, i
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, M, inv, hdr, nullptr, 0);
-  perm_check_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, inv, M, row_idx_type, hdr);
-  return cudaGetLastError();
+  cudaError_t err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                               0, stream, 1, idx, M, inv, hdr, static_cast<uint4*>(nullptr),
+                               static_cast<int64_t>(0));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(perm_check_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                    1, idx, static_cast<const int32_t*>(inv), M, row_idx_type, hdr);
 }
 
 cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_t* group_list,
@@ -393,9 +403,15 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  route_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, plan.M, inv, hdr,
-                                                                     tickets4,
-                                                                     plan.layout.n_tickets / 4);
+  // the later launches may be scheduled while their predecessor drains; each
+  // waits for it (griddepcontrol.wait) before reading anything
+  cudaError_t err = launch_pdl(route_scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                               0, stream, 1, idx, plan.M, inv, hdr, tickets4,
+                               plan.layout.n_tickets / 4);
+  if (err != cudaSuccess) return err;
+  const int32_t* cinv = inv;
+  const int64_t* coff = off;
+  int32_t* seg = reinterpret_cast<int32_t*>(ws + L.seg);
   bool owner_done = false;
   if (plan.topK <= 32) {
     const int64_t per_block = 8 * (32 / plan.topK);  // tokens per 256-thread block
@@ -408,30 +424,33 @@ cudaError_t launch_route_prep(const Plan& plan, const int64_t* idx, const int64_
     if (rblocks > cap) rblocks = cap;
     if (rblocks < 1) rblocks = 1;
     if (plan.n_slabs > 0) {
-      route_rank_owner_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
-          idx, inv, off, plan.batch, static_cast<int>(plan.topK), plan.M, plan.G,
-          plan.row_idx_type, plan.n_slabs, plan.slab_tokens, rowinfo,
-          reinterpret_cast<int32_t*>(ws + L.seg), hdr);
+      err = launch_pdl(route_rank_owner_kernel, dim3(static_cast<unsigned>(rblocks)), dim3(256), 0,
+                       stream, 1, idx, cinv, coff, plan.batch, static_cast<int>(plan.topK), plan.M,
+                       plan.G, plan.row_idx_type, plan.n_slabs, plan.slab_tokens, rowinfo, seg,
+                       hdr);
       owner_done = true;
     } else {
-      route_rank_lanes_kernel<<<static_cast<int>(rblocks), 256, 0, stream>>>(
-          idx, inv, plan.batch, static_cast<int>(plan.topK), plan.M, plan.row_idx_type, rowinfo,
-          hdr);
+      err = launch_pdl(route_rank_lanes_kernel, dim3(static_cast<unsigned>(rblocks)), dim3(256), 0,
+                       stream, 1, idx, cinv, plan.batch, static_cast<int>(plan.topK), plan.M,
+                       plan.row_idx_type, rowinfo, hdr);
     }
+    if (err != cudaSuccess) return err;
   } else {
     int64_t rblocks = (plan.batch + 127) / 128;
     if (rblocks > cap) rblocks = cap;
     if (rblocks < 1) rblocks = 1;
-    route_rank_kernel<<<static_cast<int>(rblocks), 128, 0, stream>>>(
-        idx, inv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+    err = launch_pdl(route_rank_kernel, dim3(static_cast<unsigned>(rblocks)), dim3(128), 0, stream,
+                     1, idx, cinv, plan.batch, plan.topK, plan.M, plan.row_idx_type, rowinfo, hdr);
+    if (err != cudaSuccess) return err;
   }
   if (plan.n_slabs > 0 && !owner_done) {
     int64_t oblocks = (plan.M + 255) / 256;
     if (oblocks > cap) oblocks = cap;
     if (oblocks < 1) oblocks = 1;
-    route_owner_kernel<<<static_cast<int>(oblocks), 256, 0, stream>>>(
-        idx, inv, off, plan.M, plan.G, plan.topK, plan.row_idx_type, plan.n_slabs,
-        plan.slab_tokens, reinterpret_cast<int32_t*>(ws + L.seg), hdr);
+    err = launch_pdl(route_owner_kernel, dim3(static_cast<unsigned>(oblocks)), dim3(256), 0, stream,
+                     1, idx, cinv, coff, plan.M, plan.G, plan.topK, plan.row_idx_type,
+                     plan.n_slabs, plan.slab_tokens, seg, hdr);
+    if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }

@@ -20,6 +20,7 @@
 #include <cstdint>
 
 #include "pgg_internal.h"
+#include "pgg_ptx.cuh"
 
 namespace pgg {
 namespace {
@@ -107,6 +108,7 @@ __device__ __forceinline__ uint4 pack16(const float* f) {
 template <int DT, bool PROBS, bool VEC, bool PAIRS>
 __global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermArgs a) {
   using E = Elem<DT>;
+  ptx::griddep_wait();  // the index validation before this launch
   const uint32_t st = a.hdr->status;
   if (st == kStIndex || st == kStGroupSum || st == kStNotPerm) {
     const int64_t n = a.M * a.H;
@@ -230,12 +232,13 @@ __global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermA
 
 template <int DT, bool PROBS>
 void launch_p(const UnpermArgs& a, bool vec, bool pairs, int grid, cudaStream_t s) {
+  const dim3 g(static_cast<unsigned>(grid)), b(kUThreads);
   if (vec)
-    unpermute_grad_kernel<DT, PROBS, true, false><<<grid, kUThreads, 0, s>>>(a);
+    launch_pdl(unpermute_grad_kernel<DT, PROBS, true, false>, g, b, 0, s, 1, a);
   else if (pairs && DT != PGG_F32)
-    unpermute_grad_kernel<DT, PROBS, false, DT != PGG_F32><<<grid, kUThreads, 0, s>>>(a);
+    launch_pdl(unpermute_grad_kernel<DT, PROBS, false, DT != PGG_F32>, g, b, 0, s, 1, a);
   else
-    unpermute_grad_kernel<DT, PROBS, false, false><<<grid, kUThreads, 0, s>>>(a);
+    launch_pdl(unpermute_grad_kernel<DT, PROBS, false, false>, g, b, 0, s, 1, a);
 }
 
 template <int DT>
