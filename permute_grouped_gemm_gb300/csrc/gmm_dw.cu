@@ -463,6 +463,7 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_dw_kernel(const __grid_constant__ CUtensorMap tm_dy,
                   const __grid_constant__ CUtensorMap tm_out, const DwArgs a) {
+  ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -578,8 +579,8 @@ cudaError_t launch_dw(int dtype, const CUtensorMap& tm_dy, const CUtensorMap& tm
   err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_dy, tm_out, a);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want))),
+                    dim3(kThreads), static_cast<size_t>(kSmemBytes), stream, 2, tm_dy, tm_out, a);
 }
 
 }  // namespace pgg

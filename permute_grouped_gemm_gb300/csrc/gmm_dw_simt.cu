@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "pgg_internal.h"
+#include "pgg_ptx.cuh"
 
 namespace pgg {
 namespace {
@@ -157,6 +158,7 @@ __device__ __forceinline__ void store4(void* out, bool f32, int64_t off, int64_t
 
 template <int DT>
 __global__ void __launch_bounds__(kWThreads, 3) gmm_dw_simt_kernel(const DwArgs a, int vec) {
+  ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ __align__(16) uint8_t dw_simt_smem[];
   WSmem& sm = *reinterpret_cast<WSmem*>(dw_simt_smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -262,7 +264,9 @@ cudaError_t launch_dw_simt(int dtype, const DwArgs& a, int vec, int num_sms, cud
   int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
   if (total < grid) grid = total;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kWThreads, smem, stream>>>(a, vec);
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kWThreads),
+                   static_cast<size_t>(smem), stream, 1, a, vec);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

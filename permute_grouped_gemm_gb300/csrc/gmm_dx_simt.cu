@@ -150,6 +150,7 @@ struct SimtSmem {
 
 template <int DT>
 __global__ void __launch_bounds__(kSThreads, kSMinCtas) gmm_dx_simt_kernel(const SimtArgs a) {
+  ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ __align__(16) uint8_t simt_smem_raw[];
   SimtSmem& sm = *reinterpret_cast<SimtSmem*>(simt_smem_raw);
   float (&sA)[2][kSNc * kSAStride] = sm.a;
@@ -317,7 +318,9 @@ cudaError_t launch_simt(int dtype, const SimtArgs& a, int64_t max_tiles, int num
   int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kSThreads, smem, stream>>>(a);
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kSThreads),
+                   static_cast<size_t>(smem), stream, 1, a);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -385,6 +385,7 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_fwd_kernel(const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_y, const FwdArgs a) {
+  ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -494,8 +495,8 @@ cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const CUtensorMap& tm
   err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_y, a);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want))),
+                    dim3(kThreads), static_cast<size_t>(kSmemBytes), stream, 2, tm_w, tm_y, a);
 }
 
 }  // namespace pgg

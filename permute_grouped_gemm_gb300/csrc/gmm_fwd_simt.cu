@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "pgg_internal.h"
+#include "pgg_ptx.cuh"
 
 namespace pgg {
 namespace {
@@ -140,6 +141,7 @@ __device__ __forceinline__ void store4(void* out, bool f32, int64_t off, int64_t
 
 template <int DT>
 __global__ void __launch_bounds__(kThr, 3) gmm_fwd_simt_kernel(const FwdArgs a, int vec) {
+  ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ __align__(16) uint8_t fwd_simt_smem[];
   Smem& sm = *reinterpret_cast<Smem*>(fwd_simt_smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -251,7 +253,9 @@ cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_ti
   int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), kThr, smem, stream>>>(a, vec);
+  err = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThr),
+                   static_cast<size_t>(smem), stream, 1, a, vec);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
