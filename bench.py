@@ -86,6 +86,17 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of ``values`` (floats) over all ranks of ``dist``
+    (the slowest replica's times); the values themselves without one."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def kernel_hash(kernel: str = "gmm_dx_kernel") -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
@@ -624,10 +635,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
     mean_step = statistics.mean(step_ms)
     mean_gemm = statistics.mean(gemm_ms)
-    if dist:
-        t = torch.tensor([mean_step, mean_gemm], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_step, mean_gemm = float(t[0]), float(t[1])
+    mean_step, mean_gemm = max_over_ranks([mean_step, mean_gemm], dist, dev)
 
     flops, nbytes = op.algorithmic()
     if getattr(op, "unit", "TFLOP/s") == "GB/s":
@@ -736,10 +744,7 @@ def measure_e2e(op, pgg, w, dev, stream, flops, nbytes, world, dist):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = max_over_ranks([ms], dist, dev)[0]
     if not torch.equal(h_out, d_out.cpu()):
         raise RuntimeError("e2e readback mismatch")
     if getattr(op, "unit", "TFLOP/s") == "GB/s":
