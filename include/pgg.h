@@ -35,11 +35,12 @@
  *     attributes and the test hooks at the end of this file.
  *   - Calls only enqueue work on `stream` (NULL = legacy default stream) and
  *     never synchronise. Inputs are not modified.
- *   - Kernels after the first of a call are launched with programmatic
- *     stream serialization: their CTAs may be scheduled while the previous
- *     kernel in the stream (the library's own, or the caller's) drains, and
- *     each waits for that kernel's completion before it reads any memory, so
- *     stream order is kept exactly.
+ *   - Every kernel except the one that resets the workspace header (the first
+ *     of a routing or index-validation stage) is launched with programmatic
+ *     stream serialization: its CTAs may be scheduled while the previous
+ *     kernel in the stream (the library's own, or the caller's) drains, and it
+ *     waits for that kernel's completion before it reads any memory, so stream
+ *     order is kept exactly.
  *   - Host-detected errors are returned synchronously and nothing is enqueued.
  *   - Device-detected errors (bad index, groupList sum, not a permutation,
  *     a wait that ran out) are written to the status word, the first uint32 of
