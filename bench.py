@@ -9,15 +9,25 @@ steps, outside the per-step CUDA events: a 256 MiB write, then a 256 MiB read
 of another buffer, so that the write's dirty lines are written back before
 the step starts rather than during it.
 
-Metric: fused d_x TFLOP/s = 2*M*N*K / step time, with the roofline fraction
-of the grouped-GEMM kernel and the workspace bytes.
+The default workload is large-bf16 (batch 13500, topK 8, G 60, K 7168,
+N 2048: the scale of "MoeInitRoutingGroupedMatmulGrad design", section 1.2).
+Before the warm-up, the same step runs untimed for --burn-in seconds so that
+the GPU is at its steady clock; SM clocks and clock-event reasons are sampled
+(NVML, read-only) during the burn-in and the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--op dx|dw]
+Metric: fused d_x TFLOP/s = 2*M*N*K / step time, with the roofline fraction
+of the grouped-GEMM kernel (against the measured burst bf16 peak) and the
+workspace bytes. Also reported: the median step, the same steps with L2
+left warm, and the torch allocator's peak over the library calls (0: the
+library allocates nothing).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--op dx|dw|fwd|unperm]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
 
 --op dw times the companion weight-gradient kernel (x^T d_y per expert with
 the x rows gathered by the routing) on the same workload instead; --op fwd
-the forward y = expanded_x W per expert it differentiates.
+the forward y = expanded_x W per expert it differentiates; --op unperm the
+probs-weighted unpermute backward.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload on its own GPU (the path needs no exchange); value sums the work of
@@ -41,7 +51,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "uniform-bf16"
+DEFAULT_WORKLOAD = "large-bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace bytes"
 _COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh"]
@@ -76,6 +86,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--burn-in", type=float, default=3.0,
+                    help="seconds of untimed steps before the warm-up (0: none)")
     return ap.parse_args()
 
 
@@ -137,61 +149,150 @@ def recorded_traffic(kernel: str, workload: str):
         return None
 
 
+# Clock-event reason bits of NVML (nvmlClocksEventReason*) that a run reports.
+_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, the active
+    clock-event reasons, board power) for the GPU behind a CUDA device index.
+    Changes no setting of the GPU."""
+    CLOCK_SM = 1
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:  # noqa: BLE001 - fall back to the index
+            uuid = None
+        rc = 1
+        if uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index),
+                                                   ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if self.reasons_fn is None:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        v = ctypes.c_uint()
+        self.max_mhz = (float(v.value) if lib.nvmlDeviceGetMaxClockInfo(
+            self.h, self.CLOCK_SM, ctypes.byref(v)) == 0 else None)
+
+    def sample(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn(self.h, ct.byref(rs)) != 0:
+            rs.value = 0
+        watts = mw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(
+            self.h, ct.byref(mw)) == 0 else None
+        return float(mhz.value), self.max_mhz, int(rs.value), watts
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event reasons sampled from a thread, each sample
+    stamped with the host clock, so that the samples inside any window (the
+    timed region, the burn-in) can be summarised. NVML through ctypes every
+    millisecond; nvidia-smi every 50 ms where NVML cannot be loaded."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.001):
         self.index = index
+        self.period = period_s
+        self.samples = []  # (host time, sm MHz, max MHz, reason names, power W)
         self.proc = None
-        self.lines = []
+        self.nvml = None
+        self.source = "none"
+        self._stop = threading.Event()
+        self.t = None
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.source = "nvml"
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
         return self
 
+    def _poll(self):
+        while not self._stop.is_set():
+            s = self.nvml.sample()
+            if s is not None:
+                mhz, mx, bits, w = s
+                names = tuple(n for b, n in _REASON_BITS.items() if bits & b)
+                self.samples.append((time.perf_counter(), mhz, mx, names, w))
+            self._stop.wait(self.period)
+
     def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            try:
+                w = float(parts[3])
+            except ValueError:
+                w = None
+            active = tuple(n for n, v in zip(names, parts[5:9]) if v.lower() == "active")
+            self.samples.append((time.perf_counter(), mhz, mx, active, w))
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.t is not None:
             self.t.join(timeout=2)
 
-    def summary(self):
-        sms, maxes, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sms.append(float(parts[1]))
-                maxes.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, maximum clock, the reasons seen and the sample count
+        for the samples taken between host times t0 and t1 (all if None)."""
+        sel = [s for s in self.samples
+               if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for s in sel for n in s[3]})
+        watts = [s[4] for s in sel if s[4] is not None]
+        maxes = [s[2] for s in sel if s[2] is not None]
+        return {"sm_mhz": statistics.median(s[1] for s in sel),
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": reasons, "samples": len(sel),
+                "power_w_max": max(watts) if watts else None, "source": self.source}
 
 
 class DxOp:
@@ -600,23 +701,44 @@ def run_ours(args):
         if rc:
             raise pgg.PggError(rc, "grouped_gemm")
 
-    torch.cuda.reset_peak_memory_stats(dev)
-    base_alloc = torch.cuda.memory_allocated(dev)
-    for _ in range(args.warmup):
-        flush_l2()
+    def check_status():
+        if pgg.status(ws) != 0:
+            raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        # Untimed burn-in of the same step, so that the GPU (and any outside
+        # clock sampler) is under load and at its steady clock before timing.
+        t0 = time.perf_counter()
+        burn_steps = 0
+        while time.perf_counter() - t0 < args.burn_in:
+            for _ in range(16):
+                flush_l2()
+                route_prep()
+                gemm()
+            burn_steps += 16
+            torch.cuda.synchronize()
+        burn_window = (t0, time.perf_counter())
+        for _ in range(args.warmup):
+            flush_l2()
+            route_prep()
+            gemm()
+        torch.cuda.synchronize()
+        check_status()
+
+        # The torch allocator's peak over the library calls alone (the flush's
+        # reduction allocates scratch of its own, outside them).
+        base_alloc = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
         route_prep()
         gemm()
-    torch.cuda.synchronize()
-    if pgg.status(ws) != 0:
-        raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
-    alloc_delta = torch.cuda.max_memory_allocated(dev) - base_alloc
+        torch.cuda.synchronize()
+        alloc_delta = torch.cuda.max_memory_allocated(dev) - base_alloc
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        t_wall = time.perf_counter()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         for s in range(args.steps):
             flush_l2()
             ev[s][0].record(stream)
@@ -625,32 +747,45 @@ def run_ours(args):
             gemm()
             ev[s][2].record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
-    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    gemm_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    prep_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-    if pgg.status(ws) != 0:
-        raise RuntimeError(f"device status {pgg.STATUS[pgg.status(ws)]}")
+        timed_window = (t0, time.perf_counter())
+        if dist:
+            dist.barrier()
+        step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
+        gemm_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+        prep_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+        check_status()
+
+        # The same steps with L2 left warm (no flush between them).
+        wev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        torch.cuda.synchronize()
+        wev[0].record(stream)
+        for s in range(args.steps):
+            route_prep()
+            gemm()
+            wev[s + 1].record(stream)
+        torch.cuda.synchronize()
+        warm_ms = [wev[s].elapsed_time(wev[s + 1]) for s in range(args.steps)]
+        check_status()
     mean_step = statistics.mean(step_ms)
     mean_gemm = statistics.mean(gemm_ms)
-    mean_step, mean_gemm = max_over_ranks([mean_step, mean_gemm], dist, dev)
+    med_step = statistics.median(step_ms)
+    med_warm = statistics.median(warm_ms)
+    mean_step, mean_gemm, med_step, med_warm = max_over_ranks(
+        [mean_step, mean_gemm, med_step, med_warm], dist, dev)
 
     flops, nbytes = op.algorithmic()
-    if getattr(op, "unit", "TFLOP/s") == "GB/s":
-        value = world * nbytes / (mean_step * 1e-3) / 1e9
-    else:
-        value = world * flops / (mean_step * 1e-3) / 1e12
     value_unit = getattr(op, "unit", "TFLOP/s")
+    work = nbytes / 1e9 if value_unit == "GB/s" else flops / 1e12  # per step and GPU
+    value = world * work / (mean_step * 1e-3)
 
     peaks, peak_src = load_peaks()
-    clocks = clk.summary()
-    # A kernel that ran under the power cap during the timed loop is held to
-    # the sustained (power-capped) tensor peak, otherwise to the burst peak.
-    capped = "sw_power_cap" in clocks.get("reasons", [])
-    tc_key = "bf16_tflops_sustained" if capped and "bf16_tflops_sustained" in peaks else "bf16_tflops"
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    clocks = clk.summary(*timed_window)
+    burn_clocks = clk.summary(*burn_window)
+    # The fraction is taken against the burst (short-run) tensor peak: the
+    # timed kernel runs for milliseconds at a time. A power cap seen by the
+    # clock samples is reported beside it, not folded into the peak.
+    tc_key = "bf16_tflops"
+    t_tc = flops / (peaks[tc_key] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     simt = plan["variant"] == SIMT_VARIANT
     kernel = op.kernel
@@ -672,7 +807,15 @@ def run_ours(args):
         bound, achieved = "hbm", nbytes / (mean_gemm * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
         peak_src = f"{peak_src} hbm_gbs"
-    traffic = recorded_traffic(kernel, w.name)
+    src_note = ("MEASURED_PEAKS.json" if peak_src.startswith("measured")
+                else "profiling recipe fallback")
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": recorded_traffic(kernel, w.name),
+                "peak_source": peak_src if simt else f"{peak_src} ({src_note})",
+                "kernel": kernel, "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+    if clocks.get("sm_mhz"):
+        # clock-independent size of the kernel: thousands of SM cycles per launch
+        roofline["kcycles_per_launch_at_median_clock"] = mean_gemm * clocks["sm_mhz"]
 
     e2e = None
     if not args.no_e2e:
@@ -689,14 +832,17 @@ def run_ours(args):
         "workspace_bytes": ws_bytes,
         "torch_alloc_delta_bytes": int(alloc_delta),
         "phases_ms": {"route_prep": statistics.mean(prep_ms), "grouped_gemm": mean_gemm},
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": peak_src if simt else f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src.startswith('measured') else 'profiling recipe fallback'})",
-                     "kernel": kernel, "algorithmic_flops": flops,
-                     "algorithmic_bytes": nbytes},
+        "median_ms_per_step": med_step,
+        "median_value": world * work / (med_step * 1e-3),
+        "warm_l2": {"ms_per_step_median": med_warm,
+                    "value": world * work / (med_warm * 1e-3),
+                    "l2": "not flushed: the same steps back to back"},
+        "roofline": roofline,
         "clocks": clocks,
+        "burn_in": {"seconds": burn_window[1] - burn_window[0], "steps": burn_steps,
+                    "clocks": burn_clocks},
         "gpu_launches": getattr(op, "launches", 4) * args.steps,
-        "wall_s_timed_region": t_wall,
+        "wall_s_timed_region": timed_window[1] - timed_window[0],
     }
     if e2e:
         line["e2e"] = e2e

@@ -87,7 +87,10 @@ typedef enum {
   PGG_ERR_INDEX = 16,    /* an expandedRowIdx entry outside [0, M) */
   PGG_ERR_GROUPSUM = 17, /* a negative groupList entry, or sum(groupList) != M */
   PGG_ERR_NOT_PERM = 18, /* expandedRowIdx is not a permutation of [0, M) */
-  PGG_ERR_TIMEOUT = 19   /* a bounded wait inside a kernel ran out (no hang; result invalid) */
+  PGG_ERR_TIMEOUT = 19,  /* a bounded wait inside a kernel ran out (no hang; result invalid) */
+  PGG_ERR_CHECK = 20     /* checked build only (libpgg_checks.so, compiled with -DPGG_CHECKS):
+                            a device bounds check on an index read from the routing tables
+                            failed; the access was kept in bounds, the result is invalid */
 } pgg_status;
 
 /*
@@ -223,9 +226,11 @@ void pgg_debug_set_band_k_blocks(int k_blocks);
  * 8 MiB (8388608 bytes; e.g. M = 108000, K = 7168 needs 4.3 MB), and
  * otherwise what pgg_dx_execute returns.
  *
- * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture on the device. Every call on a device shares the one
+ * Each call looks up the scratch array's device address (cudaGetSymbolAddress)
+ * on the current device, so the address stays valid after cudaDeviceReset;
+ * only a call made while `stream` is being captured reuses the address that
+ * the previous call on the device looked up, so make the first call on a
+ * device before any stream capture on it. Every call on a device shares the one
  * array, and each call re-initialises what it needs, so leftover contents from
  * the previous call do no harm -- but two calls whose work overlaps on the GPU
  * (for example on two streams without ordering between them) race on the

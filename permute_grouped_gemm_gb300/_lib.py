@@ -16,7 +16,7 @@ PGG_F32, PGG_F16, PGG_BF16 = 0, 1, 2
 STATUS = {
     0: "PGG_OK", 1: "PGG_ERR_NULL", 2: "PGG_ERR_SHAPE", 3: "PGG_ERR_ATTR", 4: "PGG_ERR_DTYPE",
     5: "PGG_ERR_WORKSPACE", 6: "PGG_ERR_CUDA", 7: "PGG_ERR_ALIGN", 16: "PGG_ERR_INDEX",
-    17: "PGG_ERR_GROUPSUM", 18: "PGG_ERR_NOT_PERM", 19: "PGG_ERR_TIMEOUT",
+    17: "PGG_ERR_GROUPSUM", 18: "PGG_ERR_NOT_PERM", 19: "PGG_ERR_TIMEOUT", 20: "PGG_ERR_CHECK",
 }
 CODES = {v: k for k, v in STATUS.items()}
 

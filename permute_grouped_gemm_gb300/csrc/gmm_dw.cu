@@ -219,7 +219,11 @@ __device__ __forceinline__ void stage_tokens(const StageIt& s, const DwArgs& a, 
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int64_t r = s.r + lane + 32 * h;
-    tok[h] = (s.valid && r < s.x.m) ? a.rowinfo[s.x.row0 + r].token : -1;
+    tok[h] = (s.valid && r < s.x.m)
+                 ? static_cast<int32_t>(check_index(
+                       a.hdr, a.rowinfo[check_index(a.hdr, s.x.row0 + r, a.M, 60)].token,
+                       a.batch, 61))
+                 : -1;
   }
 }
 

@@ -82,7 +82,9 @@ __device__ __forceinline__ void wstage_load(const DwArgs& a, const WTile& x, int
     const int64_t r = r0 + it * 4 + warp;
     const bool row_ok = r < x.m;
     int64_t tok = 0;
-    if (row_ok) tok = a.rowinfo[x.row0 + r].token;
+    if (row_ok)
+      tok = check_index(a.hdr, a.rowinfo[check_index(a.hdr, x.row0 + r, a.M, 62)].token,
+                        a.batch, 63);
 #pragma unroll
     for (int h = 0; h < kWK / 32; ++h) {
       const int64_t k = x.k0 + 32 * h + lane;

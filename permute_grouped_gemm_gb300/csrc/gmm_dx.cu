@@ -217,7 +217,13 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
     if (t >= total) return make_int4(-1, 0, 0, 0);
     uint32_t rb, ku;
     decode_tile(t, n_rb, units, band, &rb, &ku);
-    const int4 r = args.rblist[rb];
+    int4 r = args.rblist[check_index(args.hdr, rb, args.max_row_blocks, 40)];
+    // checked build: a row block outside the experts or rows becomes an empty one
+    if (!check_ok(args.hdr,
+                  r.x >= 0 && r.x < args.G && r.y >= 0 && r.z >= 0 && r.z <= ROWS &&
+                      static_cast<int64_t>(r.y) + r.z <= args.M,
+                  41))
+      r = make_int4(0, 0, 0, 0);
     return make_int4(r.x, r.y, r.z, static_cast<int>(ku));
   };
   // The next tile is claimed and its row block read while the current one
@@ -635,7 +641,11 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     const int R = e.z, row0 = e.y;
     const uint32_t kb = PAIR ? 2u * static_cast<uint32_t>(e.w) + rank : static_cast<uint32_t>(e.w);
     const bool kb_ok = kb < kbs;  // a pair's odd half may lie beyond K
-    for (int r = et; r < R; r += 128) es->meta[r] = args.rowinfo[row0 + r];
+    for (int r = et; r < R; r += 128) {
+      RowInfo m = args.rowinfo[check_index(args.hdr, row0 + r, args.M, 42)];
+      m.token = static_cast<int32_t>(check_index(args.hdr, m.token, args.batch, 43));
+      es->meta[r] = m;
+    }
     if (et < C::kWords) {
       const int nr = kb_ok ? R - et * 32 : 0;
       es->pend[et] = nr >= 32 ? 0xFFFFFFFFu : (nr <= 0 ? 0u : ((1u << nr) - 1u));
@@ -673,6 +683,7 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
         }
         continue;
       }
+      t_wait0 = 0;  // progress: the limit counts time without any
       // 2. write the ready rows
       if (args.vec_rows)
         write_rows_vec(es, args, t_lane, R, kb, quarter);

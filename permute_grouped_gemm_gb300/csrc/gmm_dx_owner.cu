@@ -122,6 +122,8 @@ struct ChunkIt {
       if (g >= a->G) return;
       r0 = nlo;
       r_end = nhi;
+      // checked build: bounds outside the expanded rows make the range empty
+      if (!check_ok(a->hdr, 0 <= r0 && r0 <= r_end && r_end <= a->M, 30)) r0 = r_end = 0;
       load_next();
       if (r0 < r_end) return;
     }
@@ -316,7 +318,7 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
         int f = kRowPad;
         const int r = 32 * b + lane;
         if (r < R) {
-          const RowInfo ri = a.rowinfo[c.r0 + r];
+          const RowInfo ri = a.rowinfo[check_index(a.hdr, c.r0 + r, a.M, 31)];
           const int64_t t = static_cast<int64_t>(ri.token) - tok0;
           if (t >= 0 && t < T) f = static_cast<int>(t) | (ri.rank == 0 ? kRowFirst : 0);
         }

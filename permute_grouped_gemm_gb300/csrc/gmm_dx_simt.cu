@@ -185,7 +185,13 @@ __global__ void __launch_bounds__(kSThreads, kSMinCtas) gmm_dx_simt_kernel(const
     __syncthreads();  // every thread has read s_tile before thread 0 may claim again
     if (t >= total) break;
     const uint32_t rb = t / kbs, kb = t - rb * kbs;
-    const int4 e = a.rblist[rb];
+    int4 e = a.rblist[check_index(hdr, rb, a.max_row_blocks, 50)];
+    // checked build: a row block outside the experts or rows becomes an empty one
+    if (!check_ok(hdr,
+                  e.x >= 0 && e.x < a.G && e.y >= 0 && e.z >= 0 &&
+                      static_cast<int64_t>(e.y) + e.z <= a.M,
+                  51))
+      e = make_int4(0, 0, 0, 0);
     const int64_t g = e.x;
     const int64_t k0 = static_cast<int64_t>(kb) * kKBlock;
 
@@ -238,7 +244,10 @@ __global__ void __launch_bounds__(kSThreads, kSMinCtas) gmm_dx_simt_kernel(const
       ri.token = 0;
       ri.rank = 0;
       const bool tracked = lane < 16 && my_row < R;
-      if (tracked) ri = a.rowinfo[row0 + my_row];
+      if (tracked) {
+        ri = a.rowinfo[check_index(hdr, row0 + my_row, a.M, 52)];
+        ri.token = static_cast<int32_t>(check_index(hdr, ri.token, a.batch, 53));
+      }
       uint32_t pend = __ballot_sync(0xFFFFFFFFu, tracked);
       uint64_t t_wait0 = 0;
       const int half = lane >> 4;
@@ -263,6 +272,7 @@ __global__ void __launch_bounds__(kSThreads, kSMinCtas) gmm_dx_simt_kernel(const
           }
           continue;
         }
+        t_wait0 = 0;  // progress: the limit counts time without any
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int j = 8 * half + i;  // row of the pass this lane writes now

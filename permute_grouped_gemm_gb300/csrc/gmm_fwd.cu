@@ -86,7 +86,13 @@ struct FTile {
 
 __device__ __forceinline__ FTile ftile_of(uint32_t t, const FwdArgs& a, uint32_t rank) {
   const uint32_t rb = t / static_cast<uint32_t>(a.n_blocks);
-  const int4 e = a.rblist[rb];
+  int4 e = a.rblist[check_index(a.hdr, rb, a.max_row_blocks, 70)];
+  // checked build: a row block outside the experts or rows becomes an empty one
+  if (!check_ok(a.hdr,
+                e.x >= 0 && e.x < a.G && e.y >= 0 && e.z >= 0 &&
+                    static_cast<int64_t>(e.y) + e.z <= a.M,
+                71))
+    e = make_int4(0, 0, 0, 0);
   FTile x;
   x.g = e.x;
   x.row0 = static_cast<int64_t>(e.y) + kFM * rank;
@@ -154,7 +160,10 @@ __device__ __forceinline__ void tile_tokens(const FTile& x, const FwdArgs& a, in
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     const int r = lane + 32 * h;
-    tok[h] = r < x.rows ? a.rowinfo[x.row0 + r].token : -1;
+    tok[h] = r < x.rows ? static_cast<int32_t>(check_index(
+                              a.hdr, a.rowinfo[check_index(a.hdr, x.row0 + r, a.M, 72)].token,
+                              a.batch, 73))
+                        : -1;
   }
 }
 

@@ -165,7 +165,13 @@ __global__ void __launch_bounds__(kThr, 3) gmm_fwd_simt_kernel(const FwdArgs a, 
   const int l_r = lane >> 3;
   for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
     const uint32_t rb = t / static_cast<uint32_t>(a.n_blocks);
-    const int4 e = a.rblist[rb];
+    int4 e = a.rblist[check_index(a.hdr, rb, a.max_row_blocks, 74)];
+    // checked build: a row block outside the experts or rows becomes an empty one
+    if (!check_ok(a.hdr,
+                  e.x >= 0 && e.x < a.G && e.y >= 0 && e.z >= 0 &&
+                      static_cast<int64_t>(e.y) + e.z <= a.M,
+                  75))
+      e = make_int4(0, 0, 0, 0);
     const int64_t g = e.x;
     const int64_t n0 = static_cast<int64_t>(t - rb * static_cast<uint32_t>(a.n_blocks)) * kCols;
     for (int p0 = 0; p0 < e.z; p0 += kRows) {
@@ -175,7 +181,10 @@ __global__ void __launch_bounds__(kThr, 3) gmm_fwd_simt_kernel(const FwdArgs a, 
 #pragma unroll
       for (int it = 0; it < kRows / 16; ++it) {
         const int r = it * 16 + warp * 4 + l_r;
-        tok[it] = r < R ? a.rowinfo[row0 + r].token : -1;
+        tok[it] = r < R ? static_cast<int32_t>(check_index(
+                              a.hdr, a.rowinfo[check_index(a.hdr, row0 + r, a.M, 76)].token,
+                              a.batch, 77))
+                        : -1;
       }
       float acc[8][8];
 #pragma unroll

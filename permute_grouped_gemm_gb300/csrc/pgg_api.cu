@@ -344,6 +344,9 @@ int run_simt(const Plan& plan, const void* gradY, const void* weight, void* ws, 
   a.N = plan.N;
   a.K = plan.K;
   a.batch = plan.batch;
+  a.M = plan.M;
+  a.G = plan.G;
+  a.max_row_blocks = plan.max_row_blocks;
   a.k_blocks = plan.k_blocks;
   a.ticket_bias = g_ticket_bias.load();
   a.vec_out = (plan.K % 4 == 0 && aligned(out, 16)) ? 1 : 0;
@@ -374,6 +377,9 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   a.out = out;
   a.K = plan.K;
   a.batch = plan.batch;
+  a.M = plan.M;
+  a.G = plan.G;
+  a.max_row_blocks = plan.max_row_blocks;
   a.k_blocks = plan.k_blocks;
   a.k_units = plan.k_units;
   a.band_units = plan.band_units;
@@ -589,6 +595,9 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
   a.M = plan.M;
   a.N = plan.N;
   a.K = plan.K;
+  a.G = plan.G;
+  a.batch = plan.batch;
+  a.max_row_blocks = plan.max_row_blocks;
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   if (fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
@@ -1008,6 +1017,7 @@ const char* pgg_status_string(int status) {
     case PGG_ERR_GROUPSUM: return "groupList negative or sum != M";
     case PGG_ERR_NOT_PERM: return "expandedRowIdx is not a permutation";
     case PGG_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case PGG_ERR_CHECK: return "a device bounds check failed (checked build)";
     default: return "unknown status";
   }
 }
@@ -1048,18 +1058,24 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {};
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (the first call on a device does this; it should come before any
-// stream capture on that device).
-int static_scratch_address(void** out) {
+// Device address of g_static_scratch on the current device. A call made while
+// `stream` is not being captured looks it up afresh (so an address made stale
+// by cudaDeviceReset or a new primary context is never used) and remembers it
+// per device; a call made during a stream capture uses the remembered address,
+// so the first call on a device must come before any capture on it.
+int static_scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PGG_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool capturing =
+      cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!capturing) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PGG_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
+  if (!g_scratch_ptr[dev]) return PGG_ERR_CUDA;
   *out = g_scratch_ptr[dev];
   return PGG_OK;
 }
@@ -1077,7 +1093,7 @@ extern "C" int pgg_dx_execute_static_scratch(const void* gradY, const void* weig
   if (rc != PGG_OK) return rc;
   if (need > kStaticScratchBytes) return PGG_ERR_WORKSPACE;
   void* scratch = nullptr;
-  rc = static_scratch_address(&scratch);
+  rc = static_scratch_address(reinterpret_cast<cudaStream_t>(stream), &scratch);
   if (rc != PGG_OK) return rc;
   rc = pgg_dx_execute(gradY, weight, expandedRowIdx, groupList, M, N, K, G, L, batch, topK,
                       rowIdxType, dtype, scratch, kStaticScratchBytes, out, stream);

@@ -32,17 +32,64 @@ struct DyMaps {
 
 // Status codes written by the kernels (same values as pgg_status).
 constexpr uint32_t kStIndex = 16, kStGroupSum = 17, kStNotPerm = 18, kStTimeout = 19;
+constexpr uint32_t kStCheck = 20;  // a device bounds check failed (checked build only)
 
 // Start of the workspace. The status word comes first (documented in pgg.h).
 struct alignas(16) WsHeader {
   uint32_t status;        // first device-detected error, 0 = ok
   uint32_t sched_next;    // dynamic tile counter of the grouped-GEMM kernel
   uint32_t n_row_blocks;  // number of non-empty row blocks
-  uint32_t timeout_site;  // where a bounded wait ran out (diagnostic)
+  uint32_t timeout_site;  // where a bounded wait ran out, or (checked build) where a
+                          // bounds check failed (diagnostic)
   uint32_t unsorted;      // 1: some expert's rows are not in increasing original position
   uint32_t pad[11];
 };
 static_assert(sizeof(WsHeader) == 64, "header size");
+
+// Device bounds checks of the checked build (compiled with -DPGG_CHECKS).
+// check_index returns i when 0 <= i < n. Otherwise it records PGG_ERR_CHECK in
+// the status word (the first error wins; `site` goes to timeout_site) and
+// returns 0, so that the access stays inside the buffer and the kernel's
+// control flow, barriers and bounded waits are unchanged: nothing traps and
+// nothing hangs, and the caller reads the status word. The default build
+// compiles the check away and returns i.
+#ifdef __CUDACC__
+__device__ __forceinline__ int64_t check_index(WsHeader* hdr, int64_t i, int64_t n,
+                                               uint32_t site) {
+#ifdef PGG_CHECKS
+  if (i >= 0 && i < n) return i;
+  if (atomicCAS(&hdr->status, 0u, kStCheck) == 0u) hdr->timeout_site = site;
+  return 0;
+#else
+  (void)hdr;
+  (void)n;
+  (void)site;
+  return i;
+#endif
+}
+
+// The same for a condition: records PGG_ERR_CHECK and returns false when `ok`
+// is false (the caller then substitutes values that keep every access in
+// bounds); always true in the default build.
+__device__ __forceinline__ bool check_ok(WsHeader* hdr, bool ok, uint32_t site) {
+#ifdef PGG_CHECKS
+  if (!ok && atomicCAS(&hdr->status, 0u, kStCheck) == 0u) hdr->timeout_site = site;
+  return ok;
+#else
+  (void)hdr;
+  (void)ok;
+  (void)site;
+  return true;
+#endif
+}
+#endif
+
+// 1 in the checked build.
+#ifdef PGG_CHECKS
+constexpr int kCheckedBuild = 1;
+#else
+constexpr int kCheckedBuild = 0;
+#endif
 
 struct Layout {
   size_t hdr, off, rbstart, rblist, inv, rowinfo, tickets, seg, total;
@@ -89,6 +136,7 @@ struct GemmArgs {
   float* out;             // [batch, K]
   int64_t K;
   int64_t batch;
+  int64_t M, G, max_row_blocks;  // bounds of the routing tables (checked build)
   int32_t k_blocks;    // ceil(K / 128): ticket columns
   int32_t k_units;     // k blocks per row block in the tile order (pairs: k-block pairs)
   int32_t band_units;  // k units per band of the tile order
@@ -143,6 +191,7 @@ struct SimtArgs {
   int64_t N;
   int64_t K;
   int64_t batch;
+  int64_t M, G, max_row_blocks;  // bounds of the routing tables (checked build)
   int32_t k_blocks;
   uint32_t ticket_bias;
   int32_t vec_out;  // 1: K % 4 == 0 and out 16-byte aligned (16-byte stores / reductions)
@@ -174,6 +223,7 @@ struct FwdArgs {
   WsHeader* hdr;
   void* out;               // y [M, N] in the output dtype, expanded order
   int64_t M, N, K;
+  int64_t G, batch, max_row_blocks;  // bounds of the routing tables (checked build)
   int32_t n_blocks;  // output column blocks per row block
   int32_t out_f32;   // 1: y is fp32; 0: y has the input dtype
   uint64_t wait_limit_ns;

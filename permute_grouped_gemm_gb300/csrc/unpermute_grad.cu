@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kUThreads) unpermute_grad_kernel(const UnpermA
   for (int64_t p = static_cast<int64_t>(blockIdx.x) * (kUThreads / 32) + (threadIdx.x >> 5);
        p < a.M; p += warps) {
     const int64_t b = p / a.topK;
-    const int64_t row = a.row_idx_type == 0 ? static_cast<int64_t>(a.inv[p]) : a.idx[p];
+    const int64_t row = check_index(
+        a.hdr, a.row_idx_type == 0 ? static_cast<int64_t>(a.inv[p]) : a.idx[p], a.M, 80);
     const float pr = PROBS ? E::get(a.probs, p) : 1.0f;
     float dot = 0.0f;
     if constexpr (VEC) {

@@ -37,6 +37,19 @@ def test_exports_every_declared_function(lib):
         assert hasattr(raw, n), n
 
 
+def test_checked_build_compiles_loads_and_exports_every_declared_function():
+    # the same sources with -DPGG_CHECKS (device bounds checks), in a library of its own
+    path = pbuild.build(checks=True)
+    assert path == pbuild.LIB_CHECKS and os.path.isfile(path) and path != pbuild.LIB
+    raw = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+    raw.pgg_status_string.argtypes = [ctypes.c_int]
+    raw.pgg_status_string.restype = ctypes.c_char_p
+    assert b"bounds check" in raw.pgg_status_string(20)
+    assert pgg.STATUS[20] == "PGG_ERR_CHECK"
+
+
 # large-config sizes (pages' scale): M = 108000, G = 60, K = 7168, N = 2048
 LARGE = dict(M=108000, N=2048, K=7168, G=60, L=108000, batch=13500, topK=8)
 

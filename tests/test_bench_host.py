@@ -96,3 +96,25 @@ def test_reference_arm_prints_one_json_line(op):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"] == "tiny-fp32"
+
+
+def test_clock_summary_covers_only_the_samples_of_its_window():
+    c = bench.ClockSampler(0)
+    c.samples = [(1.0, 2070.0, 2070.0, (), 300.0),
+                 (2.0, 1700.0, 2070.0, ("sw_power_cap",), 1390.0),
+                 (3.0, 1800.0, 2070.0, (), 1200.0),
+                 (9.0, 900.0, 2070.0, ("hw_slowdown",), 200.0)]
+    s = c.summary(1.5, 3.5)
+    assert s["samples"] == 2 and s["sm_mhz"] == 1750.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1390.0
+    assert c.summary()["samples"] == 4
+    assert c.summary(4.0, 5.0) == {"sm_mhz": None, "sm_max_mhz": None,
+                                   "reasons": ["no samples"], "samples": 0, "source": "none"}
+
+
+def test_reason_bits_name_the_nvml_clock_event_reasons():
+    # nvmlClocksEventReason* bit values of the public NVML header
+    assert bench._REASON_BITS[0x4] == "sw_power_cap"
+    assert bench._REASON_BITS[0x8] == "hw_slowdown"
+    assert bench._REASON_BITS[0x20] == "sw_thermal_slowdown"
+    assert bench._REASON_BITS[0x40] == "hw_thermal_slowdown"

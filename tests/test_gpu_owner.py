@@ -143,8 +143,7 @@ def test_uniform_workload_full_size():
     w = WORKLOADS["uniform-bf16"]
     inp = make_inputs(w, device="cuda")
     out = run(inp)
-    toks = np.sort(np.random.default_rng(7).choice(w.batch, 64, replace=False))
-    check(inp, out, tokens=toks, what=w.name)
+    check(inp, out, what=w.name)  # every token
     assert torch.equal(out.view(torch.int32), run(inp, 0).view(torch.int32))
 
 

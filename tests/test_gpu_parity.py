@@ -10,6 +10,7 @@ import torch
 
 import oracle
 import permute_grouped_gemm_gb300 as pgg
+import sampling
 from workloads import WORKLOADS, make_case, make_inputs
 from workloads.moe import with_row_idx_type
 
@@ -327,27 +328,22 @@ def test_misaligned_pointers(dtype):
 
 # ---------------------------------------------------------------- full-size workloads
 
-def test_workload_tiny_fp32_full():
-    w = WORKLOADS["tiny-fp32"]
-    inp = make_inputs(w, device="cuda")
-    out = check(inp, what=w.name)
-    again, _ = run(inp)
-    assert torch.equal(out.view(torch.int32), again.view(torch.int32))
-
-
-@pytest.mark.parametrize("name", ["uniform-bf16", "skewed-fp16", "large-bf16", "skinny-bf16"])
-def test_workload_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["tiny-fp32", "uniform-bf16", "skewed-fp16", "large-bf16",
+                                  "skinny-bf16", "unaligned-bf16"])
+def test_workload_full_size(name):
+    # every token against the oracle (large-bf16: a seeded 1/16 of them), in the
+    # launch configuration the benchmark times; bitwise equal on a second run
     w = WORKLOADS[name]
     inp = make_inputs(w, device="cuda")
     out, ws = run(inp)
     assert pgg.status(ws) == 0
-    rng = np.random.default_rng(1)
-    toks = np.sort(rng.choice(w.batch, min(w.batch, 24), replace=False))
-    got = out.double().cpu().numpy()[toks]
+    toks = sampling.units(name, w.batch, seed=1)
+    got = out.double().cpu().numpy()
+    if toks is not None:
+        got = got[toks]
     assert_close(got, ref_rows(inp, toks), name)
     again, _ = run(inp, workspace=ws)
     assert torch.equal(out.view(torch.int32), again.view(torch.int32))
-    # every row was written: no row left at its initial content
     assert torch.isfinite(out).all()
 
 

@@ -1,0 +1,85 @@
+"""Bitwise reproducibility of d_x across fresh processes.
+
+The page "MoeInitRoutingGroupedMatmulGrad design" (section 2.4.1) asks for
+deterministic computation. Each d_x element receives its topK contributions in
+a fixed order (increasing expanded row), so the result must be the same bytes
+on every run: here three runs in this process and one in each of two fresh
+Python processes (five in all), on every benchmark workload, compared by the
+SHA-256 of the output bytes.
+"""
+
+import hashlib
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+NAMES = ["tiny-fp32", "uniform-bf16", "skewed-fp16", "large-bf16", "skinny-bf16",
+         "unaligned-bf16"]
+
+# One fresh process: builds nothing new (the library is already built), runs
+# d_x once per named workload and prints {name: sha256 of the output bytes}.
+CHILD = r"""
+import hashlib, json, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_inputs
+pgg.load()
+res = {}
+for name in sys.argv[2:]:
+    inp = make_inputs(WORKLOADS[name], device="cuda")
+    out, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                     inp.batch, inp.top_k, inp.row_idx_type)
+    torch.cuda.synchronize()
+    if pgg.status(ws) != 0:
+        raise SystemExit("device status %d on %s" % (pgg.status(ws), name))
+    res[name] = hashlib.sha256(out.cpu().numpy().tobytes()).hexdigest()
+    del inp, out, ws
+print(json.dumps(res))
+"""
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from permute_grouped_gemm_gb300 import build as pbuild
+    pbuild.build()
+    pgg.load()
+
+
+def _digest(t):
+    return hashlib.sha256(t.cpu().numpy().tobytes()).hexdigest()
+
+
+def test_dx_bytes_identical_in_and_across_processes():
+    here = {}
+    for name in NAMES:
+        inp = make_inputs(WORKLOADS[name], device="cuda")
+        got = set()
+        for _ in range(3):
+            out, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
+                             inp.batch, inp.top_k, inp.row_idx_type)
+            torch.cuda.synchronize()
+            assert pgg.status(ws) == 0
+            got.add(_digest(out))
+        assert len(got) == 1, f"{name}: runs in one process differ"
+        here[name] = got.pop()
+        del inp, out, ws
+        torch.cuda.empty_cache()
+    for _ in range(2):
+        r = subprocess.run([sys.executable, "-c", CHILD, ROOT, *NAMES], capture_output=True,
+                           text=True, timeout=900, cwd=ROOT)
+        assert r.returncode == 0, r.stderr[-3000:]
+        child = json.loads(r.stdout.strip().splitlines()[-1])
+        assert child == here, {n: (here[n], child.get(n)) for n in NAMES if child.get(n) != here[n]}

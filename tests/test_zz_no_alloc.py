@@ -6,14 +6,16 @@ reserved HBM at start-up and forbids cudaMalloc afterwards, plain C code with
 no allocator handle. pgg_dx_execute_static_scratch takes the same inputs and
 output as pgg_dx_execute but no workspace; the library's fixed device scratch
 array stands in for it. These checks call it through the C ABI and compare its
-output with that of the workspace-taking entry point, on two calls in a row
-(the second call finds the first call's leftovers in the shared array).
+output with that of the workspace-taking entry point and with the fp64 oracle,
+on two calls in a row (the second call finds the first call's leftovers in the
+shared array).
 """
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import permute_grouped_gemm_gb300 as pgg
 from workloads import make_case
 
@@ -29,7 +31,13 @@ def built():
         pytest.skip("no CUDA device")
     from permute_grouped_gemm_gb300 import build as pbuild
     pbuild.build()
+    oracle.build()
     pgg.load()
+
+
+def oracle_dx(inp):
+    return oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                     inp.top_k, inp.row_idx_type)
 
 
 def call_static(inp, out, status):
@@ -50,7 +58,8 @@ def test_static_scratch_matches_workspace_entry_point(dtype, row_idx_type):
     torch.cuda.synchronize()
     assert pgg.status(ws) == 0
     ref = ref.double().cpu().numpy()
-    scale = np.abs(ref).max()
+    exact = oracle_dx(inp)
+    scale = np.abs(exact).max()
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for _ in range(2):
         out = torch.full((inp.batch, inp.workload.K), float("nan"), device="cuda")
@@ -58,8 +67,10 @@ def test_static_scratch_matches_workspace_entry_point(dtype, row_idx_type):
         assert rc == 0, pgg.STATUS.get(rc, rc)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        err = np.abs(out.double().cpu().numpy() - ref).max()
-        assert err <= TOL * scale, f"max|diff| {err:.3e} > {TOL} * {scale:.3e}"
+        got = out.double().cpu().numpy()
+        for want, what in ((ref, "workspace entry point"), (exact, "oracle")):
+            err = np.abs(got - want).max()
+            assert err <= TOL * scale, f"{what}: max|diff| {err:.3e} > {TOL} * {scale:.3e}"
 
 
 def test_static_scratch_with_the_owner_plan():
@@ -74,6 +85,10 @@ def test_static_scratch_with_the_owner_plan():
                      inp.batch, inp.top_k, inp.row_idx_type)
     torch.cuda.synchronize()
     assert pgg.status(ws) == 0
+    toks = np.sort(np.random.default_rng(23).choice(inp.batch, 256, replace=False))
+    exact = oracle.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                      inp.top_k, inp.row_idx_type, tokens=toks)
+    scale = np.abs(exact).max()
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for _ in range(2):
         out = torch.full((inp.batch, w.K), float("nan"), device="cuda")
@@ -82,6 +97,8 @@ def test_static_scratch_with_the_owner_plan():
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+        err = np.abs(out.double().cpu().numpy()[toks] - exact).max()
+        assert err <= TOL * scale, f"oracle: max|diff| {err:.3e} > {TOL} * {scale:.3e}"
 
 
 def test_sizes_beyond_the_scratch_are_rejected():
