@@ -52,11 +52,16 @@
  *     workspace to 256 bytes; otherwise PGG_ERR_ALIGN. Any N and K are
  *     accepted. When N * sizeof(dtype) is a multiple of 16 bytes and gradY
  *     and weight are 16-byte aligned, the grouped GEMM runs on the tensor
- *     cores (operands streamed by the tensor-memory-access unit, which needs
- *     both); otherwise it runs on the FP32 pipes (plan variant 3), with the
- *     same ordered scatter-add and the same determinism. For the same call
- *     the two paths may differ in the last bits of the GEMM sums, never
- *     from run to run.
+ *     cores with its operands streamed by the tensor-memory-access unit,
+ *     which needs both. Otherwise, for 16-bit dtypes with an even N and
+ *     gradY and weight 4-byte aligned, it still runs on the tensor cores,
+ *     with the operands copied 4 bytes at a time by gather warps (plan
+ *     variant 5; same tiles, same bits as variant 0 where both apply). In
+ *     every other case (fp32 rows that are not a multiple of 16 bytes, odd
+ *     N, 2-byte aligned pointers) it runs on the FP32 pipes (plan variant
+ *     3), with the same ordered scatter-add and the same determinism. For
+ *     the same call the tensor-core and FP32-pipe paths may differ in the
+ *     last bits of the GEMM sums, never from run to run.
  */
 #ifndef PGG_H
 #define PGG_H
@@ -165,8 +170,11 @@ typedef struct {
                                not a multiple of 16), 4 = owner kernel (each CTA pair owns a
                                block of d_x: few experts per token, 16-bit dtypes; falls back
                                to variant 0 when an expert's rows are not in increasing original
-                               position); pgg_dx_execute also takes variant 3 when gradY or
-                               weight is not 16-byte aligned */
+                               position), 5 = variant 0 with its operands copied by gather
+                               warps (16-bit rows of an even length that is not a multiple of
+                               8 elements); pgg_dx_execute also takes variant 5 (4-byte aligned,
+                               16-bit, even N) or else 3 when gradY or weight is not 16-byte
+                               aligned */
   int32_t rows_per_block;   /* expanded rows per tile: the MMA N extent (variant 4: tokens per
                                slab) */
   int32_t k_per_block;      /* output columns per CTA and tile (128; a CTA pair covers 256) */
@@ -193,9 +201,10 @@ const char* pgg_status_string(int status);
  * pgg_debug_set_ticket_bias: added to the ticket count each ordered
  *   scatter-add waits for; a positive bias makes every wait of a row with
  *   rank > 0 run out, which exercises the PGG_ERR_TIMEOUT path. 0 = off.
- * pgg_debug_force_variant: -1 = automatic (default), 0, 1, 2, 3 or 4 = force
- *   the variant reported by pgg_dx_plan (2 and 4 exist for the 16-bit dtypes
- *   only; rows that are not a multiple of 16 bytes always take variant 3).
+ * pgg_debug_force_variant: -1 = automatic (default), 0 .. 5 = force the
+ *   variant reported by pgg_dx_plan (2, 4 and 5 exist for the 16-bit dtypes
+ *   only, 5 for an even N only; rows that are not a multiple of 16 bytes
+ *   take variant 5 when they can, else 3).
  * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
  *   automatic). The result does not depend on it, bit for bit: only the time
  *   order of the tiles changes, never the order of the additions.
@@ -271,9 +280,13 @@ int pgg_dx_execute_static_scratch(const void* gradY, const void* weight,
  * Each element is produced by one tile with a fixed order of additions (the
  * expert's rows in increasing order, in MMA blocks of 16), so the result is
  * bitwise repeatable. Runs on the tensor cores when dtype is 16-bit, K and N
- * are multiples of 8 and x, gradY, dweight are 16-byte aligned; otherwise on
- * the FP32 pipes (also forced by pgg_debug_force_variant(3)). Alignment: x and
- * gradY aligned to their element size, dweight to its element size.
+ * are multiples of 8 and x, gradY, dweight are 16-byte aligned (variant 0);
+ * also on the tensor cores, with the gradY rows copied 4 bytes at a time by
+ * the gather warps and dweight written with 4-byte stores, when N is even but
+ * not a multiple of 8 (or gradY / dweight are only 4-byte aligned) while K is
+ * a multiple of 8 and x is 16-byte aligned (variant 5); otherwise on the FP32
+ * pipes (variant 3, also forced by pgg_debug_force_variant(3)). Alignment: x
+ * and gradY aligned to their element size, dweight to its element size.
  */
 int pgg_dw_workspace_size(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L,
                           int64_t batch, int64_t topK, int rowIdxType, pgg_dtype dtype,
@@ -300,8 +313,10 @@ int pgg_dw_grouped_gemm(const void* x, const void* gradY, const int64_t* expande
 /*
  * How pgg_dw_execute runs these sizes with 16-byte aligned pointers: variant 0
  * (tensor cores: k_per_block = 128 output rows, 256 output columns, 64
- * reduction rows per stage) or 3 (FP32 pipes: 64 rows, 128 columns, 32 rows
- * per step); k_blocks and band_k_blocks hold the k and n blocks per expert.
+ * reduction rows per stage), 5 (the same with the gradY rows gathered by
+ * warps: N even, not a multiple of 8) or 3 (FP32 pipes: 64 rows, 128
+ * columns, 32 rows per step); k_blocks and band_k_blocks hold the k and n
+ * blocks per expert.
  */
 int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
                 int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
@@ -330,7 +345,11 @@ int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
  *
  * Each element is one dot product over k in a fixed order: bitwise
  * repeatable. Tensor cores when dtype is 16-bit, K and N are multiples of 8
- * and x, weight, y are 16-byte aligned; otherwise the FP32 pipes (also forced
+ * and x, weight, y are 16-byte aligned (variant 0); also on the tensor cores,
+ * with the weight rows copied 4 bytes at a time by the gather warps and y
+ * written with 4-byte stores, when N is even but not a multiple of 8 (or
+ * weight / y are only 4-byte aligned) while K is a multiple of 8 and x is
+ * 16-byte aligned (variant 5); otherwise the FP32 pipes (variant 3, also forced
  * by pgg_debug_force_variant(3)). x and weight aligned to their element size,
  * y to its element size.
  */
@@ -365,8 +384,9 @@ int pgg_fwd_grouped_gemm(const void* x, const void* weight, const int64_t* expan
 /*
  * How pgg_fwd_execute runs these sizes with 16-byte aligned pointers: variant
  * 0 (tensor cores on CTA pairs: row blocks of rows_per_block = 256 expanded
- * rows x 256 n, k_per_block = 64 per stage) or 3 (FP32 pipes: 64 rows x 128 n,
- * 32 k per step); band_k_blocks holds the n blocks per row block.
+ * rows x 256 n, k_per_block = 64 per stage), 5 (the same with the weight rows
+ * gathered by warps: N even, not a multiple of 8) or 3 (FP32 pipes: 64 rows x
+ * 128 n, 32 k per step); band_k_blocks holds the n blocks per row block.
  */
 int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
                  int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);

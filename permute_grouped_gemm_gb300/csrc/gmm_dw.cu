@@ -21,7 +21,11 @@
 //       producer warp per stage slot so that every slot can be in flight;
 //   B = d_y rows of the expert: each CTA loads its half of the 256 n (two
 //       64-n panels) by TMA, one copy through a 3-D view {64 n, rows, n / 64}
-//       when N is a multiple of 64, else one 2-D box per panel.
+//       when N is a multiple of 64, else one 2-D box per panel. When the d_y
+//       rows are not a multiple of 16 bytes (N even, not a multiple of 8),
+//       the gather warps copy the panels instead, one 128-byte row segment
+//       per warp instruction, 4 bytes per lane, into the same swizzled
+//       layout, and the epilogue writes with 4-byte stores.
 // Per SM a stage is 32 KB, so six stages fit: enough tensor work buffered to
 // cover the round trip of a stage (MMA done -> slot free -> copies -> slot
 // full). The even CTA issues the MMAs; completions are multicast to both.
@@ -125,8 +129,9 @@ __device__ void dy_producer(uint8_t* smem, DwCtl* ctl, const CUtensorMap* tm_dy,
   bool failed = false;
   for (uint32_t t = cluster_id(); t < total && !failed; t += n_clusters()) {
     const Tile x = tile_of(t, a, rank);
-    const uint32_t mine = b_bytes(a, x.n0, rank);
-    const uint32_t both = b_bytes(a, x.n0, 0) + b_bytes(a, x.n0, 1);
+    // gathered d_y rows: the arrival carries no bytes
+    const uint32_t mine = a.gather_dy ? 0u : b_bytes(a, x.n0, rank);
+    const uint32_t both = a.gather_dy ? 0u : b_bytes(a, x.n0, 0) + b_bytes(a, x.n0, 1);
     const int64_t nc = x.n0 + 128 * rank;
     for (int64_t r = 0; r < x.m; r += kDwRows) {
       if (!ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
@@ -268,6 +273,31 @@ __device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t 
                            : static_cast<const void*>(xb);
       ptx::cp_async_16(sa_slot + rr * 128 + (((kc & 7) ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
     }
+    if (a.gather_dy) {
+      // the d_y panels: the stage's 64 rows of the expert, this CTA's 128 n,
+      // 4 bytes (two n) per lane, zeros past the expert's rows and past N
+      const char* yb = static_cast<const char*>(a.dy);
+      const int64_t left = cur.x.m - cur.r;
+      const int64_t nrows = left < kDwRows ? left : kDwRows;
+      const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;
+      const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
+      const int64_t row_bytes = a.N * 2;
+      const uint32_t sb_slot = ptx::smem_addr(smem + w * kStageBytes) + kABytes;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int64_t n = cur.x.n0 + 128 * rank + 64 * p + 2 * lane;
+        const bool n_ok = n < a.N;  // N is even: n and n + 1 are both in or both out
+        const char* src = yb + ((cur.x.row0 + cur.r) * a.N + n) * 2;
+#pragma unroll 4
+        for (int r = 0; r < kDwRows; ++r) {
+          const bool ok = n_ok && r < nrows;
+          ptx::cp_async_4(sb_slot + p * kPanel + r * 128 + (((chunk ^ (r & 7)) << 4) | piece),
+                          ok ? static_cast<const void*>(src + r * row_bytes)
+                             : static_cast<const void*>(yb),
+                          ok ? 4u : 0u);
+        }
+      }
+    }
     ptx::cp_async_commit();
     stage_tokens(nxt, a, lane, tok);
     ptx::cp_async_wait<0>();
@@ -404,7 +434,14 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
     const int64_t k = x.k0 + 32 * quarter + lane;
     const bool k_ok = k < a.K;
     if (x.m == 0) {
-      if (k_ok) {
+      if (k_ok && a.gather_dy) {
+        // rows not 16-byte aligned: 4-byte zeros (N is even)
+        const int64_t n0 = x.n0 + col0;
+        uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<char*>(a.out) +
+                                                  ((x.g * a.K + k) * a.N + n0) * (f32 ? 4 : 2));
+        const int per = f32 ? 1 : 2;  // elements per 4-byte word
+        for (int c = 0; c < span / per && n0 + per * c < a.N; ++c) o[c] = 0u;
+      } else if (k_ok) {
         const int64_t n0 = x.n0 + col0;
         const int64_t base = (x.g * a.K + k) * a.N + n0;
         if (f32) {
@@ -443,6 +480,27 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
       if (lane == 0) ptx::bulk_wait_read<kOutBufs - 1>();
       __syncwarp();
       stage_row<DT>(buf, lane, v, f32);
+      if (a.gather_dy) {
+        // rows of N * 2 (or 4) bytes that are not 16-byte multiples: 4 bytes per
+        // lane, one 128-byte row segment per warp instruction, rows below K
+        // and columns below N only
+        __syncwarp();
+        const int64_t col = x.n0 + c0 + lane * (f32 ? 1 : 2);
+        const uint32_t off = ((static_cast<uint32_t>(lane) >> 2) << 4) | ((lane & 3) << 2);
+        const int oes = f32 ? 4 : 2;
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          if (k_row + r < a.K && col < a.N) {
+            const uint32_t d =
+                *reinterpret_cast<const uint32_t*>(buf + r * 128 + (off ^ ((r & 7) << 4)));
+            char* dst = static_cast<char*>(a.out) + ((x.g * a.K + k_row + r) * a.N + col) * oes;
+            *reinterpret_cast<uint32_t*>(dst) = d;
+          }
+        }
+        __syncwarp();
+        ++nb;
+        continue;
+      }
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -507,8 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tm_dy);
-    ptx::tma_prefetch_desc(&tm_out);
+    if (!a.gather_dy) {
+      ptx::tma_prefetch_desc(&tm_dy);
+      ptx::tma_prefetch_desc(&tm_out);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);

@@ -88,7 +88,7 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int DT, int ROWS, int STAGES, bool PAIR = false>
+template <int DT, int ROWS, int STAGES, bool PAIR = false, bool GATHER = false>
 struct Cfg {
   static constexpr bool kSplit = DtTraits<DT>::kSplit;
   static constexpr int kElemsPerRow = kRowBytes / DtTraits<DT>::kElem;
@@ -107,7 +107,11 @@ struct Cfg {
   static constexpr int kEpiGroups = kSplit ? 1 : 2;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kXformWarps = kSplit ? 4 : 0;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps + kXformWarps);
+  // Gathered operands: one warp per stage slot copies the slot's rows with
+  // 4-byte cp.async (rows whose byte length is not a multiple of 16).
+  static constexpr int kGatherWarps = GATHER ? STAGES : 0;
+  static constexpr int kGatherWarp0 = 2 + kEpiWarps + kXformWarps;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kXformWarps + kGatherWarps);
   static constexpr int kMmaM = PAIR ? 2 * kKBlock : kKBlock;
   static constexpr int kNAlign = PAIR ? 32 : 16;  // MMA N granularity
   // consumers of a tile-queue slot: MMA + epilogue (+ fp32 split), and in a
@@ -116,6 +120,7 @@ struct Cfg {
   static constexpr uint32_t kTEmpty = PAIR ? 8 : 4;  // one group's warps (of both CTAs)
   static_assert(ROWS % 32 == 0 && ROWS <= 256, "rows per block");
   static_assert(!PAIR || (!kSplit && ROWS % 64 == 0), "pairs: 16-bit inputs, rows % 64 == 0");
+  static_assert(!GATHER || !kSplit, "gathered operands: 16-bit inputs");
   static_assert(kTmemCols <= 512, "tmem columns");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -138,9 +143,21 @@ struct EpiState {
   RowInfo meta[ROWS];
 };
 
+// What the gather warp of a stage slot copies (gathered-operand kernel): the
+// weight rows of k block kb of expert g and `fill` rows of d_y from `row` on
+// (of which the first `valid` are read, the rest zero-filled), each over the
+// 64 n from n0.
+struct GatherDesc {
+  int32_t g;  // -1: no more stages
+  int32_t row, valid, fill, kb, n0;
+  int32_t pad[2];
+};
+
 template <int ROWS, int STAGES>
 struct Ctl {
-  uint64_t full[STAGES];   // TMA bytes landed (pairs: both CTAs' bytes, even CTA's barrier)
+  uint64_t full[STAGES];   // operands landed: TMA bytes (pairs: both CTAs' bytes, even CTA's
+                           // barrier), or the arrivals of the gather warps of both CTAs
+  uint64_t dfull[STAGES];  // gathered operands: the slot's descriptor is posted
   uint64_t empty[STAGES];  // MMAs reading the stage completed
   uint64_t ready[STAGES];  // fp32 split done
   uint64_t tfull[2];       // accumulator complete
@@ -149,6 +166,7 @@ struct Ctl {
   uint64_t qempty[kQueue];
   uint64_t drain;
   int4 q[kQueue];  // {expert (-1 = stop), first row, rows, k unit}
+  GatherDesc desc[STAGES];
   uint32_t tmem_base;
   int abort;
   EpiState<ROWS> epi[2];  // one per epilogue group
@@ -200,11 +218,11 @@ __device__ __forceinline__ void decode_tile(uint32_t t, uint32_t n_rb, uint32_t 
   *kb = kb_lo + rem % w;
 }
 
-template <int DT, int ROWS, int STAGES, bool PAIR>
+template <int DT, int ROWS, int STAGES, bool PAIR, bool GATHER>
 __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy_maps,
                          const CUtensorMap* tm_w, const GemmArgs& args, uint32_t total,
                          uint32_t rank) {
-  using C = Cfg<DT, ROWS, STAGES, PAIR>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR, GATHER>;
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const bool leader = rank == 0;
@@ -264,7 +282,8 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
       break;
     }
     const int nm = mma_n<C>(e.z);
-    const int b_rows = PAIR ? nm / 2 : e.z;  // rows of d_y this CTA stages
+    // rows of d_y this CTA stages (gathered: every row the MMA reads)
+    const int b_rows = PAIR ? nm / 2 : (GATHER ? nm : e.z);
     const int bj = dy_box<C::kBRows>(b_rows);
     const uint32_t box_bytes = static_cast<uint32_t>(kDyMinRows << bj) * kRowBytes;
     const uint32_t tx = PAIR ? 2 * (C::kABytes + box_bytes) : C::kABytes + box_bytes;
@@ -282,7 +301,22 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
       }
       uint8_t* sa = smem + stage * C::kStageBytes;
       const int32_t n0 = ks * C::kElemsPerRow;
-      if constexpr (PAIR) {
+      if constexpr (GATHER) {
+        // the slot's gather warp copies the operands (the slot is free: the
+        // MMAs that read it, and so the copies of its previous use, are done)
+        GatherDesc& d = ctl->desc[stage];
+        const int mine = e.z - (PAIR ? static_cast<int>(rank) * (nm / 2) : 0);
+        d.g = e.x;
+        d.row = brow;
+        d.fill = b_rows;
+        d.valid = mine < 0 ? 0 : (mine < b_rows ? mine : b_rows);
+        d.kb = kb;
+        d.n0 = n0;
+        ptx::mbar_arrive(&ctl->dfull[stage]);
+        (void)sa;
+        (void)tx;
+        (void)tm_dy;
+      } else if constexpr (PAIR) {
         const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
         if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], tx);
         ptx::tma_load_3d_pair(sa, tm_w, fb, n0, kb * kKBlock, e.x);
@@ -308,13 +342,32 @@ __device__ void producer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const DyMaps* dy
       e = e_next;
     }
   }
+  if constexpr (GATHER) {
+    // one stop descriptor per slot, each once the slot's last stage is consumed
+    for (int i = 0; i < STAGES && !failed; ++i) {
+      const bool ok = PAIR ? ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)
+                           : ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, lim, abort);
+      if (!ok) {
+        failed = true;
+        break;
+      }
+      ctl->desc[stage].g = -1;
+      ptx::mbar_arrive(&ctl->dfull[stage]);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
   if (failed) {
     ctl->abort = 1;
     raise_status(args.hdr, kStTimeout, 2);
   }
-  // Never leave while a copy into this CTA's shared memory may be in flight.
+  // Gathered operands: each gather warp waits for its own copies. Otherwise
+  // never leave while a copy into this CTA's shared memory may be in flight.
   // A pair's odd CTA cannot see its copies complete (they signal the even
   // CTA's barrier); the even CTA's MMA consuming the stage implies it.
+  if constexpr (GATHER) return;
   int no_abort = 0;
   for (int s = 0; s < STAGES; ++s) {
     if (!(outstanding & (1u << s))) continue;
@@ -472,6 +525,81 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
     }
     if (stop) break;
   }
+}
+
+// Gather warp of stage slot `slot` (gathered-operand kernel, rows of N * 2
+// bytes that are 4-byte but not 16-byte multiples): for each descriptor the
+// scheduler posts to the slot, it copies the slot's 128 weight rows and `fill`
+// d_y rows, one 128-byte row segment (64 n) per warp instruction, 4 bytes per
+// lane, with cp.async into the layout the tensor-memory-access unit would
+// have written (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)
+// of the row's 128 bytes, rows 128 bytes apart), zero-filling rows and
+// columns outside the operands. Then it waits for its copies, makes them
+// visible to the tensor cores and arrives on the slot's full barrier (the even
+// CTA's, for a pair).
+template <int DT, int ROWS, int STAGES, bool PAIR>
+__device__ void gatherer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArgs& args) {
+  using C = Cfg<DT, ROWS, STAGES, PAIR, true>;
+  using T = Cfg<DT, ROWS, STAGES, PAIR, false>;
+  static_assert(C::kStageBytes == T::kStageBytes && C::kMmaM == T::kMmaM &&
+                    C::kWords == T::kWords && C::kABytes == T::kABytes,
+                "the gathered operands fill the stages of the TMA variant");
+  const uint64_t lim = args.wait_limit_ns;
+  volatile int* abort = &ctl->abort;
+  const int slot = (threadIdx.x >> 5) - C::kGatherWarp0;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sa = ptx::smem_addr(smem + slot * C::kStageBytes);
+  const uint32_t sb = sa + C::kABytes;
+  const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;  // bytes within the chunk
+  const uint32_t chunk = static_cast<uint32_t>(lane >> 2);      // 16-byte chunk of the row
+  const char* wb = static_cast<const char*>(args.w);
+  const char* yb = static_cast<const char*>(args.dy);
+  const int64_t N = args.N, K = args.K;
+  const int64_t row_bytes = N * 2;
+  uint32_t full = 0;
+  if constexpr (PAIR) full = ptx::mapa(&ctl->full[slot], 0);
+  uint32_t phase = 0;
+  while (true) {
+    if (!ptx::mbar_wait(&ctl->dfull[slot], phase, lim, abort)) {
+      if (!*abort) {
+        ctl->abort = 1;
+        if (lane == 0) raise_status(args.hdr, kStTimeout, 7);
+      }
+      break;
+    }
+    const GatherDesc d = ctl->desc[slot];
+    if (d.g < 0) break;
+    const int64_t n = static_cast<int64_t>(d.n0) + 2 * lane;
+    const bool n_ok = n < N;  // N is even: the pair n, n + 1 is all in or all out
+    const int64_t k0 = static_cast<int64_t>(d.kb) * kKBlock;
+    const int64_t kn = K - k0 < kKBlock ? K - k0 : kKBlock;  // weight rows inside K
+    const char* src = wb + ((static_cast<int64_t>(d.g) * K + k0) * N + n) * 2;
+#pragma unroll 4
+    for (int r = 0; r < kKBlock; ++r) {
+      const bool ok = n_ok && r < kn;
+      const uint32_t dst = sa + r * kRowBytes + (((chunk ^ (r & 7)) << 4) | piece);
+      ptx::cp_async_4(dst, ok ? src + r * row_bytes : wb, ok ? 4u : 0u);
+    }
+    const char* ysrc = yb + (static_cast<int64_t>(d.row) * N + n) * 2;
+#pragma unroll 4
+    for (int r = 0; r < d.fill; ++r) {
+      const bool ok = n_ok && r < d.valid;
+      const uint32_t dst = sb + r * kRowBytes + (((chunk ^ (r & 7)) << 4) | piece);
+      ptx::cp_async_4(dst, ok ? ysrc + r * row_bytes : yb, ok ? 4u : 0u);
+    }
+    ptx::cp_async_commit();
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (PAIR)
+        ptx::mbar_arrive_remote(full);
+      else
+        ptx::mbar_arrive(&ctl->full[slot]);
+    }
+    phase ^= 1u;
+  }
+  ptx::cp_async_wait<0>();
 }
 
 // Rows of the tile whose ticket says they may be added now. Thread et looks
@@ -664,7 +792,9 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
                             static_cast<uint32_t>(acc * C::kAccCols);
     uint64_t t_wait0 = 0;
-    while (kb_ok) {
+    // (a tile without rows, which only the checked build's substitution for a
+    // bad row block makes, has nothing to wait for)
+    while (kb_ok && R > 0) {
       // 1. which pending rows may go now
       ready_rows(es, args, R, kb, gave_up);
       ptx::named_bar_sync(bar, 128);
@@ -718,11 +848,11 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
   }
 }
 
-template <int DT, int ROWS, int STAGES, bool PAIR>
-__global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
+template <int DT, int ROWS, int STAGES, bool PAIR, bool GATHER>
+__global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR, GATHER>::kThreads, 1)
     gmm_dx_kernel(const __grid_constant__ DyMaps dy_maps, const __grid_constant__ CUtensorMap tm_w,
                   const GemmArgs args) {
-  using C = Cfg<DT, ROWS, STAGES, PAIR>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR, GATHER>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -749,9 +879,11 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&ctl->full[s], 1);
+      // gathered operands: one arrival from the slot's gather warp in each CTA
+      ptx::mbar_init(&ctl->full[s], GATHER ? (PAIR ? 2 : 1) : 1);
       ptx::mbar_init(&ctl->empty[s], 1);
       ptx::mbar_init(&ctl->ready[s], 1);
+      ptx::mbar_init(&ctl->dfull[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ctl->tfull[a], 1);
@@ -765,7 +897,7 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (!GATHER && warp == 0 && lane == 0) {
     for (int j = 0; j < kDyMaps; ++j) ptx::tma_prefetch_desc(&dy_maps.box[j]);
     ptx::tma_prefetch_desc(&tm_w);
   }
@@ -785,13 +917,16 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer<DT, ROWS, STAGES, PAIR>(smem, ctl, &dy_maps, &tm_w, args, total, rank);
+    if (lane == 0)
+      producer<DT, ROWS, STAGES, PAIR, GATHER>(smem, ctl, &dy_maps, &tm_w, args, total, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_issuer<DT, ROWS, STAGES, PAIR>(smem, ctl, tmem_base, args);
   } else if (warp < 2 + C::kEpiWarps) {
     epilogue<DT, ROWS, STAGES, PAIR>(ctl, tmem_base, args, rank);
-  } else if constexpr (C::kSplit) {
-    transformer<DT, ROWS, STAGES>(smem, ctl, args);
+  } else if (warp < C::kGatherWarp0) {
+    if constexpr (C::kSplit) transformer<DT, ROWS, STAGES>(smem, ctl, args);
+  } else {
+    if constexpr (GATHER) gatherer<DT, ROWS, STAGES, PAIR>(smem, ctl, args);
   }
 
   ptx::tc_fence_before_sync();
@@ -806,12 +941,12 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR>::kThreads, 1)
   }
 }
 
-template <int DT, int ROWS, int STAGES, bool PAIR>
+template <int DT, int ROWS, int STAGES, bool PAIR, bool GATHER>
 cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& args, int max_ctas,
                      cudaStream_t stream) {
-  using C = Cfg<DT, ROWS, STAGES, PAIR>;
+  using C = Cfg<DT, ROWS, STAGES, PAIR, GATHER>;
   constexpr int smem = smem_bytes<DT, ROWS, STAGES, PAIR>();
-  auto kern = gmm_dx_kernel<DT, ROWS, STAGES, PAIR>;
+  auto kern = gmm_dx_kernel<DT, ROWS, STAGES, PAIR, GATHER>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   if constexpr (!PAIR) {
@@ -840,26 +975,29 @@ cudaError_t launch_t(const DyMaps& tdy, const CUtensorMap& tw, const GemmArgs& a
   }
 }
 
-// (dtype, variant) -> (rows per block, stages, CTA pair)
-#define PGG_VARIANTS(X)          \
-  X(PGG_BF16, 0, 256, 6, true)   \
-  X(PGG_BF16, 1, 32, 10, false)  \
-  X(PGG_BF16, 2, 256, 4, false)  \
-  X(PGG_F16, 0, 256, 6, true)    \
-  X(PGG_F16, 1, 32, 10, false)   \
-  X(PGG_F16, 2, 256, 4, false)   \
-  X(PGG_F32, 0, 128, 3, false)   \
-  X(PGG_F32, 1, 32, 4, false)
+// (dtype, variant) -> (rows per block, stages, CTA pair, gathered operands);
+// variant 5 is variant 0 with its operands copied by gather warps.
+#define PGG_VARIANTS(X)                \
+  X(PGG_BF16, 0, 256, 6, true, false)  \
+  X(PGG_BF16, 1, 32, 10, false, false) \
+  X(PGG_BF16, 2, 256, 4, false, false) \
+  X(PGG_BF16, 5, 256, 6, true, true)   \
+  X(PGG_F16, 0, 256, 6, true, false)   \
+  X(PGG_F16, 1, 32, 10, false, false)  \
+  X(PGG_F16, 2, 256, 4, false, false)  \
+  X(PGG_F16, 5, 256, 6, true, true)    \
+  X(PGG_F32, 0, 128, 3, false, false)  \
+  X(PGG_F32, 1, 32, 4, false, false)
 
 }  // namespace
 
 bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads, int* smem,
                    int* pair) {
-#define PGG_CFG(DT, V, R, S, P)                 \
+#define PGG_CFG(DT, V, R, S, P, GA)             \
   if (dtype == DT && variant == V) {            \
     *rows = R;                                  \
     *stages = S;                                \
-    *threads = Cfg<DT, R, S, P>::kThreads;      \
+    *threads = Cfg<DT, R, S, P, GA>::kThreads;  \
     *smem = smem_bytes<DT, R, S, P>();          \
     *pair = P ? 1 : 0;                          \
     return true;                                \
@@ -871,8 +1009,9 @@ bool kernel_config(int dtype, int variant, int* rows, int* stages, int* threads,
 
 cudaError_t launch_grouped_gemm(int dtype, int variant, const DyMaps& tdy, const CUtensorMap& tw,
                                 const GemmArgs& args, int max_ctas, cudaStream_t stream) {
-#define PGG_LAUNCH(DT, V, R, S, P) \
-  if (dtype == DT && variant == V) return launch_t<DT, R, S, P>(tdy, tw, args, max_ctas, stream);
+#define PGG_LAUNCH(DT, V, R, S, P, GA) \
+  if (dtype == DT && variant == V)     \
+    return launch_t<DT, R, S, P, GA>(tdy, tw, args, max_ctas, stream);
   PGG_VARIANTS(PGG_LAUNCH)
 #undef PGG_LAUNCH
   return cudaErrorInvalidValue;

@@ -18,7 +18,11 @@
 //       producer warp per stage slot; rows past the block and k past K read
 //       as 0. The tokens of a tile are loaded once.
 //   B = weight[g, k0 .. k0 + 63, n], MN-major: each CTA loads its half of the
-//       256 n as two 64-n panels by TMA from a 3-D map {N, K, G}.
+//       256 n as two 64-n panels by TMA from a 3-D map {N, K, G}. When the
+//       weight rows are not a multiple of 16 bytes (N even, not a multiple of
+//       8), the gather warps copy the panels instead, one 128-byte k row
+//       segment per warp instruction, 4 bytes per lane, into the same
+//       swizzled layout, and the epilogue writes y with 4-byte stores.
 // The epilogue warps convert 128-byte row chunks into a swizzled
 // shared-memory box and store it with one TMA tensor store; a box that would
 // cross the end of the row block (into the next expert's rows) is written
@@ -119,7 +123,8 @@ __device__ void w_producer(uint8_t* smem, FwdCtl* ctl, const CUtensorMap* tm_w, 
   bool failed = false;
   for (uint32_t t = cluster_id(); t < total && !failed; t += n_clusters()) {
     const FTile x = ftile_of(t, a, rank);
-    const uint32_t both = b_bytes(a, x.n0, 0) + b_bytes(a, x.n0, 1);
+    // gathered weight rows: the arrival carries no bytes
+    const uint32_t both = a.gather_w ? 0u : b_bytes(a, x.n0, 0) + b_bytes(a, x.n0, 1);
     const int64_t nc = x.n0 + 128 * rank;
     for (int ks = 0; ks < nks; ++ks) {
       if (!ptx::mbar_wait_cluster(&ctl->empty[stage], phase ^ 1u, lim, abort)) {
@@ -129,7 +134,7 @@ __device__ void w_producer(uint8_t* smem, FwdCtl* ctl, const CUtensorMap* tm_w, 
       uint8_t* sb = smem + stage * kStageBytes + kABytes;
       const uint32_t fb = ptx::mapa(&ctl->full[stage], 0);
       if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], both);
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < 2 && !a.gather_w; ++j)
         if (nc + 64 * j < a.N)
           ptx::tma_load_3d_pair(sb + j * kPanel, tm_w, fb, static_cast<int32_t>(nc + 64 * j),
                                 ks * kFK, static_cast<int32_t>(x.g));
@@ -211,6 +216,31 @@ __device__ void x_gatherer(uint8_t* smem, FwdCtl* ctl, const FwdArgs& a, uint32_
       const void* src = ok ? static_cast<const void*>(xb + (static_cast<int64_t>(tk) * a.K + k) * 2)
                            : static_cast<const void*>(xb);
       ptx::cp_async_16(sa_slot + rr * 128 + ((c ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
+    }
+    if (a.gather_w) {
+      // the weight panels: k rows kb * 64 .. + 63 of expert g, this CTA's 128
+      // n from nc, 4 bytes (two n) per lane, zeros outside K and N
+      const char* wb = static_cast<const char*>(a.w);
+      const int64_t k0 = static_cast<int64_t>(kb) * kFK;
+      const int64_t kn = a.K - k0 < kFK ? a.K - k0 : kFK;
+      const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;
+      const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
+      const int64_t row_bytes = a.N * 2;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int64_t n = x.n0 + 128 * rank + 64 * p + 2 * lane;
+        const bool n_ok = n < a.N;  // N is even: n and n + 1 are both in or both out
+        const char* src = wb + ((x.g * a.K + k0) * a.N + n) * 2;
+        const uint32_t dst0 = sa_slot + kABytes + p * kPanel;
+#pragma unroll 4
+        for (int r = 0; r < kFK; ++r) {
+          const bool ok = n_ok && r < kn;
+          ptx::cp_async_4(dst0 + r * 128 + (((chunk ^ (r & 7)) << 4) | piece),
+                          ok ? static_cast<const void*>(src + r * row_bytes)
+                             : static_cast<const void*>(wb),
+                          ok ? 4u : 0u);
+        }
+      }
     }
     ptx::cp_async_commit();
     ptx::cp_async_wait<0>();
@@ -355,7 +385,25 @@ __device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
         *reinterpret_cast<uint4*>(buf + lane * 128 + ((p ^ (lane & 7)) << 4)) = q;
       }
       const int64_t n = x.n0 + c0;
-      if (valid >= 32) {
+      if (a.gather_w) {
+        // rows of N * 2 bytes that are not 16-byte multiples: 4 bytes per
+        // lane (one 128-byte row segment per warp instruction), existing rows
+        // and columns only
+        __syncwarp();
+        const int rows = valid < 32 ? valid : 32;
+        const int64_t col = n + lane * (4 / oes);
+        const uint32_t off = (((static_cast<uint32_t>(lane) >> 2) << 4) | ((lane & 3) << 2));
+#pragma unroll 4
+        for (int r = 0; r < rows; ++r) {
+          if (col < a.N) {
+            const uint32_t d =
+                *reinterpret_cast<const uint32_t*>(buf + r * 128 + (off ^ ((r & 7) << 4)));
+            char* dst = static_cast<char*>(a.out) + ((row_w + r) * a.N + col) * oes;
+            *reinterpret_cast<uint32_t*>(dst) = d;
+          }
+        }
+        __syncwarp();
+      } else if (valid >= 32) {
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -432,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && !a.gather_w) {
     ptx::tma_prefetch_desc(&tm_w);
     ptx::tma_prefetch_desc(&tm_y);
   }

@@ -66,8 +66,9 @@ std::atomic<int> g_force_variant{-1};
 std::atomic<int> g_band_k_blocks{0};
 
 constexpr int64_t kInt32Max = 2147483647;
-constexpr int kVariantSimt = 3;   // FP32-pipe kernel (gmm_dx_simt.cu)
-constexpr int kVariantOwner = 4;  // slab-owner kernel (gmm_dx_owner.cu), ticketed fallback
+constexpr int kVariantSimt = 3;    // FP32-pipe kernel (gmm_dx_simt.cu)
+constexpr int kVariantOwner = 4;   // slab-owner kernel (gmm_dx_owner.cu), ticketed fallback
+constexpr int kVariantGather = 5;  // ticketed pair kernel, operands copied by gather warps
 
 // Token slab of the owner variant: about 112 rows of each expert per slab
 // when the routing is even (G * T / topK rows), so that most experts take one
@@ -111,6 +112,10 @@ int check_sizes(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
 // byte length must be a multiple of 16.
 bool rows_streamable(int64_t N, int dtype) { return (N * elem_size(dtype)) % 16 == 0; }
 
+// Rows that the gather warps of variant 5 can copy 4 bytes at a time: 16-bit
+// elements, an even count per row.
+bool rows_gatherable(int64_t N, int dtype) { return dtype != PGG_F32 && N % 2 == 0; }
+
 // rows_override > 0: row blocks of that many rows (the forward's 256) instead
 // of the d_x variant's.
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
@@ -123,7 +128,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t
     if (owner_fits(K, G, batch, topK, dtype)) variant = kVariantOwner;
   }
   if (variant == kVariantOwner && dtype == PGG_F32) variant = 0;
-  if (!rows_streamable(N, dtype)) variant = kVariantSimt;
+  if (variant == kVariantGather && !rows_gatherable(N, dtype)) variant = kVariantSimt;
+  if (!rows_streamable(N, dtype) && variant != kVariantSimt)
+    variant = rows_gatherable(N, dtype) ? kVariantGather : kVariantSimt;
   p->variant = variant;
   if (variant == kVariantSimt) {
     simt_config(&p->rows_per_block, &p->stages, &p->threads, &p->smem_bytes);
@@ -361,15 +368,27 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
                      cudaStream_t stream) {
   DeviceInfo di;
   if (device_info(&di) != PGG_OK) return PGG_ERR_CUDA;
-  if (plan.variant == kVariantSimt || !aligned(gradY, 16) || !aligned(weight, 16))
+  if (plan.variant == kVariantSimt) return run_simt(plan, gradY, weight, ws, out, di, stream);
+  // Operands the tensor-memory-access unit cannot stream (rows, or pointers
+  // not 16-byte aligned): copied by gather warps when their rows and pointers
+  // allow 4-byte copies, else the FP32-pipe kernel. Every plan's row blocks
+  // have at most 256 rows, which both kernels take.
+  const bool gather = plan.variant == kVariantGather || !aligned(gradY, 16) ||
+                      !aligned(weight, 16);
+  if (gather && !(rows_gatherable(plan.N, plan.dtype) && aligned(gradY, 4) && aligned(weight, 4)))
     return run_simt(plan, gradY, weight, ws, out, di, stream);
   DyMaps tdy;
-  const bool owner = plan.variant == kVariantOwner;
+  const bool owner = plan.variant == kVariantOwner && !gather;
   CUtensorMap tw;
-  int rc = encode_maps(plan, gradY, weight, &tdy, &tw);
+  std::memset(&tdy, 0, sizeof(tdy));
+  std::memset(&tw, 0, sizeof(tw));
+  int rc = gather ? PGG_OK : encode_maps(plan, gradY, weight, &tdy, &tw);
   if (rc != PGG_OK) return rc;
   char* w = static_cast<char*>(ws);
   GemmArgs a;
+  a.dy = gradY;
+  a.w = weight;
+  a.N = plan.N;
   a.rblist = reinterpret_cast<const int4*>(w + plan.layout.rblist);
   a.rowinfo = reinterpret_cast<const RowInfo*>(w + plan.layout.rowinfo);
   a.tickets = reinterpret_cast<uint32_t*>(w + plan.layout.tickets);
@@ -427,10 +446,18 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
   }
   // the ticketed kernel; after the owner kernel it works only when that one
   // could not (some expert's rows not in increasing original position)
-  const int64_t max_ctas = plan.max_row_blocks * plan.k_units * (plan.pair ? 2 : 1);
+  // the gathered-operand kernel takes the tiles of variant 0 (CTA pairs of
+  // 256 k, row blocks of up to 256 rows)
+  const int kernel_variant = gather ? kVariantGather : (owner ? 0 : plan.variant);
+  const int k_units = gather ? (plan.k_blocks + 1) / 2 : plan.k_units;
+  if (gather) {
+    a.k_units = k_units;
+    a.band_units = (plan.band_k_blocks + 1) / 2;
+  }
+  const int64_t max_ctas =
+      plan.max_row_blocks * k_units * ((gather || plan.pair) ? 2 : 1);
   const int grid = static_cast<int>(max_ctas < di.num_sms ? max_ctas : di.num_sms);
-  return launch_grouped_gemm(plan.dtype, owner ? 0 : plan.variant, tdy, tw, a, grid, stream) ==
-                 cudaSuccess
+  return launch_grouped_gemm(plan.dtype, kernel_variant, tdy, tw, a, grid, stream) == cudaSuccess
              ? PGG_OK
              : PGG_ERR_CUDA;
 }
@@ -446,6 +473,18 @@ bool dw_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void* 
   if (dtype == PGG_F32) return false;
   if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0) return false;
   return aligned(x, 16) && aligned(dy, 16) && aligned(out, 16);
+}
+
+// The tensor-core weight gradient with the d_y rows copied by its gather
+// warps (4 bytes at a time) and the output written with 4-byte stores: 16-bit
+// inputs, x rows whole 16-byte units and x 16-byte aligned (gathered 16 bytes
+// at a time), N even, d_y and the output 4-byte aligned.
+bool dw_gather_path(int dtype, int64_t N, int64_t K, const void* x, const void* dy,
+                    const void* out) {
+  if (g_force_variant.load() == kVariantSimt) return false;
+  if (dtype == PGG_F32) return false;
+  if ((K * 2) % 16 != 0 || N % 2 != 0) return false;
+  return aligned(x, 16) && aligned(dy, 4) && aligned(out, 4);
 }
 
 int check_dw(const void* x, const void* gradY, const int64_t* idx, const int64_t* gl,
@@ -487,7 +526,17 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
   a.batch = plan.batch;
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
   a.dy_3d = 0;
+  a.gather_dy = 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
+  if (!dw_tensor_path(plan.dtype, plan.N, plan.K, x, gradY, dweight) &&
+      dw_gather_path(plan.dtype, plan.N, plan.K, x, gradY, dweight)) {
+    dw_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
+    a.gather_dy = 1;
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof(none));
+    return launch_dw(plan.dtype, none, none, a, di.num_sms, stream) == cudaSuccess ? PGG_OK
+                                                                                   : PGG_ERR_CUDA;
+  }
   if (dw_tensor_path(plan.dtype, plan.N, plan.K, x, gradY, dweight)) {
     dw_tiles(plan.K, plan.N, &a.k_blocks, &a.n_blocks);
     EncodeTiledFn enc = encode_fn();
@@ -555,6 +604,18 @@ bool fwd_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void*
   return aligned(x, 16) && aligned(w, 16) && aligned(y, 16);
 }
 
+// The tensor-core forward with the weight rows copied by its gather warps (4
+// bytes at a time) and y written with 4-byte stores: 16-bit inputs, x rows
+// whole 16-byte units and x 16-byte aligned (gathered 16 bytes at a time), N
+// even, weight and y 4-byte aligned.
+bool fwd_gather_path(int dtype, int64_t N, int64_t K, const void* x, const void* w,
+                     const void* y) {
+  if (g_force_variant.load() == kVariantSimt) return false;
+  if (dtype == PGG_F32) return false;
+  if ((K * 2) % 16 != 0 || N % 2 != 0) return false;
+  return aligned(x, 16) && aligned(w, 4) && aligned(y, 4);
+}
+
 int make_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t batch, int64_t topK,
                   int rowIdxType, int dtype, Plan* p) {
   return make_plan(M, N, K, G, batch, topK, rowIdxType, dtype, p, fwd_rows_per_block());
@@ -600,6 +661,18 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
   a.max_row_blocks = plan.max_row_blocks;
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
+  a.gather_w = 0;
+  if (!fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y) &&
+      fwd_gather_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
+    fwd_tiles(plan.N, &a.n_blocks);
+    a.gather_w = 1;
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof(none));
+    return launch_fwd(plan.dtype, none, none, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
+                      stream) == cudaSuccess
+               ? PGG_OK
+               : PGG_ERR_CUDA;
+  }
   if (fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
     fwd_tiles(plan.N, &a.n_blocks);
     EncodeTiledFn enc = encode_fn();
@@ -744,11 +817,12 @@ int pgg_dw_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t b
   // 16-byte aligned pointers assumed: only the shape decides here
   alignas(16) static const char probe[16] = {0};
   const bool tc = dw_tensor_path(dtype, N, K, probe, probe, probe);
+  const bool ga = !tc && dw_gather_path(dtype, N, K, probe, probe, probe);
   std::memset(info, 0, sizeof(*info));
   int kb = 0, nb = 0;
-  if (tc) {
+  if (tc || ga) {
     dw_tiles(K, N, &kb, &nb);
-    info->variant = 0;
+    info->variant = tc ? 0 : kVariantGather;
     info->rows_per_block = dw_stage_rows();
     info->k_per_block = 256;
     info->stages = dw_stages();
@@ -821,14 +895,15 @@ int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t 
   if (rc != PGG_OK) return rc;
   alignas(16) static const char probe[16] = {0};
   const bool tc = fwd_tensor_path(dtype, N, K, probe, probe, probe);
+  const bool ga = !tc && fwd_gather_path(dtype, N, K, probe, probe, probe);
   std::memset(info, 0, sizeof(*info));
   int nb = 0;
   info->rows_per_block = p.rows_per_block;
   info->max_row_blocks = p.max_row_blocks;
   info->workspace_bytes = p.layout.total;
-  if (tc) {
+  if (tc || ga) {
     fwd_tiles(N, &nb);
-    info->variant = 0;
+    info->variant = tc ? 0 : kVariantGather;
     info->k_per_block = 64;
     info->stages = fwd_stages();
     info->threads = fwd_threads();

@@ -101,7 +101,8 @@ constexpr int kMaxSlabTokens = 256;
 
 struct Plan {
   int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single
-                       // CTAs, 3 FP32-pipe kernel for rows the tensor-memory-access unit cannot stream
+                       // CTAs, 3 FP32-pipe kernel, 4 owner kernel, 5 variant 0 with operands
+                       // gathered by warps (rows the tensor-memory-access unit cannot stream)
   int pair;            // 1: CTA-pair tiles of 256 k
   int dtype;           // pgg_dtype
   int rows_per_block;  // MMA N extent
@@ -129,6 +130,9 @@ struct RowInfo {
 };
 
 struct GemmArgs {
+  const void* dy;         // [M, N] dtype (read directly by the gathered-operand variant)
+  const void* w;          // [G, K, N] dtype (read directly by the gathered-operand variant)
+  int64_t N;
   const int4* rblist;     // {expert, first row, rows, 0} per row block
   const RowInfo* rowinfo; // [M]
   uint32_t* tickets;      // [batch * k_blocks]
@@ -211,6 +215,9 @@ struct DwArgs {
   int32_t n_blocks;  // output column (n) blocks per expert
   int32_t out_f32;   // 1: out is fp32; 0: out has the input dtype
   int32_t dy_3d;     // tensor-core kernel: d_y map is 3-D {64 n, rows, n / 64} (N % 64 == 0)
+  int32_t gather_dy;  // tensor-core kernel: 1 = d_y rows copied by the gather warps (4-byte
+                      // cp.async) and the output written with 4-byte stores (N even, N * 2
+                      // not a multiple of 16); 0 = TMA for both
   uint64_t wait_limit_ns;
 };
 
@@ -226,6 +233,9 @@ struct FwdArgs {
   int64_t G, batch, max_row_blocks;  // bounds of the routing tables (checked build)
   int32_t n_blocks;  // output column blocks per row block
   int32_t out_f32;   // 1: y is fp32; 0: y has the input dtype
+  int32_t gather_w;  // tensor-core kernel: 1 = weight rows copied by the gather warps (4-byte
+                     // cp.async) and y written with 4-byte stores (N even, N * 2 not a
+                     // multiple of 16); 0 = TMA for both
   uint64_t wait_limit_ns;
 };
 

@@ -314,12 +314,20 @@ __host__ __device__ constexpr uint32_t idesc_make_mn(uint32_t ab_format, uint32_
   return idesc_make(ab_format, m, n) | (1u << 15) | (1u << 16);
 }
 
-// ------------------------------------------------------------------ cp.async (16 bytes)
+// ------------------------------------------------------------------ cp.async (16 and 4 bytes)
 
 // 16 bytes global -> shared; `src_bytes` (0 or 16) of them are read, the rest
 // are zero-filled.
 __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// 4 bytes global -> shared (both 4-byte aligned), through L1; `src_bytes` (0
+// or 4) of them are read, the rest are zero-filled.
+__device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src),
                "r"(src_bytes)
                : "memory");
 }

@@ -138,14 +138,28 @@ def test_status_strings(lib):
         assert pgg.pgg_status_string(code) != "unknown status", name
 
 
-def test_rows_the_tma_cannot_stream_take_the_fp32_pipe_kernel(lib):
+def test_rows_the_tma_cannot_stream_take_the_gather_warps_or_the_fp32_pipes(lib):
     # row bytes N * sizeof(dtype) not a multiple of 16 (the page's N = 1 and
-    # N = 286 white-box cases) plan the FP32-pipe kernel instead of an error
-    for n, dt in ((1, pgg.PGG_BF16), (286, pgg.PGG_BF16), (2047, pgg.PGG_F16), (6, pgg.PGG_F32),
+    # N = 286 white-box cases): 16-bit rows of an even length are copied by the
+    # gather warps of variant 5 (tensor cores); odd lengths and fp32 plan the
+    # FP32-pipe kernel; never an error
+    for n, dt in ((286, pgg.PGG_BF16), (2046, pgg.PGG_F16), (2, pgg.PGG_BF16)):
+        p = pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)
+        assert p["variant"] == 5 and p["rows_per_block"] == 256 and p["cta_pair"] == 1, (n, dt)
+        assert p["threads"] == 512 and p["smem_bytes"] <= 227 * 1024, (n, dt)
+    for n, dt in ((1, pgg.PGG_BF16), (287, pgg.PGG_BF16), (2047, pgg.PGG_F16), (6, pgg.PGG_F32),
                   (1, pgg.PGG_F32)):
         p = pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)
         assert p["variant"] == 3 and p["rows_per_block"] == 64 and p["threads"] == 128, (n, dt)
         assert p["cta_pair"] == 0 and p["smem_bytes"] <= 227 * 1024 // 3  # 3 CTAs per SM
+    # forcing variant 5 where it cannot copy the rows gives the FP32-pipe kernel
+    pgg.pgg_debug_force_variant(5)
+    try:
+        assert pgg.pgg_dx_plan(1280, 287, 178, 4, 1280, 640, 2, 0, pgg.PGG_BF16)["variant"] == 3
+        assert pgg.pgg_dx_plan(1280, 288, 178, 4, 1280, 640, 2, 0, pgg.PGG_F32)["variant"] == 3
+        assert pgg.pgg_dx_plan(1280, 288, 178, 4, 1280, 640, 2, 0, pgg.PGG_BF16)["variant"] == 5
+    finally:
+        pgg.pgg_debug_force_variant(-1)
     for n, dt in ((8, pgg.PGG_BF16), (4, pgg.PGG_F32), (280, pgg.PGG_F16)):
         assert pgg.pgg_dx_plan(1280, n, 178, 4, 1280, 640, 2, 0, dt)["variant"] != 3, (n, dt)
     # the workspace stays small at the pages' scale
@@ -162,6 +176,11 @@ def test_weight_gradient_plan_and_host_errors(lib):
     assert p["k_blocks"] == 28 and p["band_k_blocks"] == 8 and p["smem_bytes"] <= 227 * 1024
     assert pgg.pgg_dw_plan(*sizes, pgg.PGG_F32)["variant"] == 3
     assert pgg.pgg_dw_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
+                           pgg.PGG_BF16)["variant"] == 3
+    # d_y rows of 572 bytes, x rows of 384: d_y gathered by warps (variant 5)
+    assert pgg.pgg_dw_plan(a["M"], 286, 192, a["G"], a["L"], a["batch"], a["topK"], 0,
+                           pgg.PGG_BF16)["variant"] == 5
+    assert pgg.pgg_dw_plan(a["M"], 287, 192, a["G"], a["L"], a["batch"], a["topK"], 0,
                            pgg.PGG_BF16)["variant"] == 3
     assert pgg.pgg_dw_workspace_size(*sizes, pgg.PGG_BF16) == ws()
     fake = 1 << 20
@@ -188,6 +207,11 @@ def test_forward_plan_and_host_errors(lib):
     assert p["smem_bytes"] <= 227 * 1024
     assert pgg.pgg_fwd_plan(*sizes, pgg.PGG_F32)["variant"] == 3
     assert pgg.pgg_fwd_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
+                            pgg.PGG_BF16)["variant"] == 3
+    # weight and y rows of 572 bytes, x rows of 384: weight gathered by warps (variant 5)
+    assert pgg.pgg_fwd_plan(a["M"], 286, 192, a["G"], a["L"], a["batch"], a["topK"], 0,
+                            pgg.PGG_BF16)["variant"] == 5
+    assert pgg.pgg_fwd_plan(a["M"], 287, 192, a["G"], a["L"], a["batch"], a["topK"], 0,
                             pgg.PGG_BF16)["variant"] == 3
     need = pgg.pgg_fwd_workspace_size(*sizes, pgg.PGG_BF16)
     assert need <= 16 * 2**20

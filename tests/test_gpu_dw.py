@@ -248,3 +248,46 @@ def test_random_shapes(case):
     x = forward_input(inp)
     got = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
     assert_close(got, ref_of(inp, x), what=str(case))
+
+
+# ---------------------------------------------------------------- rows the TMA cannot stream
+
+def _plan(inp):
+    M, N = inp.grad_y.shape
+    G, K, _ = inp.weight.shape
+    return pgg.pgg_dw_plan(M, N, K, G, M, inp.batch, inp.top_k, inp.row_idx_type,
+                           pgg.dtype_code(inp.grad_y.dtype))["variant"]
+
+
+@pytest.mark.parametrize("n", [2, 6, 286, 1022])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_unaligned_dy_rows_on_the_tensor_cores(n, dtype, out_f32):
+    # d_y and d_weight rows of N * 2 bytes (N even, not a multiple of 8): the
+    # gather warps copy the d_y panels 4 bytes at a time (plan variant 5); the
+    # empty experts of the Zipf routing get zeros through 4-byte stores
+    inp = make_case(batch=400, top_k=4, G=9, K=320, N=n, dtype=dtype, routing="zipf",
+                    zipf_zero=2, seed=27, device="cuda")
+    assert _plan(inp) == 5
+    x = forward_input(inp)
+    out = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert_close(out, ref_of(inp, x), f"N={n}")
+    again = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_four_byte_aligned_dy_and_output_equal_the_tma_path_bitwise(out_f32):
+    inp = make_case(batch=300, top_k=4, G=6, K=256, N=320, dtype="bf16", seed=28,
+                    routing="zipf", zipf_zero=1, device="cuda")
+    x = forward_input(inp)
+    od = torch.float32 if out_f32 else torch.bfloat16
+    want = run(inp, x, out_dtype=od)
+    G, K, N = want.shape
+    obuf = torch.empty(G * K * N + 2, dtype=od, device="cuda")
+    o = obuf[(1 if out_f32 else 2):][:G * K * N].view(G, K, N)
+    got, ws = pgg.dw(x, _shifted(inp.grad_y, 2), inp.expanded_row_idx, inp.group_list,
+                     inp.batch, inp.top_k, inp.row_idx_type, out_dtype=od, out=o)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))

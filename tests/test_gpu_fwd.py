@@ -230,3 +230,46 @@ def test_random_shapes(case):
     x = forward_input(inp)
     got = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
     assert_close(got, ref_of(inp, x), what=str(case))
+
+
+# ---------------------------------------------------------------- rows the TMA cannot stream
+
+def _plan(inp):
+    M, N = inp.grad_y.shape
+    G, K, _ = inp.weight.shape
+    return pgg.pgg_fwd_plan(M, N, K, G, M, inp.batch, inp.top_k, inp.row_idx_type,
+                            pgg.dtype_code(inp.grad_y.dtype))["variant"]
+
+
+@pytest.mark.parametrize("n", [2, 6, 286, 1022])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_unaligned_weight_rows_on_the_tensor_cores(n, dtype, out_f32):
+    # weight and y rows of N * 2 bytes (N even, not a multiple of 8): the gather
+    # warps copy the weight panels 4 bytes at a time (plan variant 5)
+    inp = make_case(batch=400, top_k=4, G=9, K=320, N=n, dtype=dtype, routing="zipf",
+                    zipf_zero=2, seed=38, device="cuda")
+    assert _plan(inp) == 5
+    x = forward_input(inp)
+    y = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert_close(y, ref_of(inp, x), f"N={n}")
+    again = run(inp, x, out_dtype=torch.float32 if out_f32 else None)
+    assert torch.equal(y.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_four_byte_aligned_weight_and_y_equal_the_tma_path_bitwise(out_f32):
+    # weight / y 4-byte but not 16-byte aligned: the gathered weight panels and
+    # the 4-byte stores give the bits of the TMA path
+    inp = make_case(batch=300, top_k=4, G=6, K=256, N=320, dtype="bf16", seed=39, device="cuda")
+    x = forward_input(inp)
+    od = torch.float32 if out_f32 else torch.bfloat16
+    want = run(inp, x, out_dtype=od)
+    M, N = want.shape
+    ybuf = torch.empty(M * N + 2, dtype=od, device="cuda")
+    y = ybuf[(1 if out_f32 else 2):][:M * N].view(M, N)
+    got, ws = pgg.fwd(x, _shifted(inp.weight, 2), inp.expanded_row_idx, inp.group_list,
+                      inp.batch, inp.top_k, 0, out_dtype=od, out=y)
+    torch.cuda.synchronize()
+    assert pgg.status(ws) == 0
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))

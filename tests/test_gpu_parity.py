@@ -99,11 +99,11 @@ def test_large_m_white_box(dtype):
     check(inp, tokens=toks, what="large M")
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 5])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 def test_multi_tile_ragged(dtype, variant):
-    if dtype == "fp32" and variant == 2:
-        pytest.skip("variant 2 exists for 16-bit inputs only")
+    if dtype == "fp32" and variant in (2, 5):
+        pytest.skip("variants 2 and 5 exist for 16-bit inputs only")
     # several k blocks with a ragged tail, a ragged reduction tail, groups of
     # 0 .. several hundred rows
     pgg.pgg_debug_force_variant(variant)
@@ -120,7 +120,7 @@ def test_multi_tile_ragged(dtype, variant):
 def test_same_expert_twice_for_a_token(dtype):
     # degenerate routing: rows of one token inside one tile must still be
     # added in order (no deadlock, correct sum)
-    for variant in ((0, 1, 2, 3) if dtype != "fp32" else (0, 1, 3)):
+    for variant in ((0, 1, 2, 3, 5) if dtype != "fp32" else (0, 1, 3)):
         pgg.pgg_debug_force_variant(variant)
         try:
             inp = make_case(batch=200, top_k=4, G=3, K=384, N=128, dtype=dtype,
@@ -162,13 +162,15 @@ def test_variants_agree():
     ref = ref_rows(inp)
     outs = []
     try:
-        for variant in (0, 1, 2, 3):
+        for variant in (0, 1, 2, 3, 5):
             pgg.pgg_debug_force_variant(variant)
             out, _ = run(inp)
             outs.append(out)
             assert_close(out.double().cpu().numpy(), ref, f"variant {variant}")
     finally:
         pgg.pgg_debug_force_variant(-1)
+    # the gathered operands are those the tensor-memory-access unit loads
+    assert torch.equal(outs[0].view(torch.int32), outs[4].view(torch.int32))
 
 
 @pytest.mark.parametrize("n", [192, 190])
@@ -236,7 +238,7 @@ def test_device_detected_errors_zero_the_output(n):
     check(base, what="after errors")
 
 
-@pytest.mark.parametrize("n", [128, 127])
+@pytest.mark.parametrize("n", [128, 127, 126])
 def test_bounded_wait_reports_timeout_and_recovers(n):
     inp = make_case(batch=256, top_k=4, G=8, K=256, N=n, dtype="bf16", seed=10,
                     device="cuda")
@@ -269,13 +271,21 @@ def test_no_writes_outside_out_and_workspace():
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 def test_unaligned_rows_many_tiles(dtype):
-    # rows of 2 * 1030 (or 4 * 1031) bytes: the FP32-pipe kernel over many row
-    # blocks, k blocks with a ragged tail, and a ragged reduction tail
+    # rows of 2 * 1030 (or 4 * 1031) bytes over many row blocks, k blocks with
+    # a ragged tail, and a ragged reduction tail: 16-bit rows on the gather
+    # warps of variant 5, fp32 rows on the FP32-pipe kernel; then 16-bit rows
+    # of an odd length (2 * 1031 bytes), also on the FP32 pipes
     n = 1031 if dtype == "fp32" else 1030
     inp = make_case(batch=1000, top_k=4, G=9, K=300, N=n, dtype=dtype, routing="zipf",
                     zipf_zero=2, seed=12, device="cuda")
-    assert pgg.pgg_dx_plan(*_sizes(inp), 0, pgg.dtype_code(inp.grad_y.dtype))["variant"] == 3
+    want = 3 if dtype == "fp32" else 5
+    assert pgg.pgg_dx_plan(*_sizes(inp), 0, pgg.dtype_code(inp.grad_y.dtype))["variant"] == want
     check(inp, what=f"unaligned rows {dtype}")
+    if dtype != "fp32":
+        inp = make_case(batch=1000, top_k=4, G=9, K=300, N=1031, dtype=dtype, routing="zipf",
+                        zipf_zero=2, seed=12, device="cuda")
+        assert pgg.pgg_dx_plan(*_sizes(inp), 0, pgg.dtype_code(inp.grad_y.dtype))["variant"] == 3
+        check(inp, what=f"odd rows {dtype}")
 
 
 def _sizes(inp):
