@@ -154,8 +154,12 @@ def _shifted(t, elems):
 
 
 def test_misaligned_pointers_take_the_fp32_pipes():
+    # x 2-byte aligned: the FP32-pipe kernel, whose result does not depend on
+    # the addresses; an output that is 4-byte but not 16-byte aligned: the
+    # tensor cores with 4-byte stores, bitwise equal to the aligned run
     inp = make_case(batch=300, top_k=4, G=6, K=256, N=256, dtype="bf16", seed=25, device="cuda")
     x = forward_input(inp)
+    tc = run(inp, x, out_dtype=torch.float32)
     try:
         pgg.pgg_debug_force_variant(3)
         simt = run(inp, x, out_dtype=torch.float32)
@@ -172,7 +176,7 @@ def test_misaligned_pointers_take_the_fp32_pipes():
                    out_dtype=torch.float32, out=o)
     torch.cuda.synchronize()
     assert pgg.status(ws) == 0
-    assert torch.equal(o.view(torch.int32), simt.view(torch.int32))
+    assert torch.equal(o.view(torch.int32), tc.view(torch.int32))
 
 
 def test_device_detected_errors_zero_the_output():
