@@ -56,14 +56,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace bytes"
 _COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh"]
 # grouped-GEMM kernel -> the sources its ncu counters depend on
+_GATHER = "permute_grouped_gemm_gb300/csrc/pgg_gather.cuh"
 KERNEL_SOURCES = {
-    "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", *_COMMON],
+    "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", _GATHER, *_COMMON],
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
     "gmm_dx_owner_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_owner.cu", *_COMMON],
     "unpermute_grad_kernel": ["permute_grouped_gemm_gb300/csrc/unpermute_grad.cu"],
-    "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", *_COMMON],
+    "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", _GATHER, *_COMMON],
     "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],
-    "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", *_COMMON],
+    "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", _GATHER, *_COMMON],
     "gmm_fwd_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd_simt.cu", *_COMMON],
 }
 SIMT_VARIANT = 3

@@ -46,6 +46,7 @@
 
 #include <cstdint>
 
+#include "pgg_gather.cuh"
 #include "pgg_internal.h"
 #include "pgg_ptx.cuh"
 
@@ -275,27 +276,19 @@ __device__ void x_gatherer(uint8_t* smem, DwCtl* ctl, const DwArgs& a, uint32_t 
     }
     if (a.gather_dy) {
       // the d_y panels: the stage's 64 rows of the expert, this CTA's 128 n,
-      // 4 bytes (two n) per lane, zeros past the expert's rows and past N
+      // copied as wide as each row's alignment allows, zeros past the
+      // expert's rows and past N
       const char* yb = static_cast<const char*>(a.dy);
-      const int64_t left = cur.x.m - cur.r;
-      const int64_t nrows = left < kDwRows ? left : kDwRows;
-      const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;
-      const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
-      const int64_t row_bytes = a.N * 2;
+      const int64_t rows_left = cur.x.m - cur.r;
+      const int nrows = rows_left < kDwRows ? static_cast<int>(rows_left) : kDwRows;
       const uint32_t sb_slot = ptx::smem_addr(smem + w * kStageBytes) + kABytes;
-#pragma unroll
+#pragma unroll 1
       for (int p = 0; p < 2; ++p) {
-        const int64_t n = cur.x.n0 + 128 * rank + 64 * p + 2 * lane;
-        const bool n_ok = n < a.N;  // N is even: n and n + 1 are both in or both out
-        const char* src = yb + ((cur.x.row0 + cur.r) * a.N + n) * 2;
-#pragma unroll 4
-        for (int r = 0; r < kDwRows; ++r) {
-          const bool ok = n_ok && r < nrows;
-          ptx::cp_async_4(sb_slot + p * kPanel + r * 128 + (((chunk ^ (r & 7)) << 4) | piece),
-                          ok ? static_cast<const void*>(src + r * row_bytes)
-                             : static_cast<const void*>(yb),
-                          ok ? 4u : 0u);
-        }
+        const int64_t n = cur.x.n0 + 128 * rank + 64 * p;
+        const int64_t left = (a.N - n) * 2;
+        const int seg = left < 0 ? 0 : (left < 128 ? static_cast<int>(left) : 128);
+        gather_rows_sw128(sb_slot + p * kPanel, yb + ((cur.x.row0 + cur.r) * a.N + n) * 2,
+                          a.N * 2, kDwRows, nrows, seg, a.hdr, lane, 0, 1);
       }
     }
     ptx::cp_async_commit();

@@ -53,6 +53,7 @@
 
 #include <cstdint>
 
+#include "pgg_gather.cuh"
 #include "pgg_internal.h"
 #include "pgg_ptx.cuh"
 
@@ -107,9 +108,10 @@ struct Cfg {
   static constexpr int kEpiGroups = kSplit ? 1 : 2;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kXformWarps = kSplit ? 4 : 0;
-  // Gathered operands: one warp per stage slot copies the slot's rows with
-  // 4-byte cp.async (rows whose byte length is not a multiple of 16).
-  static constexpr int kGatherWarps = GATHER ? STAGES : 0;
+  // Gathered operands: two warps per stage slot copy the slot's rows with
+  // cp.async (rows whose byte length is not a multiple of 16).
+  static constexpr int kWarpsPerSlot = 2;
+  static constexpr int kGatherWarps = GATHER ? kWarpsPerSlot * STAGES : 0;
   static constexpr int kGatherWarp0 = 2 + kEpiWarps + kXformWarps;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kXformWarps + kGatherWarps);
   static constexpr int kMmaM = PAIR ? 2 * kKBlock : kKBlock;
@@ -527,16 +529,16 @@ __device__ void transformer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArg
   }
 }
 
-// Gather warp of stage slot `slot` (gathered-operand kernel, rows of N * 2
-// bytes that are 4-byte but not 16-byte multiples): for each descriptor the
-// scheduler posts to the slot, it copies the slot's 128 weight rows and `fill`
-// d_y rows, one 128-byte row segment (64 n) per warp instruction, 4 bytes per
-// lane, with cp.async into the layout the tensor-memory-access unit would
-// have written (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)
-// of the row's 128 bytes, rows 128 bytes apart), zero-filling rows and
-// columns outside the operands. Then it waits for its copies, makes them
-// visible to the tensor cores and arrives on the slot's full barrier (the even
-// CTA's, for a pair).
+// Gather warps of stage slot `slot` (gathered-operand kernel, rows of N * 2
+// bytes that are 4-byte but not 16-byte multiples), two per slot: for each
+// descriptor the scheduler posts to the slot, they copy the slot's 128 weight
+// rows and `fill` d_y rows, 128-byte row segments (64 n) with cp.async as wide
+// as each row's alignment allows, into the layout the tensor-memory-access
+// unit would have written (128-byte swizzle: 16-byte chunk c of row r at chunk
+// c ^ (r % 8) of the row's 128 bytes, rows 128 bytes apart), zero-filling rows
+// and columns outside the operands. Each warp then waits for its copies, makes
+// them visible to the tensor cores and arrives on the slot's full barrier (the
+// even CTA's, for a pair).
 template <int DT, int ROWS, int STAGES, bool PAIR>
 __device__ void gatherer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArgs& args) {
   using C = Cfg<DT, ROWS, STAGES, PAIR, true>;
@@ -546,14 +548,14 @@ __device__ void gatherer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArgs& 
                 "the gathered operands fill the stages of the TMA variant");
   const uint64_t lim = args.wait_limit_ns;
   volatile int* abort = &ctl->abort;
-  const int slot = (threadIdx.x >> 5) - C::kGatherWarp0;
+  const int gw = (threadIdx.x >> 5) - C::kGatherWarp0;
+  const int slot = gw / C::kWarpsPerSlot, part = gw % C::kWarpsPerSlot;
   const int lane = threadIdx.x & 31;
   const uint32_t sa = ptx::smem_addr(smem + slot * C::kStageBytes);
   const uint32_t sb = sa + C::kABytes;
-  const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;  // bytes within the chunk
-  const uint32_t chunk = static_cast<uint32_t>(lane >> 2);      // 16-byte chunk of the row
   const char* wb = static_cast<const char*>(args.w);
   const char* yb = static_cast<const char*>(args.dy);
+  const void* safe = args.hdr;  // 64-byte aligned, named by zero-filling copies only
   const int64_t N = args.N, K = args.K;
   const int64_t row_bytes = N * 2;
   uint32_t full = 0;
@@ -569,24 +571,15 @@ __device__ void gatherer(uint8_t* smem, Ctl<ROWS, STAGES>* ctl, const GemmArgs& 
     }
     const GatherDesc d = ctl->desc[slot];
     if (d.g < 0) break;
-    const int64_t n = static_cast<int64_t>(d.n0) + 2 * lane;
-    const bool n_ok = n < N;  // N is even: the pair n, n + 1 is all in or all out
+    const int64_t left = (N - d.n0) * 2;  // bytes of the row segment inside N
+    const int seg = left < 0 ? 0 : (left < kRowBytes ? static_cast<int>(left) : kRowBytes);
     const int64_t k0 = static_cast<int64_t>(d.kb) * kKBlock;
     const int64_t kn = K - k0 < kKBlock ? K - k0 : kKBlock;  // weight rows inside K
-    const char* src = wb + ((static_cast<int64_t>(d.g) * K + k0) * N + n) * 2;
-#pragma unroll 4
-    for (int r = 0; r < kKBlock; ++r) {
-      const bool ok = n_ok && r < kn;
-      const uint32_t dst = sa + r * kRowBytes + (((chunk ^ (r & 7)) << 4) | piece);
-      ptx::cp_async_4(dst, ok ? src + r * row_bytes : wb, ok ? 4u : 0u);
-    }
-    const char* ysrc = yb + (static_cast<int64_t>(d.row) * N + n) * 2;
-#pragma unroll 4
-    for (int r = 0; r < d.fill; ++r) {
-      const bool ok = n_ok && r < d.valid;
-      const uint32_t dst = sb + r * kRowBytes + (((chunk ^ (r & 7)) << 4) | piece);
-      ptx::cp_async_4(dst, ok ? ysrc + r * row_bytes : yb, ok ? 4u : 0u);
-    }
+    gather_rows_sw128(sa, wb + ((static_cast<int64_t>(d.g) * K + k0) * N + d.n0) * 2, row_bytes,
+                      kKBlock, kn < 0 ? 0 : static_cast<int>(kn), seg, safe, lane, part,
+                      C::kWarpsPerSlot);
+    gather_rows_sw128(sb, yb + (static_cast<int64_t>(d.row) * N + d.n0) * 2, row_bytes, d.fill,
+                      d.valid, seg, safe, lane, part, C::kWarpsPerSlot);
     ptx::cp_async_commit();
     ptx::cp_async_wait<0>();
     ptx::fence_proxy_async_smem();
@@ -879,8 +872,8 @@ __global__ void __launch_bounds__(Cfg<DT, ROWS, STAGES, PAIR, GATHER>::kThreads,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // gathered operands: one arrival from the slot's gather warp in each CTA
-      ptx::mbar_init(&ctl->full[s], GATHER ? (PAIR ? 2 : 1) : 1);
+      // gathered operands: one arrival from each gather warp of the slot, in each CTA
+      ptx::mbar_init(&ctl->full[s], GATHER ? C::kWarpsPerSlot * (PAIR ? 2 : 1) : 1);
       ptx::mbar_init(&ctl->empty[s], 1);
       ptx::mbar_init(&ctl->ready[s], 1);
       ptx::mbar_init(&ctl->dfull[s], 1);

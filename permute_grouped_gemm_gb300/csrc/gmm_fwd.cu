@@ -39,6 +39,7 @@
 
 #include <cstdint>
 
+#include "pgg_gather.cuh"
 #include "pgg_internal.h"
 #include "pgg_ptx.cuh"
 
@@ -219,27 +220,19 @@ __device__ void x_gatherer(uint8_t* smem, FwdCtl* ctl, const FwdArgs& a, uint32_
     }
     if (a.gather_w) {
       // the weight panels: k rows kb * 64 .. + 63 of expert g, this CTA's 128
-      // n from nc, 4 bytes (two n) per lane, zeros outside K and N
+      // n from x.n0 + 128 rank, copied as wide as each row's alignment allows,
+      // zeros outside K and N
       const char* wb = static_cast<const char*>(a.w);
       const int64_t k0 = static_cast<int64_t>(kb) * kFK;
       const int64_t kn = a.K - k0 < kFK ? a.K - k0 : kFK;
-      const uint32_t piece = static_cast<uint32_t>(lane & 3) << 2;
-      const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
-      const int64_t row_bytes = a.N * 2;
-#pragma unroll
+#pragma unroll 1
       for (int p = 0; p < 2; ++p) {
-        const int64_t n = x.n0 + 128 * rank + 64 * p + 2 * lane;
-        const bool n_ok = n < a.N;  // N is even: n and n + 1 are both in or both out
-        const char* src = wb + ((x.g * a.K + k0) * a.N + n) * 2;
-        const uint32_t dst0 = sa_slot + kABytes + p * kPanel;
-#pragma unroll 4
-        for (int r = 0; r < kFK; ++r) {
-          const bool ok = n_ok && r < kn;
-          ptx::cp_async_4(dst0 + r * 128 + (((chunk ^ (r & 7)) << 4) | piece),
-                          ok ? static_cast<const void*>(src + r * row_bytes)
-                             : static_cast<const void*>(wb),
-                          ok ? 4u : 0u);
-        }
+        const int64_t n = x.n0 + 128 * rank + 64 * p;
+        const int64_t left = (a.N - n) * 2;
+        const int seg = left < 0 ? 0 : (left < 128 ? static_cast<int>(left) : 128);
+        gather_rows_sw128(sa_slot + kABytes + p * kPanel, wb + ((x.g * a.K + k0) * a.N + n) * 2,
+                          a.N * 2, kFK, kn < 0 ? 0 : static_cast<int>(kn), seg, a.hdr, lane, 0,
+                          1);
       }
     }
     ptx::cp_async_commit();
