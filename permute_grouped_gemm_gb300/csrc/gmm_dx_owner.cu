@@ -103,15 +103,20 @@ __device__ __forceinline__ int mma_n(int R) {
 // the next expert are loaded one expert ahead, so that moving on does not wait
 // for memory.
 struct ChunkIt {
-  const OwnerArgs* a;
+  // the parameters it needs, copied into registers once (reading them through
+  // a pointer to the kernel's parameters costs a memory round trip each time)
+  const int32_t* seg;
+  WsHeader* hdr;
+  int64_t G, M;
+  int32_t ns1;  // n_slabs + 1: row length of seg
   int64_t s;
   int64_t g, r0, r_end;
   int64_t ng;          // next expert, its bounds in flight
   int32_t nlo, nhi;
   __device__ void load_next() {
     ng = g + 1;
-    if (ng < a->G) {
-      const int32_t* row = a->seg + ng * (a->n_slabs + 1);
+    if (ng < G) {
+      const int32_t* row = seg + ng * ns1;
       nlo = row[s];
       nhi = row[s + 1];
     }
@@ -119,24 +124,28 @@ struct ChunkIt {
   __device__ void next_expert() {
     while (true) {
       g = ng;
-      if (g >= a->G) return;
+      if (g >= G) return;
       r0 = nlo;
       r_end = nhi;
       // checked build: bounds outside the expanded rows make the range empty
-      if (!check_ok(a->hdr, 0 <= r0 && r0 <= r_end && r_end <= a->M, 30)) r0 = r_end = 0;
+      if (!check_ok(hdr, 0 <= r0 && r0 <= r_end && r_end <= M, 30)) r0 = r_end = 0;
       load_next();
       if (r0 < r_end) return;
     }
   }
   __device__ void start(const OwnerArgs* args, int64_t slab) {
-    a = args;
+    seg = args->seg;
+    hdr = args->hdr;
+    G = args->G;
+    M = args->M;
+    ns1 = args->n_slabs + 1;
     s = slab;
     g = -1;
     r0 = r_end = 0;
     load_next();
     next_expert();
   }
-  __device__ bool valid() const { return g < a->G; }
+  __device__ bool valid() const { return g < G; }
   __device__ int rows() const {
     const int64_t left = r_end - r0;
     return static_cast<int>(left < kMaxRows ? left : kMaxRows);
