@@ -2,7 +2,7 @@
 // design", section "数学定义和公式": d_x[b, k] = sum over the token's rows i of
 // sum_n d_y[i, n] * weight[g(i), k, n]), for problems with few experts.
 //
-// A CTA pair owns a block of d_x outright: a slab of T tokens (T <= 256, set
+// A CTA pair owns a block of d_x outright: a slab of T tokens (T <= 224, set
 // by the host so that a slab holds about 112 rows of each expert) x 256 k
 // (128 per CTA). It walks the experts in increasing order; for each expert it
 // takes the expert's rows whose tokens lie in the slab (one contiguous range
@@ -17,21 +17,29 @@
 // reads, adds and writes that column, in program order, in increasing expanded index
 // (increasing expert, then increasing row within the expert), which is the
 // order of additions of the ticketed kernel, with no tickets, no barriers
-// between threads and no atomics. A token's first row (rank 0) stores, later
-// rows load, add and store; two rows of one token inside one expert are
-// adjacent and carried in a register. When the slab is done each thread
-// writes its column to d_x once.
+// between threads and no atomics. The slab block starts as -0.0, so every
+// row loads, adds and stores (a token's first row gives -0 + x == x); two
+// rows of one token inside one expert are adjacent and carried in a
+// register. When the slab is done each thread writes its column to d_x once.
 //
 // When some expert's rows are not in increasing original position the kernel
 // leaves at once and the ticketed kernel, launched after it, does the work.
 //
 // Pipeline stages: when N is a multiple of 64, each stage covers 128 n as two
 // 64-n panels, loaded by one 4-D weight copy and one 3-D d_y copy (4 stages);
-// otherwise 64 n (8 stages). Warp roles per CTA: 0 TMA; 1 tensor-memory
-// allocation and (even CTA) MMA issue; 2-5 epilogue. Units (slab, k range) are statically interleaved over
-// the clusters. Waits are bounded; when one runs out the kernel records
-// PGG_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
-// returns.
+// otherwise 64 n (8 stages). The chunks alternate between two pipelines, one
+// per accumulator, each with its own TMA thread, MMA-issuing thread and half
+// of the stages: an MMA-issuing thread leaves the tensor pipe idle while it
+// waits on a barrier or commits (a few hundred cycles each time), and at
+// N <= 128 its eight MMAs per stage do not cover that, so the other
+// pipeline's MMAs fill the gap. Each accumulator still receives its MMAs from
+// one thread in a fixed order, and the epilogue takes the chunks in order, so
+// the results do not depend on how the two interleave. Warp roles per CTA: 0
+// and 1 TMA (pipeline 0 and 1); 2 and 3 (even CTA) MMA issue, warp 2 also
+// tensor-memory allocation; 4-7 epilogue. Units (slab, k range) are
+// statically interleaved over the clusters. Waits are bounded; when one runs
+// out the kernel records PGG_ERR_TIMEOUT, drains its copies and MMAs, frees
+// tensor memory and returns.
 
 #include <cstdint>
 
@@ -54,24 +62,28 @@ struct Geo {
   static constexpr int kA = kPanels * kABytes;
   static constexpr int kStageBytes = kPanels * (kABytes + kBBytes);
   static constexpr int kStages = WIDE ? 4 : kMaxStages;
+  static constexpr int kRing = kStages / 2;  // stages of each pipeline
 };
 
 // Write-out staging: per epilogue warp two buffers of 32 tokens x 32 k fp32,
 // stored to d_x by TMA.
 constexpr int kOutBuf = 32 * 32;  // floats
 constexpr int kOutBytes = 4 * 2 * kOutBuf * 4;
-constexpr int kThreads = 32 * 6;
+constexpr int kThreads = 32 * 8;
+constexpr int kEpiWarp0 = 4;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 128;              // per MMA accumulator
 constexpr int kSlabCol = 2 * kAccCols;     // the slab block: columns 256 .. 256 + T
+constexpr int kScratchTok = 255;           // column kSlabCol + 255: padding rows' scratch
 static_assert(kSlabCol + kMaxSlabTokens <= kTmemCols, "tensor memory columns");
+static_assert(kMaxSlabTokens <= kScratchTok, "the scratch column lies past every slab");
 
 struct OwnCtl {
-  uint64_t full[kMaxStages];
+  uint64_t full[kMaxStages];  // pipeline p uses stages p * kRing .. p * kRing + kRing - 1
   uint64_t empty[kMaxStages];
-  uint64_t tfull[2];
+  uint64_t tfull[2];          // per accumulator = per pipeline
   uint64_t tempty[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -156,21 +168,26 @@ struct ChunkIt {
   }
 };
 
+// TMA thread of pipeline `pipe`: the operands of every other chunk (those of
+// parity `pipe`), into the pipeline's stages.
 template <bool WIDE>
 __device__ void producer(uint8_t* smem, OwnCtl* ctl, const OwnerMaps* m, const OwnerArgs& a,
-                         uint32_t n_units, uint32_t rank) {
+                         uint32_t n_units, uint32_t rank, int pipe) {
   using Gm = Geo<WIDE>;
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const bool leader = rank == 0;
-  int stage = 0;
+  const int s0 = pipe * Gm::kRing;
+  int stage = s0;
   uint32_t phase = 0, outstanding = 0, last_parity = 0;
+  uint32_t parity = 0;  // of the chunk index
   bool failed = false;
   for (uint32_t u = cluster_id(); u < n_units && !failed; u += n_clusters()) {
     const int64_t slab = u / a.k_units;
     const int32_t k0 = static_cast<int32_t>((u % a.k_units) * 2 * kOK + kOK * rank);
     ChunkIt c;
-    for (c.start(&a, slab); c.valid() && !failed; c.next()) {
+    for (c.start(&a, slab); c.valid() && !failed; c.next(), parity ^= 1u) {
+      if (parity != static_cast<uint32_t>(pipe)) continue;
       const int nm = mma_n<WIDE>(c.rows());
       const int half = nm / 2;  // this CTA's rows: a multiple of 8 (WIDE) or 16, at most 64
       // wide stages load whole 64-row boxes (the MMA reads the first half rows)
@@ -202,8 +219,8 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const OwnerMaps* m, const O
         }
         outstanding |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == Gm::kStages) {
-          stage = 0;
+        if (++stage == s0 + Gm::kRing) {
+          stage = s0;
           phase ^= 1u;
         }
       }
@@ -215,28 +232,36 @@ __device__ void producer(uint8_t* smem, OwnCtl* ctl, const OwnerMaps* m, const O
   }
   if (leader) {
     int no_abort = 0;
-    for (int s = 0; s < Gm::kStages; ++s)
+    for (int s = s0; s < s0 + Gm::kRing; ++s)
       if (outstanding & (1u << s))
         ptx::mbar_wait_cluster(&ctl->full[s], (last_parity >> s) & 1u, lim, &no_abort);
   }
 }
 
+// MMA-issuing thread of pipeline `pipe` (even CTA): every other chunk (those
+// of parity `pipe`), into accumulator `pipe`.
 template <int DT, bool WIDE>
 __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const OwnerArgs& a,
-                           uint32_t n_units) {
+                           uint32_t n_units, int pipe) {
   using Gm = Geo<WIDE>;
   constexpr uint32_t kFmt = DT == PGG_BF16 ? 1u : 0u;
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
-  int stage = 0, acc = 0;
+  const int s0 = pipe * Gm::kRing;
+  const int acc = pipe;
+  int stage = s0;
   uint32_t phase = 0, aph = 0;
+  uint32_t parity = 0;  // of the chunk index
   bool issued = false, failed = false;
   for (uint32_t u = cluster_id(); u < n_units && !failed; u += n_clusters()) {
     ChunkIt c;
-    for (c.start(&a, u / a.k_units); c.valid() && !failed; c.next()) {
+    for (c.start(&a, u / a.k_units); c.valid() && !failed; c.next(), parity ^= 1u) {
+      if (parity != static_cast<uint32_t>(pipe)) continue;
       const uint32_t idesc =
           ptx::idesc_make(kFmt, 2 * kOK, static_cast<uint32_t>(mma_n<WIDE>(c.rows())));
-      if (!ptx::mbar_wait_cluster(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
+      // (tensor memory changes hands through the tcgen05 fences around this
+      // wait and the epilogue's arrivals: a CTA-scope wait suffices)
+      if (!ptx::mbar_wait(&ctl->tempty[acc], aph ^ 1u, lim, abort)) {
         failed = true;
         break;
       }
@@ -261,15 +286,14 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
         }
         issued = true;
         ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
-        if (++stage == Gm::kStages) {
-          stage = 0;
+        if (++stage == s0 + Gm::kRing) {
+          stage = s0;
           phase ^= 1u;
         }
       }
       if (failed) break;
       ptx::mma_commit_pair(&ctl->tfull[acc], 0x3);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
+      aph ^= 1u;
     }
   }
   if (failed) {
@@ -278,21 +302,43 @@ __device__ void mma_issuer(uint8_t* smem, OwnCtl* ctl, uint32_t tmem_base, const
   }
   if (issued) {
     int no_abort = 0;
-    ptx::mma_commit_pair(&ctl->drain, 0x1);
-    ptx::mbar_wait(&ctl->drain, 0u, lim, &no_abort);
+    ptx::mma_commit_pair(&ctl->drain[pipe], 0x1);
+    ptx::mbar_wait(&ctl->drain[pipe], 0u, lim, &no_abort);
   }
 }
 
 // Row flags of the epilogue: bits 0-7 the token within the slab.
-constexpr int kRowPad = 1 << 8;    // no row (past the chunk's end)
-constexpr int kRowFirst = 1 << 9;  // the token's first row: store, no load
+constexpr int kRowPad = 1 << 8;    // no row (past the chunk's end): token kScratchTok
 constexpr int kRowDup = 1 << 10;   // same token as the row before, in this batch: carry
 
-// Tensor-memory column that row j of a batch reads and writes: its token's
-// slab column, or for a padding row its own accumulator column (already read,
-// and cleared by the next MMA into that accumulator).
-__device__ __forceinline__ uint32_t row_col(int row, uint32_t own) {
-  return (row & kRowPad) ? own : static_cast<uint32_t>(kSlabCol + (row & 0xFF));
+// Row records of a chunk's rows: lane j of ri[b] gets row 32 b + j (token -1
+// past the chunk's end).
+__device__ __forceinline__ void load_rows(const ChunkIt& c, const OwnerArgs& a, int lane,
+                                          RowInfo (&ri)[kMaxRows / 32]) {
+  const int R = c.rows();
+#pragma unroll
+  for (int b = 0; b < kMaxRows / 32; ++b) {
+    const int r = 32 * b + lane;
+    ri[b] = r < R ? a.rowinfo[check_index(a.hdr, c.r0 + r, a.M, 31)] : RowInfo{-1, 0};
+  }
+}
+
+// 32 lanes x 32 columns of tensor memory set to x.
+__device__ __forceinline__ void tmem_fill_32x32b_x32(uint32_t taddr, uint32_t x) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1,"
+      " %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(
+          taddr),
+      "r"(x)
+      : "memory");
+}
+
+// Arrival on the accumulator's barrier in the even CTA, CTA-scope: what
+// changes hands is tensor memory, ordered by the tcgen05 fences around the
+// barrier, not generic memory (a cluster-scope release costs ~1,800 cycles
+// here).
+__device__ __forceinline__ void arrive_acc_free(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Epilogue warp q (of 4) owns tensor-memory lanes 32 q .. 32 q + 31: one d_x
@@ -316,27 +362,35 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
     const int64_t tok0 = slab * T;
     const int64_t k =
         static_cast<int64_t>(u % a.k_units) * 2 * kOK + kOK * rank + 32 * quarter + lane;
+    // The slab block starts as -0.0 in every column, so that a token's first
+    // row is added like the others (-0 + x == x for every x).
+    for (int t0 = 0; t0 < T; t0 += 32)
+      tmem_fill_32x32b_x32(t_lane + kSlabCol + static_cast<uint32_t>(t0), 0x80000000u);
+    ptx::tmem_st_wait();
     ChunkIt c;
-    for (c.start(&a, slab); c.valid(); c.next()) {
+    c.start(&a, slab);
+    // the row records of each chunk are loaded while the chunk before it is
+    // added (they do not depend on the MMA)
+    RowInfo ri[kMaxRows / 32];
+    if (c.valid()) load_rows(c, a, lane, ri);
+    while (c.valid()) {
       const int R = c.rows();
-      // lane j of info[b] describes row 32 b + j of the chunk (read before the
-      // accumulator is ready: it does not depend on the MMA)
+      // lane j of info[b] describes row 32 b + j of the chunk
       int info[kMaxRows / 32];
 #pragma unroll
       for (int b = 0; b < kMaxRows / 32; ++b) {
-        int f = kRowPad;
-        const int r = 32 * b + lane;
-        if (r < R) {
-          const RowInfo ri = a.rowinfo[check_index(a.hdr, c.r0 + r, a.M, 31)];
-          const int64_t t = static_cast<int64_t>(ri.token) - tok0;
-          if (t >= 0 && t < T) f = static_cast<int>(t) | (ri.rank == 0 ? kRowFirst : 0);
-        }
+        int f = kRowPad | kScratchTok;
+        const int64_t t = static_cast<int64_t>(ri[b].token) - tok0;
+        if (32 * b + lane < R && t >= 0 && t < T) f = static_cast<int>(t);
         const int before = __shfl_up_sync(0xFFFFFFFFu, f, 1);
         if (lane > 0 && !(f & kRowPad) && !(before & kRowPad) && ((before ^ f) & 0xFF) == 0)
           f |= kRowDup;
         info[b] = f;
       }
-      const bool ok = ptx::mbar_wait_cluster(&ctl->tfull[acc], aph, lim, abort);
+      ChunkIt cn = c;
+      cn.next();
+      if (cn.valid()) load_rows(cn, a, lane, ri);
+      const bool ok = ptx::mbar_wait(&ctl->tfull[acc], aph, lim, abort);
       if (!__all_sync(0xFFFFFFFFu, ok)) {
         if (lane == 0) {
           ctl->abort = 1;
@@ -347,38 +401,47 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
       }
       ptx::tc_fence_after_sync();
       const uint32_t acc_col = static_cast<uint32_t>(acc * kAccCols);
-#pragma unroll
+      // (a loop, not unrolled: the smaller code runs faster here)
+#pragma unroll 1
       for (int b = 0; b < kMaxRows / 32; ++b) {
         if (32 * b >= R) break;
+        // The batch's carry flags as a warp-wide bit mask, its tokens four to
+        // a 32-bit word: the per-row column arithmetic then runs on values
+        // the whole warp shares (a per-row shuffle costs ~2.5x in the loads
+        // and stores below).
+        const int f = b == 0 ? info[0] : (b == 1 ? info[1] : (b == 2 ? info[2] : info[3]));
+        const uint32_t dupm = __ballot_sync(0xFFFFFFFFu, f & kRowDup);
+        uint32_t x = static_cast<uint32_t>(f & 0xFF) << (8 * (lane & 3));
+        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+        x |= __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+        uint32_t pk[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) pk[w] = __shfl_sync(0xFFFFFFFFu, x, 4 * w);
+        // row j's column: its token's slab column (a padding row's is the
+        // scratch column, whose contents nothing reads)
+        auto col = [&](int j) -> uint32_t {
+          return kSlabCol + ((pk[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+        };
         uint32_t v[32], old[32];
         ptx::tmem_ld_32x32b_x32(t_lane + acc_col + static_cast<uint32_t>(32 * b), v);
-        int row[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          row[j] = __shfl_sync(0xFFFFFFFFu, info[b], j);
-          old[j] = ptx::tmem_ld_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j));
-        }
+        for (int j = 0; j < 32; ++j) old[j] = ptx::tmem_ld_32x32b_x1(t_lane + col(j));
         ptx::tmem_ld_wait_regs(v);
         ptx::tmem_ld_wait_regs(old);
-        if (!__any_sync(0xFFFFFFFFu, info[b] & kRowDup)) {
-          // distinct tokens: independent updates (-0 + x == x for every x)
+        if (dupm == 0) {
+          // distinct tokens: independent updates
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float base = (row[j] & kRowFirst) ? -0.0f : __uint_as_float(old[j]);
-            ptx::tmem_st_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j),
-                                   __float_as_uint(base + __uint_as_float(v[j])));
-          }
+          for (int j = 0; j < 32; ++j)
+            ptx::tmem_st_32x32b_x1(t_lane + col(j),
+                                   __float_as_uint(__uint_as_float(old[j]) + __uint_as_float(v[j])));
         } else {
           // a token twice in a row: carry its running sum
           float carry = 0.0f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = __uint_as_float(v[j]);
-            const float val = (row[j] & kRowFirst)
-                                  ? x
-                                  : ((row[j] & kRowDup) ? carry + x : __uint_as_float(old[j]) + x);
-            ptx::tmem_st_32x32b_x1(t_lane + row_col(row[j], acc_col + 32 * b + j),
-                                   __float_as_uint(val));
+            const float xv = __uint_as_float(v[j]);
+            const float val = ((dupm >> j) & 1u) ? carry + xv : __uint_as_float(old[j]) + xv;
+            ptx::tmem_st_32x32b_x1(t_lane + col(j), __float_as_uint(val));
             carry = val;
           }
         }
@@ -387,9 +450,10 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_remote(acc ? tempty1 : tempty0);
+      if (lane == 0) arrive_acc_free(acc ? tempty1 : tempty0);
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
+      c = cn;
     }
     if (stop) break;
     // the slab is done: this thread's column to d_x (every token of the
@@ -468,11 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&ctl->tfull[b], 1);
       ptx::mbar_init(&ctl->tempty[b], 8);
     }
-    ptx::mbar_init(&ctl->drain, 1);
+    ptx::mbar_init(&ctl->drain[0], 1);
+    ptx::mbar_init(&ctl->drain[1], 1);
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
+    // (both TMA threads use the same maps)
     if constexpr (WIDE) {
       ptx::tma_prefetch_desc(&m.tw4);
       ptx::tma_prefetch_desc(&m.dy3);
@@ -482,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (a.tma_out) ptx::tma_prefetch_desc(&m.tout);
   }
-  if (warp == 1) {
+  if (warp == 2) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
     ptx::tmem_relinquish_pair();
   }
@@ -492,10 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
-  if (warp == 0) {
-    if (lane == 0) producer<WIDE>(smem, ctl, &m, a, n_units, rank);
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_issuer<DT, WIDE>(smem, ctl, tmem_base, a, n_units);
+  if (warp < 2) {
+    if (lane == 0) producer<WIDE>(smem, ctl, &m, a, n_units, rank, warp);
+  } else if (warp < kEpiWarp0) {
+    if (lane == 0 && rank == 0) mma_issuer<DT, WIDE>(smem, ctl, tmem_base, a, n_units, warp - 2);
   } else {
     epilogue(ctl, out_stage + (warp & 3) * 2 * kOutBuf, &m.tout, tmem_base, a, n_units, rank);
   }
@@ -503,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::cluster_sync();
-  if (warp == 1) {
+  if (warp == 2) {
     ptx::tc_fence_after_sync();
     ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }

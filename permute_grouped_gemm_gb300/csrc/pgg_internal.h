@@ -97,7 +97,7 @@ struct Layout {
 };
 
 // Largest token slab of the owner variant of the d_x kernel (gmm_dx_owner.cu).
-constexpr int kMaxSlabTokens = 256;
+constexpr int kMaxSlabTokens = 224;  // owner variant; tensor memory columns 480-511 stay free
 
 struct Plan {
   int variant;         // 0 wide row blocks on CTA pairs, 1 narrow row blocks, 2 wide on single
