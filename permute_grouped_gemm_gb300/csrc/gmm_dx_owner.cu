@@ -420,7 +420,7 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
         // row j's column: its token's slab column (a padding row's is the
         // scratch column, whose contents nothing reads)
         auto col = [&](int j) -> uint32_t {
-          return kSlabCol + ((pk[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+          return kSlabCol + __byte_perm(pk[j >> 2], 0u, 0x4440u + static_cast<uint32_t>(j & 3));
         };
         uint32_t v[32], old[32];
         ptx::tmem_ld_32x32b_x32(t_lane + acc_col + static_cast<uint32_t>(32 * b), v);
