@@ -133,6 +133,30 @@ def test_plan_variants(lib):
         pgg.pgg_debug_force_variant(-1)
 
 
+def test_owner_plan(lib):
+    # few experts per token: the owner variant, slabs of T = 112 G / topK tokens
+    # rounded down to 32 (at most 224: tensor-memory columns 480-511 stay free),
+    # 256 threads (two TMA warps, two MMA-issuing warps, four epilogue warps)
+    uni = pgg.pgg_dx_plan(32768, 1024, 2048, 16, 32768, 4096, 8, 0, pgg.PGG_BF16)
+    assert uni["variant"] == 4 and uni["rows_per_block"] == 224
+    assert uni["threads"] == 256 and uni["cta_pair"] == 1 and uni["stages"] == 4
+    assert uni["smem_bytes"] <= 227 * 1024
+    # 112 G > 224 topK: the ticketed kernel, unless forced; forced, the slab is capped
+    wide = pgg.pgg_dx_plan(16000, 256, 2048, 40, 16000, 8000, 2, 0, pgg.PGG_BF16)
+    assert wide["variant"] == 0
+    pgg.pgg_debug_force_variant(4)
+    try:
+        p = pgg.pgg_dx_plan(16000, 256, 2048, 40, 16000, 8000, 2, 0, pgg.PGG_BF16)
+        assert p["variant"] == 4 and p["rows_per_block"] == 224
+        # N not a multiple of 64: one-panel stages, eight of them
+        p = pgg.pgg_dx_plan(32768, 1000, 2048, 16, 32768, 4096, 8, 0, pgg.PGG_F16)
+        assert p["variant"] == 4 and p["stages"] == 8 and p["smem_bytes"] <= 227 * 1024
+        # fp32 never takes the owner variant
+        assert pgg.pgg_dx_plan(32768, 1024, 2048, 16, 32768, 4096, 8, 0, pgg.PGG_F32)["variant"] == 0
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+
+
 def test_status_strings(lib):
     for code, name in pgg.STATUS.items():
         assert pgg.pgg_status_string(code) != "unknown status", name
