@@ -118,3 +118,30 @@ def test_reason_bits_name_the_nvml_clock_event_reasons():
     assert bench._REASON_BITS[0x8] == "hw_slowdown"
     assert bench._REASON_BITS[0x20] == "sw_thermal_slowdown"
     assert bench._REASON_BITS[0x40] == "hw_thermal_slowdown"
+
+
+def test_profile_summaries_match_the_current_kernel_sources():
+    # every ncu summary that records a kernel source hash was taken on the
+    # current source of that kernel, or says that it was not
+    import glob
+    import os
+    import re
+    import bench
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    checked = 0
+    for path in sorted(glob.glob(os.path.join(root, "profiles", "*.md"))):
+        text = open(path).read()
+        m = re.search(r"kernel_source_hash:\s*([0-9a-f]{16})", text)
+        if not m:
+            continue
+        name = os.path.basename(path)[: -len(".md")]
+        kernel = name[: name.rindex("_")]
+        assert kernel in bench.KERNEL_SOURCES, (path, kernel)
+        if "capture_of_earlier_source: yes" in text:
+            continue
+        assert m.group(1) == bench.kernel_hash(kernel), (
+            f"{os.path.basename(path)} records {m.group(1)}, the source now hashes to "
+            f"{bench.kernel_hash(kernel)}: re-take it or mark it as a capture of an earlier source")
+        checked += 1
+    assert checked >= 5
