@@ -357,6 +357,7 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
   int acc = 0, obuf = 0;
   uint32_t aph = 0;
   bool stop = false;
+  bool held = a.hold_release != 0;  // (test hook: the first release is withheld)
   for (uint32_t u = cluster_id(); u < n_units && !stop; u += n_clusters()) {
     const int64_t slab = u / a.k_units;
     const int64_t tok0 = slab * T;
@@ -450,7 +451,8 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) arrive_acc_free(acc ? tempty1 : tempty0);
+      if (lane == 0 && !held) arrive_acc_free(acc ? tempty1 : tempty0);
+      held = false;
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
       c = cn;

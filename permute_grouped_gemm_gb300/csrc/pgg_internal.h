@@ -166,6 +166,8 @@ struct OwnerArgs {
   int32_t nk;       // reduction steps: ceil(N / 128) when wide, else ceil(N / 64)
   int32_t wide;     // 1: stages of two 64-n panels (N a multiple of 64)
   int32_t tma_out;  // 1: d_x written by TMA stores (K % 4 == 0, out 16-byte aligned)
+  int32_t hold_release;  // test hook: 1 = the epilogue never frees accumulator 0 after its
+                         // first chunk (the bounded waits then run out); 0 in normal use
   uint64_t wait_limit_ns;
 };
 

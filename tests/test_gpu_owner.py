@@ -139,6 +139,28 @@ def test_device_errors_zero_the_output_in_owner_mode():
     assert torch.count_nonzero(out) == 0
 
 
+def test_bounded_wait_reports_timeout_and_recovers():
+    # the epilogue withholds its first release of accumulator 0 (test hook), so
+    # the MMA thread of that pipeline waits for it until the limit: every role
+    # of every CTA gives up, the call reports PGG_ERR_TIMEOUT, and the next call
+    # on the same context is correct
+    inp = make_case(batch=2048, top_k=8, G=16, K=512, N=512, dtype="bf16", seed=58,
+                    device="cuda")
+    pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    pgg.pgg_debug_set_owner_hold(1)
+    try:
+        pgg.pgg_debug_force_variant(4)
+        _, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                       inp.top_k, inp.row_idx_type)
+        torch.cuda.synchronize()
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+        pgg.pgg_debug_set_owner_hold(0)
+        pgg.pgg_debug_set_wait_limit_ns(0)
+    check(inp, run(inp, 4), what="after timeout")
+
+
 def test_uniform_workload_full_size():
     w = WORKLOADS["uniform-bf16"]
     inp = make_inputs(w, device="cuda")
