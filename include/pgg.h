@@ -208,17 +208,18 @@ const char* pgg_status_string(int status);
  * pgg_debug_set_band_k_blocks: k-blocks per band of the tile order (0 =
  *   automatic). The result does not depend on it, bit for bit: only the time
  *   order of the tiles changes, never the order of the additions.
- * pgg_debug_set_owner_hold: non-zero makes the owner variant's epilogue
- *   withhold its first release of an accumulator, so that the MMA thread's
- *   bounded wait for it runs out: exercises PGG_ERR_TIMEOUT in that kernel
- *   (every CTA role gives up, drains its copies and MMAs and frees tensor
- *   memory). 0 = off.
+ * pgg_debug_set_hold_release: non-zero makes the epilogue of the owner d_x
+ *   variant, of the forward and of the weight-gradient kernels withhold its
+ *   first release of an accumulator, so that the MMA thread's bounded wait
+ *   for it runs out: exercises PGG_ERR_TIMEOUT in those kernels (every CTA
+ *   role gives up, drains its copies and MMAs and frees tensor memory). A CTA
+ *   pair with fewer than three tiles never waits for that release. 0 = off.
  */
 void pgg_debug_set_wait_limit_ns(uint64_t ns);
 void pgg_debug_set_ticket_bias(uint32_t bias);
 void pgg_debug_force_variant(int variant);
 void pgg_debug_set_band_k_blocks(int k_blocks);
-void pgg_debug_set_owner_hold(int hold);
+void pgg_debug_set_hold_release(int hold);
 
 /*
  * pgg_dx_execute for callers that cannot allocate device memory. (The pages

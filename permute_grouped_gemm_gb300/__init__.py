@@ -11,7 +11,7 @@ from __future__ import annotations
 
 from ._lib import (  # noqa: F401
     CODES, PGG_BF16, PGG_F16, PGG_F32, STATUS, PggError, load,
-    pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_owner_hold,
+    pgg_debug_force_variant, pgg_debug_set_band_k_blocks, pgg_debug_set_hold_release,
     pgg_debug_set_ticket_bias, pgg_debug_set_wait_limit_ns,
     pgg_dw_execute, pgg_dw_grouped_gemm, pgg_dw_plan, pgg_dw_workspace_size,
     pgg_fwd_execute, pgg_fwd_grouped_gemm, pgg_fwd_plan, pgg_fwd_route_prep,

@@ -100,10 +100,10 @@ def load(path: str | None = None):
             lib.pgg_debug_set_ticket_bias.argtypes = [ctypes.c_uint32]
             lib.pgg_debug_force_variant.argtypes = [ctypes.c_int]
             lib.pgg_debug_set_band_k_blocks.argtypes = [ctypes.c_int]
-            lib.pgg_debug_set_owner_hold.argtypes = [ctypes.c_int]
+            lib.pgg_debug_set_hold_release.argtypes = [ctypes.c_int]
             for f in ("pgg_debug_set_wait_limit_ns", "pgg_debug_set_ticket_bias",
                       "pgg_debug_force_variant", "pgg_debug_set_band_k_blocks",
-                      "pgg_debug_set_owner_hold"):
+                      "pgg_debug_set_hold_release"):
                 getattr(lib, f).restype = None
             _handle = lib
     return _handle
@@ -279,5 +279,5 @@ def pgg_debug_set_band_k_blocks(k_blocks: int):
     load().pgg_debug_set_band_k_blocks(k_blocks)
 
 
-def pgg_debug_set_owner_hold(hold: int):
-    load().pgg_debug_set_owner_hold(hold)
+def pgg_debug_set_hold_release(hold: int):
+    load().pgg_debug_set_hold_release(hold)

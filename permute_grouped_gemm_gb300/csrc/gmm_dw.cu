@@ -422,6 +422,7 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   int acc = 0, nb = 0;
   uint32_t aph = 0;
+  bool held = a.hold_release != 0;  // (test hook: the first release is withheld)
   for (uint32_t t = cluster_id(); t < total; t += n_clusters()) {
     const Tile x = tile_of(t, a, rank);
     const int64_t k = x.k0 + 32 * quarter + lane;
@@ -506,7 +507,10 @@ __device__ void epilogue(uint8_t* obuf, DwCtl* ctl, uint32_t tmem_base, const CU
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_remote(acc ? tempty1 : tempty0);
+    // tensor memory changes hands (the output goes out through global memory,
+    // not to the MMA thread): CTA scope
+    if (lane == 0 && !held) ptx::mbar_arrive_remote_cta(acc ? tempty1 : tempty0);
+    held = false;
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }

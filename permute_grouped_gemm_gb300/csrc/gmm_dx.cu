@@ -832,9 +832,14 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
+    // The accumulator is free again. What changes hands is tensor memory,
+    // ordered by the tcgen05 fences on both sides of the barrier; the rows'
+    // global writes go to other tiles through the tickets, not to the MMA
+    // thread. So the odd CTA arrives at CTA scope too: a cluster-scope release
+    // here waits for the warp's ticket reductions to reach L2 first.
     if (lane == 0) {
       if (remote)
-        ptx::mbar_arrive_remote(ptx::mapa(&ctl->tempty[acc], 0));
+        ptx::mbar_arrive_remote_cta(ptx::mapa(&ctl->tempty[acc], 0));
       else
         ptx::mbar_arrive(&ctl->tempty[acc]);
     }

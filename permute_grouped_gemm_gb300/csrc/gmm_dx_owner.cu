@@ -333,14 +333,6 @@ __device__ __forceinline__ void tmem_fill_32x32b_x32(uint32_t taddr, uint32_t x)
       : "memory");
 }
 
-// Arrival on the accumulator's barrier in the even CTA, CTA-scope: what
-// changes hands is tensor memory, ordered by the tcgen05 fences around the
-// barrier, not generic memory (a cluster-scope release costs ~1,800 cycles
-// here).
-__device__ __forceinline__ void arrive_acc_free(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 // Epilogue warp q (of 4) owns tensor-memory lanes 32 q .. 32 q + 31: one d_x
 // column k each, for every token of the slab.
 __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
@@ -451,7 +443,9 @@ __device__ void epilogue(OwnCtl* ctl, float* out_stage, const CUtensorMap* tout,
       }
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0 && !held) arrive_acc_free(acc ? tempty1 : tempty0);
+      // tensor memory changes hands: CTA scope (a cluster-scope release
+      // cost ~1,800 cycles here)
+      if (lane == 0 && !held) ptx::mbar_arrive_remote_cta(acc ? tempty1 : tempty0);
       held = false;
       acc ^= 1;
       if (acc == 0) aph ^= 1u;

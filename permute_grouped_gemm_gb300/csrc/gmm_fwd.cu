@@ -345,6 +345,7 @@ __device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   int acc = 0;
   uint32_t aph = 0;
+  bool held = a.hold_release != 0;  // (test hook: the first release is withheld)
   for (uint32_t t = cluster_id(); t < total; t += n_clusters()) {
     const FTile x = ftile_of(t, a, rank);
     const int valid = x.rows - 32 * quarter;  // rows of this warp's 32 that exist
@@ -423,7 +424,10 @@ __device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_remote(acc ? tempty1 : tempty0);
+    // tensor memory changes hands (the output goes out through global memory,
+    // not to the MMA thread): CTA scope
+    if (lane == 0 && !held) ptx::mbar_arrive_remote_cta(acc ? tempty1 : tempty0);
+    held = false;
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }

@@ -62,7 +62,7 @@ namespace {
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 std::atomic<uint32_t> g_ticket_bias{0};
-std::atomic<int> g_owner_hold{0};
+std::atomic<int> g_hold_release{0};
 std::atomic<int> g_force_variant{-1};
 std::atomic<int> g_band_k_blocks{0};
 
@@ -424,7 +424,7 @@ int run_grouped_gemm(const Plan& plan, const void* gradY, const void* weight, vo
     o.k_units = static_cast<int32_t>((plan.K + 255) / 256);
     o.nk = plan.nk;
     o.wide = 0;
-    o.hold_release = g_owner_hold.load() != 0 ? 1 : 0;
+    o.hold_release = g_hold_release.load() != 0 ? 1 : 0;
     o.wait_limit_ns = a.wait_limit_ns;
     OwnerMaps om;
     om.dy = tdy;
@@ -529,6 +529,7 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
   a.dy_3d = 0;
   a.gather_dy = 0;
+  a.hold_release = g_hold_release.load() != 0 ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   if (!dw_tensor_path(plan.dtype, plan.N, plan.K, x, gradY, dweight) &&
       dw_gather_path(plan.dtype, plan.N, plan.K, x, gradY, dweight)) {
@@ -664,6 +665,7 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
   a.out_f32 = out_dtype == PGG_F32 ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.gather_w = 0;
+  a.hold_release = g_hold_release.load() != 0 ? 1 : 0;
   if (!fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y) &&
       fwd_gather_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
     fwd_tiles(plan.N, &a.n_blocks);
@@ -1104,7 +1106,7 @@ void pgg_debug_set_wait_limit_ns(uint64_t ns) {
 }
 
 void pgg_debug_set_ticket_bias(uint32_t bias) { g_ticket_bias.store(bias); }
-void pgg_debug_set_owner_hold(int hold) { g_owner_hold.store(hold); }
+void pgg_debug_set_hold_release(int hold) { g_hold_release.store(hold); }
 
 void pgg_debug_force_variant(int variant) { g_force_variant.store(variant); }
 

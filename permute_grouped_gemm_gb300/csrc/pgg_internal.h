@@ -220,6 +220,8 @@ struct DwArgs {
   int32_t gather_dy;  // tensor-core kernel: 1 = d_y rows copied by the gather warps (4-byte
                       // cp.async) and the output written with 4-byte stores (N even, N * 2
                       // not a multiple of 16); 0 = TMA for both
+  int32_t hold_release;  // test hook (tensor-core kernel): 1 = each epilogue warp keeps its
+                         // first accumulator release back; 0 in normal use
   uint64_t wait_limit_ns;
 };
 
@@ -238,6 +240,8 @@ struct FwdArgs {
   int32_t gather_w;  // tensor-core kernel: 1 = weight rows copied by the gather warps (4-byte
                      // cp.async) and y written with 4-byte stores (N even, N * 2 not a
                      // multiple of 16); 0 = TMA for both
+  int32_t hold_release;  // test hook (tensor-core kernel): 1 = each epilogue warp keeps its
+                         // first accumulator release back; 0 in normal use
   uint64_t wait_limit_ns;
 };
 

@@ -393,6 +393,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrival on a barrier of either CTA of the cluster with the default
+// CTA-scope release. For hand-overs of tensor memory, which the tcgen05 fences
+// on both sides of the barrier order, and through which no generic-memory data
+// changes hands. (A cluster-scope release first waits for the thread's
+// outstanding global writes: 1,000 to 1,800 cycles in the epilogues.)
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)

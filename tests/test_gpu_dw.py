@@ -295,3 +295,33 @@ def test_four_byte_aligned_dy_and_output_equal_the_tma_path_bitwise(out_f32):
     torch.cuda.synchronize()
     assert pgg.status(ws) == 0
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("n", [1024, 1022])
+def test_bounded_wait_reports_timeout_and_recovers(n):
+    # every epilogue warp withholds its first release of accumulator 0 (test
+    # hook), so the MMA thread's wait for it runs out at each CTA pair's third
+    # tile (16 experts x 4 k blocks x 4 n blocks = 256 tiles over 76 pairs):
+    # every role of both CTAs gives up, the call reports PGG_ERR_TIMEOUT, and
+    # the next call on the same context is correct. N = 1022 takes the d_y
+    # panels copied by the gather warps.
+    inp = make_case(batch=2048, top_k=8, G=16, K=1024, N=n, dtype="bf16", seed=60,
+                    device="cuda")
+    x = forward_input(inp)
+    assert plan_variant(inp, x) == (0 if n == 1024 else 5)
+    pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    pgg.pgg_debug_set_hold_release(1)
+    try:
+        _, ws = pgg.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch,
+                       inp.top_k, inp.row_idx_type)
+        torch.cuda.synchronize()
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
+    finally:
+        pgg.pgg_debug_set_hold_release(0)
+        pgg.pgg_debug_set_wait_limit_ns(0)
+    rng = np.random.default_rng(60)
+    g = rng.integers(0, 16, 256)
+    k = rng.integers(0, 1024, 256)
+    out = run(inp, x)
+    got = out[torch.from_numpy(g).cuda(), torch.from_numpy(k).cuda()]
+    assert_close(got, ref_of(inp, x, sel=(g, k)), "after timeout")

@@ -273,3 +273,29 @@ def test_four_byte_aligned_weight_and_y_equal_the_tma_path_bitwise(out_f32):
     torch.cuda.synchronize()
     assert pgg.status(ws) == 0
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("n", [1024, 1022])
+def test_bounded_wait_reports_timeout_and_recovers(n):
+    # every epilogue warp withholds its first release of accumulator 0 (test
+    # hook), so the MMA thread's wait for it runs out at each CTA pair's third
+    # tile (256 tiles over 76 pairs): every role of both CTAs gives up, the call
+    # reports PGG_ERR_TIMEOUT, and the next call on the same context is correct.
+    # N = 1022 takes the weight panels copied by the gather warps.
+    inp = make_case(batch=2048, top_k=8, G=16, K=512, N=n, dtype="bf16", seed=59,
+                    device="cuda")
+    x = forward_input(inp)
+    assert variant(inp, x) == (0 if n == 1024 else 5)
+    pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    pgg.pgg_debug_set_hold_release(1)
+    try:
+        _, ws = pgg.fwd(x, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                        inp.top_k, inp.row_idx_type)
+        torch.cuda.synchronize()
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
+    finally:
+        pgg.pgg_debug_set_hold_release(0)
+        pgg.pgg_debug_set_wait_limit_ns(0)
+    rows = np.sort(np.random.default_rng(59).choice(inp.grad_y.shape[0], 512, replace=False))
+    y = run(inp, x)
+    assert_close(y[torch.from_numpy(rows).cuda()], ref_of(inp, x, rows=rows), "after timeout")

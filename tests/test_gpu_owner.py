@@ -147,7 +147,7 @@ def test_bounded_wait_reports_timeout_and_recovers():
     inp = make_case(batch=2048, top_k=8, G=16, K=512, N=512, dtype="bf16", seed=58,
                     device="cuda")
     pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
-    pgg.pgg_debug_set_owner_hold(1)
+    pgg.pgg_debug_set_hold_release(1)
     try:
         pgg.pgg_debug_force_variant(4)
         _, ws = pgg.dx(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
@@ -156,7 +156,7 @@ def test_bounded_wait_reports_timeout_and_recovers():
         assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
     finally:
         pgg.pgg_debug_force_variant(-1)
-        pgg.pgg_debug_set_owner_hold(0)
+        pgg.pgg_debug_set_hold_release(0)
         pgg.pgg_debug_set_wait_limit_ns(0)
     check(inp, run(inp, 4), what="after timeout")
 

@@ -253,6 +253,28 @@ def test_bounded_wait_reports_timeout_and_recovers(n):
     check(inp, what="after timeout")
 
 
+@pytest.mark.parametrize("variant,dtype", [(1, "bf16"), (2, "fp16"), (0, "fp32"), (1, "fp32")])
+def test_bounded_wait_timeout_single_cta_forms(variant, dtype):
+    """The single-CTA instantiations of the ticketed kernel (narrow and wide
+    row blocks, and the 3xTF32 fp32 form) give up on a ticket that never comes
+    the same way the CTA-pair form does."""
+    inp = make_case(batch=256, top_k=4, G=8, K=256, N=128, dtype=dtype, seed=11,
+                    device="cuda")
+    pgg.pgg_debug_force_variant(variant)
+    pgg.pgg_debug_set_wait_limit_ns(20_000_000)  # 20 ms
+    pgg.pgg_debug_set_ticket_bias(1000)
+    try:
+        plan = pgg.pgg_dx_plan(*_sizes(inp), inp.row_idx_type, pgg.dtype_code(inp.grad_y.dtype))
+        assert plan["variant"] == variant and plan["cta_pair"] == 0
+        _, ws = run(inp)
+        assert pgg.STATUS[pgg.status(ws)] == "PGG_ERR_TIMEOUT"
+    finally:
+        pgg.pgg_debug_set_ticket_bias(0)
+        pgg.pgg_debug_set_wait_limit_ns(0)
+        pgg.pgg_debug_force_variant(-1)
+    check(inp, what="after timeout")
+
+
 def test_no_writes_outside_out_and_workspace():
     inp = make_case(batch=100, top_k=3, G=5, K=200, N=96, dtype="bf16", seed=11, device="cuda")
     need = pgg.workspace_bytes(inp.grad_y, inp.weight, inp.expanded_row_idx, inp.group_list,
