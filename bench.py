@@ -57,14 +57,17 @@ METRIC = "fused d_x TFLOP/s (2*M*N*K/s) & % of roofline, 1xGB300; peak workspace
 _COMMON = ["permute_grouped_gemm_gb300/csrc/pgg_ptx.cuh"]
 # grouped-GEMM kernel -> the sources its ncu counters depend on
 _GATHER = "permute_grouped_gemm_gb300/csrc/pgg_gather.cuh"
+_EPILOGUE = "permute_grouped_gemm_gb300/csrc/pgg_epilogue.cuh"
 KERNEL_SOURCES = {
     "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", _GATHER, *_COMMON],
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
     "gmm_dx_owner_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_owner.cu", *_COMMON],
     "unpermute_grad_kernel": ["permute_grouped_gemm_gb300/csrc/unpermute_grad.cu"],
-    "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", _GATHER, *_COMMON],
+    "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", _GATHER, _EPILOGUE,
+                       *_COMMON],
     "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],
-    "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", _GATHER, *_COMMON],
+    "gmm_fwd_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd.cu", _GATHER, _EPILOGUE,
+                       *_COMMON],
     "gmm_fwd_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_fwd_simt.cu", *_COMMON],
 }
 SIMT_VARIANT = 3

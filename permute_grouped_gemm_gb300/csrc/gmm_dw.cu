@@ -46,6 +46,7 @@
 
 #include <cstdint>
 
+#include "pgg_epilogue.cuh"
 #include "pgg_gather.cuh"
 #include "pgg_internal.h"
 #include "pgg_ptx.cuh"
@@ -363,24 +364,6 @@ __device__ void mma_issuer(uint8_t* smem, DwCtl* ctl, uint32_t tmem_base, const 
     ptx::mma_commit_pair(&ctl->drain, 0x1);
     ptx::mbar_wait(&ctl->drain, 0u, lim, &no_abort);
   }
-}
-
-// 8 fp32 values -> 16 bytes of the 16-bit output dtype.
-template <int DT>
-__device__ __forceinline__ uint4 pack8(const uint32_t* v) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
-    if constexpr (DT == PGG_BF16) {
-      const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
-    } else {
-      const __half2 p = __floats2half2_rn(lo, hi);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Rows of 128 bytes of the output chunk: 64 values of the 16-bit dtype or 32

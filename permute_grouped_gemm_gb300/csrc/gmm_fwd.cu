@@ -23,13 +23,18 @@
 //       8), the gather warps copy the panels instead, one 128-byte k row
 //       segment per warp instruction, 4 bytes per lane, into the same
 //       swizzled layout, and the epilogue writes y with 4-byte stores.
-// The epilogue warps convert 128-byte row chunks into a swizzled
-// shared-memory box and store it with one TMA tensor store; a box that would
-// cross the end of the row block (into the next expert's rows) is written
-// row by row with ordinary stores instead.
+// Seven stage slots: the gathers' round trip (slot free -> rows copied ->
+// slot full) is what bounds the kernel, and the shared memory in flight covers
+// it. The epilogue therefore writes y straight from registers, with no
+// shared-memory staging: each warp turns its 32 rows x 128 bytes into 16-byte
+// blocks, transposes them within groups of eight lanes, and every warp store
+// then writes four rows' full 128-byte segments. Rows past the row block
+// (the next expert's rows) are not written.
 //
 // Warp roles per CTA: 0 TMA for the weight; 1 tensor-memory allocation and
-// (even CTA) MMA issue; one gather warp per stage slot; eight epilogue warps.
+// (even CTA) MMA issue; one gather warp per stage slot; four epilogue warps,
+// one per tensor-memory lane quarter (13 warps in all, so that no SM
+// sub-partition holds more than four and each thread may use 128 registers).
 // Tiles are statically interleaved over the clusters. Waits are bounded; when
 // one runs out the kernel records PGG_ERR_TIMEOUT, drains its copies and
 // MMAs, frees tensor memory and returns.
@@ -39,6 +44,7 @@
 
 #include <cstdint>
 
+#include "pgg_epilogue.cuh"
 #include "pgg_gather.cuh"
 #include "pgg_internal.h"
 #include "pgg_ptx.cuh"
@@ -49,19 +55,17 @@ namespace {
 constexpr int kFM = 128;       // expanded rows per CTA (the pair's MMA M is 256)
 constexpr int kFN = 256;       // output columns n per tile (MMA N)
 constexpr int kFK = 64;        // reduction (k) per stage: one 128-byte row of A
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kPanel = kFK * 128;                // B panel: 64 k rows x 128 bytes (64 n)
 constexpr int kABytes = kFM * 128;               // A: 128 rows x 128 bytes
 constexpr int kBBytes = 2 * kPanel;              // B: this CTA's 128 n
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kGatherWarps = kStages;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 4;
 constexpr int kEpiWarp0 = 2 + kGatherWarps;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr int kOutBuf = 32 * 128;
-constexpr int kOutBytes = kEpiWarps * kOutBuf;
 
 struct FwdCtl {
   uint64_t full[kStages];   // even CTA: weight bytes of both CTAs + x gathered in both (2 arrivals)
@@ -74,7 +78,7 @@ struct FwdCtl {
 };
 
 constexpr int kSmemBytes =
-    kStages * kStageBytes + kOutBytes + static_cast<int>(sizeof(FwdCtl)) + 1024;
+    kStages * kStageBytes + static_cast<int>(sizeof(FwdCtl)) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ void raise_status(WsHeader* hdr, uint32_t code, uint32_t site) {
@@ -311,36 +315,18 @@ __device__ void mma_issuer(uint8_t* smem, FwdCtl* ctl, uint32_t tmem_base, const
 }
 
 template <int DT>
-__device__ __forceinline__ uint4 pack8(const uint32_t* v) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
-    if constexpr (DT == PGG_BF16) {
-      const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
-    } else {
-      const __half2 p = __floats2half2_rn(lo, hi);
-      w[i] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-template <int DT>
-__device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
-                         const CUtensorMap* tm_y, const FwdArgs& a, uint32_t total,
+__device__ void epilogue(FwdCtl* ctl, uint32_t tmem_base, const FwdArgs& a, uint32_t total,
                          uint32_t rank) {
   const uint64_t lim = a.wait_limit_ns;
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // accumulator lanes (rows) 32 q .. 32 q + 31
   const int e = warp - kEpiWarp0;
-  const int col0 = (e / 4) * (kFN / 2);
+  constexpr int kSpan = kFN / (kEpiWarps / 4);  // accumulator columns this warp writes
+  const int col0 = (e / 4) * kSpan;
   const bool f32 = a.out_f32 != 0;
   const int oes = f32 ? 4 : 2;
   const int cols = 128 / oes;
-  uint8_t* buf = obuf + e * kOutBuf;
   const uint32_t tempty0 = ptx::mapa(&ctl->tempty[0], 0);
   const uint32_t tempty1 = ptx::mapa(&ctl->tempty[1], 0);
   int acc = 0;
@@ -362,65 +348,12 @@ __device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
         tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(acc * kAccCols);
     const int64_t row_w = x.row0 + 32 * quarter;  // first expanded row of this warp
 #pragma unroll 1
-    for (int c0 = col0; c0 < col0 + kFN / 2 && x.n0 + c0 < a.N && valid > 0; c0 += cols) {
-      uint32_t v[64];
-      ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0),
-                              *reinterpret_cast<uint32_t(*)[32]>(v));
-      if (!f32)
-        ptx::tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c0 + 32),
-                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      ptx::tmem_ld_wait();
-      if (lane == 0) ptx::bulk_wait_read<0>();  // the previous store has read the buffer
-      __syncwarp();
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const uint4 q = f32 ? make_uint4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3])
-                            : pack8<DT>(v + 8 * p);
-        *reinterpret_cast<uint4*>(buf + lane * 128 + ((p ^ (lane & 7)) << 4)) = q;
-      }
-      const int64_t n = x.n0 + c0;
-      if (a.gather_w) {
-        // rows of N * 2 bytes that are not 16-byte multiples: 4 bytes per
-        // lane (one 128-byte row segment per warp instruction), existing rows
-        // and columns only
-        __syncwarp();
-        const int rows = valid < 32 ? valid : 32;
-        const int64_t col = n + lane * (4 / oes);
-        const uint32_t off = (((static_cast<uint32_t>(lane) >> 2) << 4) | ((lane & 3) << 2));
-#pragma unroll 4
-        for (int r = 0; r < rows; ++r) {
-          if (col < a.N) {
-            const uint32_t d =
-                *reinterpret_cast<const uint32_t*>(buf + r * 128 + (off ^ ((r & 7) << 4)));
-            char* dst = static_cast<char*>(a.out) + ((row_w + r) * a.N + col) * oes;
-            *reinterpret_cast<uint32_t*>(dst) = d;
-          }
-        }
-        __syncwarp();
-      } else if (valid >= 32) {
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_3d(tm_y, buf, static_cast<int32_t>(n), static_cast<int32_t>(row_w), 0);
-          ptx::bulk_commit();
-        }
-      } else {
-        // the block ends inside these 32 rows: the rows after it belong to
-        // the next expert, so write only the existing ones
-        __syncwarp();
-#pragma unroll 4
-        for (int q = 0; q < 8; ++q) {
-          const int r = (lane >> 3) + 4 * q;
-          const int p = lane & 7;
-          const int64_t col = n + p * (16 / oes);
-          if (r < valid && col < a.N) {
-            const uint4 d = *reinterpret_cast<const uint4*>(buf + r * 128 + ((p ^ (r & 7)) << 4));
-            char* dst = static_cast<char*>(a.out) + ((row_w + r) * a.N + col) * oes;
-            *reinterpret_cast<uint4*>(dst) = d;
-          }
-        }
-        __syncwarp();
-      }
+    for (int c0 = col0; c0 < col0 + kSpan && x.n0 + c0 < a.N && valid > 0; c0 += cols) {
+      uint4 b[8];
+      chunk_blocks<DT>(t_lane + static_cast<uint32_t>(c0), f32, b);
+      // rows past the block belong to the next expert and are not written
+      store_chunk(b, static_cast<char*>(a.out), row_w, valid, a.N, x.n0 + c0, oes, a.gather_w != 0,
+                  lane);
     }
     ptx::tc_fence_before_sync();
     __syncwarp();
@@ -431,20 +364,16 @@ __device__ void epilogue(uint8_t* obuf, FwdCtl* ctl, uint32_t tmem_base,
     acc ^= 1;
     if (acc == 0) aph ^= 1u;
   }
-  if (lane == 0) ptx::bulk_wait<0>();
-  __syncwarp();
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gmm_fwd_kernel(const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ CUtensorMap tm_y, const FwdArgs a) {
+    gmm_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const FwdArgs a) {
   ptx::griddep_wait();  // launched with programmatic serialization: predecessors done
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* obuf = smem + kStages * kStageBytes;
-  auto* ctl = reinterpret_cast<FwdCtl*>(obuf + kOutBytes);
+  auto* ctl = reinterpret_cast<FwdCtl*>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
 
@@ -477,10 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0 && lane == 0 && !a.gather_w) {
-    ptx::tma_prefetch_desc(&tm_w);
-    ptx::tma_prefetch_desc(&tm_y);
-  }
+  if (warp == 0 && lane == 0 && !a.gather_w) ptx::tma_prefetch_desc(&tm_w);
   if (warp == 1) {
     ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
     ptx::tmem_relinquish_pair();
@@ -498,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     x_gatherer<DT>(smem, ctl, a, total, nks, rank);
   } else {
-    epilogue<DT>(obuf, ctl, tmem_base, &tm_y, a, total, rank);
+    epilogue<DT>(ctl, tmem_base, a, total, rank);
   }
 
   ptx::tc_fence_before_sync();
@@ -519,9 +445,9 @@ int fwd_stages() { return kStages; }
 
 void fwd_tiles(int64_t N, int* n_blocks) { *n_blocks = static_cast<int>((N + kFN - 1) / kFN); }
 
-cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const CUtensorMap& tm_y,
-                       const FwdArgs& a, int64_t max_tiles, int num_sms, cudaStream_t stream) {
-  void (*kern)(const CUtensorMap, const CUtensorMap, const FwdArgs) = nullptr;
+cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const FwdArgs& a, int64_t max_tiles,
+                       int num_sms, cudaStream_t stream) {
+  void (*kern)(const CUtensorMap, const FwdArgs) = nullptr;
   if (dtype == PGG_BF16)
     kern = gmm_fwd_kernel<PGG_BF16>;
   else if (dtype == PGG_F16)
@@ -550,7 +476,7 @@ cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const CUtensorMap& tm
   if (err != cudaSuccess) return err;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, dim3(static_cast<unsigned>(2 * (clusters < want ? clusters : want))),
-                    dim3(kThreads), static_cast<size_t>(kSmemBytes), stream, 2, tm_w, tm_y, a);
+                    dim3(kThreads), static_cast<size_t>(kSmemBytes), stream, 2, tm_w, a);
 }
 
 }  // namespace pgg

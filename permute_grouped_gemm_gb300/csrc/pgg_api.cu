@@ -41,8 +41,8 @@ int fwd_threads();
 int fwd_rows_per_block();
 int fwd_stages();
 void fwd_tiles(int64_t N, int* n_blocks);
-cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const CUtensorMap& tm_y,
-                       const FwdArgs& a, int64_t max_tiles, int num_sms, cudaStream_t stream);
+cudaError_t launch_fwd(int dtype, const CUtensorMap& tm_w, const FwdArgs& a, int64_t max_tiles,
+                       int num_sms, cudaStream_t stream);
 void fwd_simt_tiles(int64_t N, int* n_blocks);
 int fwd_simt_smem_bytes();
 cudaError_t launch_fwd_simt(int dtype, const FwdArgs& a, int vec, int64_t max_tiles, int num_sms,
@@ -672,7 +672,7 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
     a.gather_w = 1;
     CUtensorMap none;
     std::memset(&none, 0, sizeof(none));
-    return launch_fwd(plan.dtype, none, none, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
+    return launch_fwd(plan.dtype, none, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
                       stream) == cudaSuccess
                ? PGG_OK
                : PGG_ERR_CUDA;
@@ -681,7 +681,7 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
     fwd_tiles(plan.N, &a.n_blocks);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PGG_ERR_CUDA;
-    CUtensorMap tm_w, tm_y;
+    CUtensorMap tm_w;
     {
       // weight [G, K, N]: boxes of 64 n x 64 k of one expert
       cuuint64_t dims[3] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.K),
@@ -696,21 +696,7 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PGG_ERR_CUDA;
     }
-    {
-      // y [M, N] (as {N, M, 1}): boxes of 128 bytes x 32 rows
-      const int oes = out_dtype == PGG_F32 ? 4 : 2;
-      cuuint64_t dims[3] = {static_cast<cuuint64_t>(plan.N), static_cast<cuuint64_t>(plan.M), 1};
-      cuuint64_t strides[2] = {static_cast<cuuint64_t>(plan.N) * oes,
-                               static_cast<cuuint64_t>(plan.N) * static_cast<cuuint64_t>(plan.M) *
-                                   oes};
-      cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / oes), 32, 1};
-      cuuint32_t estr[3] = {1, 1, 1};
-      if (enc(&tm_y, tmap_type(out_dtype), 3, y, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PGG_ERR_CUDA;
-    }
-    return launch_fwd(plan.dtype, tm_w, tm_y, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
+    return launch_fwd(plan.dtype, tm_w, a, plan.max_row_blocks * a.n_blocks, di.num_sms,
                       stream) == cudaSuccess
                ? PGG_OK
                : PGG_ERR_CUDA;

@@ -196,7 +196,7 @@ def test_weight_gradient_plan_and_host_errors(lib):
     sizes = (a["M"], a["N"], a["K"], a["G"], a["L"], a["batch"], a["topK"], 0)
     p = pgg.pgg_dw_plan(*sizes, pgg.PGG_BF16)
     assert p["variant"] == 0 and p["k_per_block"] == 256 and p["threads"] % 32 == 0
-    assert p["cta_pair"] == 1 and p["stages"] == 6
+    assert p["cta_pair"] == 1 and p["stages"] == 6 and p["threads"] == 16 * 32
     assert p["k_blocks"] == 28 and p["band_k_blocks"] == 8 and p["smem_bytes"] <= 227 * 1024
     assert pgg.pgg_dw_plan(*sizes, pgg.PGG_F32)["variant"] == 3
     assert pgg.pgg_dw_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
@@ -228,7 +228,7 @@ def test_forward_plan_and_host_errors(lib):
     p = pgg.pgg_fwd_plan(*sizes, pgg.PGG_BF16)
     assert p["variant"] == 0 and p["rows_per_block"] == 256 and p["cta_pair"] == 1
     assert p["k_per_block"] == 64 and p["k_blocks"] == 112 and p["band_k_blocks"] == 8
-    assert p["smem_bytes"] <= 227 * 1024
+    assert p["smem_bytes"] <= 227 * 1024 and p["stages"] == 7 and p["threads"] == 13 * 32
     assert pgg.pgg_fwd_plan(*sizes, pgg.PGG_F32)["variant"] == 3
     assert pgg.pgg_fwd_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
                             pgg.PGG_BF16)["variant"] == 3
