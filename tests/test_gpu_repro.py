@@ -1,4 +1,5 @@
-"""Bitwise reproducibility of d_x across fresh processes.
+"""Bitwise reproducibility across fresh processes: d_x, and the forward and the
+weight gradient.
 
 The page "MoeInitRoutingGroupedMatmulGrad design" (section 2.4.1) asks for
 deterministic computation. Each d_x element receives its topK contributions in
@@ -59,7 +60,8 @@ def built():
 
 
 def _digest(t):
-    return hashlib.sha256(t.cpu().numpy().tobytes()).hexdigest()
+    # the bytes themselves, whatever the dtype (numpy has no bfloat16)
+    return hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
 
 
 def test_dx_bytes_identical_in_and_across_processes():
@@ -83,3 +85,58 @@ def test_dx_bytes_identical_in_and_across_processes():
         assert r.returncode == 0, r.stderr[-3000:]
         child = json.loads(r.stdout.strip().splitlines()[-1])
         assert child == here, {n: (here[n], child.get(n)) for n in NAMES if child.get(n) != here[n]}
+
+
+# The forward and the weight gradient: every output element is produced by one
+# tile in a fixed order of MMAs, so their bytes must not change either.
+CHILD_FWD_DW = r"""
+import hashlib, json, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import permute_grouped_gemm_gb300 as pgg
+from workloads import WORKLOADS, make_inputs
+from workloads.moe import forward_input
+pgg.load()
+res = {}
+for name in sys.argv[2:]:
+    inp = make_inputs(WORKLOADS[name], device="cuda")
+    x = forward_input(inp)
+    y, ws = pgg.fwd(x, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k,
+                    inp.row_idx_type)
+    d, ws2 = pgg.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch, inp.top_k,
+                    inp.row_idx_type)
+    torch.cuda.synchronize()
+    if pgg.status(ws) != 0 or pgg.status(ws2) != 0:
+        raise SystemExit("device status on %s" % name)
+    res[name] = [hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
+                 for t in (y, d)]
+    del inp, x, y, d, ws, ws2
+print(json.dumps(res))
+"""
+
+
+def test_forward_and_weight_gradient_bytes_identical_across_processes():
+    from workloads.moe import forward_input
+    names = ["uniform-bf16", "skewed-fp16", "unaligned-bf16"]
+    here = {}
+    for name in names:
+        inp = make_inputs(WORKLOADS[name], device="cuda")
+        x = forward_input(inp)
+        seen = set()
+        for _ in range(2):
+            y, ws = pgg.fwd(x, inp.weight, inp.expanded_row_idx, inp.group_list, inp.batch,
+                            inp.top_k, inp.row_idx_type)
+            d, ws2 = pgg.dw(x, inp.grad_y, inp.expanded_row_idx, inp.group_list, inp.batch,
+                            inp.top_k, inp.row_idx_type)
+            torch.cuda.synchronize()
+            assert pgg.status(ws) == 0 and pgg.status(ws2) == 0
+            seen.add((_digest(y), _digest(d)))
+        assert len(seen) == 1, f"{name}: runs in one process differ"
+        here[name] = list(seen.pop())
+        del inp, x, y, d, ws, ws2
+        torch.cuda.empty_cache()
+    r = subprocess.run([sys.executable, "-c", CHILD_FWD_DW, ROOT, *names], capture_output=True,
+                       text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    child = json.loads(r.stdout.strip().splitlines()[-1])
+    assert child == here, {n: (here[n], child.get(n)) for n in names if child.get(n) != here[n]}
