@@ -197,14 +197,25 @@ __device__ void x_gatherer(uint8_t* smem, FwdCtl* ctl, const FwdArgs& a, uint32_
   uint32_t j = static_cast<uint32_t>(w / nks);
   int kb = w % nks;
   uint32_t tok_tile = 0xFFFFFFFFu;
-  int32_t tok[4] = {-1, -1, -1, -1};
+  // this lane's rows (lane >> 3) + 4 q of the current tile: the x row's
+  // offset in 16-byte units, or kNoRow past the block
+  constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+  const uint32_t row_units = static_cast<uint32_t>(a.K / 8);
+  uint32_t row16[kFM / 4];
   FTile x;
   while (true) {
     const uint32_t t = cluster_id() + j * n_clusters();
     if (t >= total) break;
     if (t != tok_tile) {
       x = ftile_of(t, a, rank);
+      int32_t tok[4];
       tile_tokens(x, a, lane, tok);
+#pragma unroll
+      for (int q = 0; q < kFM / 4; ++q) {
+        const int rr = (lane >> 3) + 4 * q;
+        const int32_t tk = __shfl_sync(0xFFFFFFFFu, tok[rr >> 5], rr & 31);
+        row16[q] = tk >= 0 ? static_cast<uint32_t>(tk) * row_units : kNoRow;
+      }
       tok_tile = t;
     }
     if (!ptx::mbar_wait_cluster(&ctl->empty[w], phase ^ 1u, lim, abort)) {
@@ -213,12 +224,12 @@ __device__ void x_gatherer(uint8_t* smem, FwdCtl* ctl, const FwdArgs& a, uint32_
     }
     const int64_t k = static_cast<int64_t>(kb) * kFK + c * 8;
     const bool k_ok = k < a.K;
+    const char* xk = xb + k * 2;
 #pragma unroll
     for (int q = 0; q < kFM / 4; ++q) {
       const int rr = (lane >> 3) + 4 * q;
-      const int32_t tk = __shfl_sync(0xFFFFFFFFu, tok[rr >> 5], rr & 31);
-      const bool ok = k_ok && tk >= 0;
-      const void* src = ok ? static_cast<const void*>(xb + (static_cast<int64_t>(tk) * a.K + k) * 2)
+      const bool ok = k_ok && row16[q] != kNoRow;
+      const void* src = ok ? static_cast<const void*>(xk + (static_cast<uint64_t>(row16[q]) << 4))
                            : static_cast<const void*>(xb);
       ptx::cp_async_16(sa_slot + rr * 128 + ((c ^ (rr & 7)) << 4), src, ok ? 16u : 0u);
     }

@@ -597,13 +597,17 @@ int run_dw(const Plan& plan, const void* x, const void* gradY, void* ws, void* d
 
 // ---------------------------------------------------------------- forward
 
+// The tensor-core forward's gather warps address an x row by its offset in
+// 16-byte units, held in 32 bits (x below 64 GiB).
+bool fwd_x_rows_fit(int64_t batch, int64_t K) { return batch * (K / 8) < 0xFFFFFFFFll; }
+
 // The tensor-core forward takes 16-bit inputs whose x, weight and y rows are
 // whole 16-byte units, with x, weight and y 16-byte aligned.
-bool fwd_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void* w,
+bool fwd_tensor_path(int dtype, int64_t N, int64_t K, int64_t batch, const void* x, const void* w,
                      const void* y) {
   if (g_force_variant.load() == kVariantSimt) return false;
   if (dtype == PGG_F32) return false;
-  if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0) return false;
+  if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0 || !fwd_x_rows_fit(batch, K)) return false;
   return aligned(x, 16) && aligned(w, 16) && aligned(y, 16);
 }
 
@@ -611,11 +615,11 @@ bool fwd_tensor_path(int dtype, int64_t N, int64_t K, const void* x, const void*
 // bytes at a time) and y written with 4-byte stores: 16-bit inputs, x rows
 // whole 16-byte units and x 16-byte aligned (gathered 16 bytes at a time), N
 // even, weight and y 4-byte aligned.
-bool fwd_gather_path(int dtype, int64_t N, int64_t K, const void* x, const void* w,
+bool fwd_gather_path(int dtype, int64_t N, int64_t K, int64_t batch, const void* x, const void* w,
                      const void* y) {
   if (g_force_variant.load() == kVariantSimt) return false;
   if (dtype == PGG_F32) return false;
-  if ((K * 2) % 16 != 0 || N % 2 != 0) return false;
+  if ((K * 2) % 16 != 0 || N % 2 != 0 || !fwd_x_rows_fit(batch, K)) return false;
   return aligned(x, 16) && aligned(w, 4) && aligned(y, 4);
 }
 
@@ -666,8 +670,8 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.gather_w = 0;
   a.hold_release = g_hold_release.load() != 0 ? 1 : 0;
-  if (!fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y) &&
-      fwd_gather_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
+  if (!fwd_tensor_path(plan.dtype, plan.N, plan.K, plan.batch, x, weight, y) &&
+      fwd_gather_path(plan.dtype, plan.N, plan.K, plan.batch, x, weight, y)) {
     fwd_tiles(plan.N, &a.n_blocks);
     a.gather_w = 1;
     CUtensorMap none;
@@ -677,7 +681,7 @@ int run_fwd(const Plan& plan, const void* x, const void* weight, void* ws, void*
                ? PGG_OK
                : PGG_ERR_CUDA;
   }
-  if (fwd_tensor_path(plan.dtype, plan.N, plan.K, x, weight, y)) {
+  if (fwd_tensor_path(plan.dtype, plan.N, plan.K, plan.batch, x, weight, y)) {
     fwd_tiles(plan.N, &a.n_blocks);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PGG_ERR_CUDA;
@@ -884,8 +888,8 @@ int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t 
   rc = make_fwd_plan(M, N, K, G, batch, topK, rowIdxType, dtype, &p);
   if (rc != PGG_OK) return rc;
   alignas(16) static const char probe[16] = {0};
-  const bool tc = fwd_tensor_path(dtype, N, K, probe, probe, probe);
-  const bool ga = !tc && fwd_gather_path(dtype, N, K, probe, probe, probe);
+  const bool tc = fwd_tensor_path(dtype, N, K, batch, probe, probe, probe);
+  const bool ga = !tc && fwd_gather_path(dtype, N, K, batch, probe, probe, probe);
   std::memset(info, 0, sizeof(*info));
   int nb = 0;
   info->rows_per_block = p.rows_per_block;

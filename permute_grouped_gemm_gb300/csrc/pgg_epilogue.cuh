@@ -113,7 +113,8 @@ __device__ __forceinline__ void store_chunk(uint4 (&b)[8], char* out, int64_t ro
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int64_t c = col + q * (4 / oes);
-        if (r < nrows && c < N) *reinterpret_cast<uint32_t*>(out + ((row0 + r) * N + c) * oes) = w4[q];
+        if (r < nrows && c < N)
+          *reinterpret_cast<uint32_t*>(out + ((row0 + r) * N + c) * oes) = w4[q];
       }
     }
   }

@@ -230,6 +230,11 @@ def test_forward_plan_and_host_errors(lib):
     assert p["k_per_block"] == 64 and p["k_blocks"] == 112 and p["band_k_blocks"] == 8
     assert p["smem_bytes"] <= 227 * 1024 and p["stages"] == 7 and p["threads"] == 13 * 32
     assert pgg.pgg_fwd_plan(*sizes, pgg.PGG_F32)["variant"] == 3
+    # the gather warps hold an x row's offset in 16-byte units in 32 bits: x of
+    # 64 GiB or more (batch x K / 8 >= 2^32 - 1) takes the FP32-pipe kernel
+    for batch, want in ((2**22 - 1, 0), (2**22, 3)):
+        assert pgg.pgg_fwd_plan(batch, 256, 8192, 1, batch, batch, 1, 0,
+                                pgg.PGG_BF16)["variant"] == want, batch
     assert pgg.pgg_fwd_plan(a["M"], 286, 178, a["G"], a["L"], a["batch"], a["topK"], 0,
                             pgg.PGG_BF16)["variant"] == 3
     # weight and y rows of 572 bytes, x rows of 384: weight gathered by warps (variant 5)
