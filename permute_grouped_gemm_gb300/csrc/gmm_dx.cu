@@ -632,6 +632,21 @@ __device__ __forceinline__ void ready_rows(EpiState<ROWS>* es, const GemmArgs& a
 // sharing a row then cover its 128 contiguous bytes of this warp's quarter, and
 // one v4 store (rank 0) or v4 fp32 reduction at L2 (rank > 0) per lane writes
 // four rows per warp instruction. Needs K % 4 == 0.
+// Four consecutive fp32 to p: stored if `st`, added at L2 if `add`, neither
+// otherwise (predicated instructions, no branch).
+__device__ __forceinline__ void store_or_add_v4(float* p, float4 v, bool st, bool add) {
+  asm volatile(
+      "{\n"
+      ".reg .pred ps, pa;\n"
+      "setp.ne.u32 ps, %5, 0;\n"
+      "setp.ne.u32 pa, %6, 0;\n"
+      "@ps st.global.v4.f32 [%0], {%1, %2, %3, %4};\n"
+      "@pa red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n"
+      "}\n" ::"l"(p),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(st ? 1u : 0u), "r"(add ? 1u : 0u)
+      : "memory");
+}
+
 template <int ROWS>
 __device__ __forceinline__ void write_rows_vec(const EpiState<ROWS>* es, const GemmArgs& args,
                                                uint32_t t_lane, int R, uint32_t kb, int quarter) {
@@ -671,18 +686,16 @@ __device__ __forceinline__ void write_rows_vec(const EpiState<ROWS>* es, const G
         r1 = t0;
         r3 = t1;
       }
+      // every lane issues both writes, predicated: no divergence between the
+      // rows of a warp instruction (their ranks and readiness differ)
       const int j = 4 * g + (lane & 3);
-      const int r = r_lo + j;
-      if (r < R && ((word >> j) & 1u) && k_ok) {
-        const RowInfo m = es->meta[r];
-        float* dst = args.out + static_cast<int64_t>(m.token) * K + k;
-        const float4 x = make_float4(__uint_as_float(r0), __uint_as_float(r1), __uint_as_float(r2),
-                                     __uint_as_float(r3));
-        if (m.rank == 0)
-          *reinterpret_cast<float4*>(dst) = x;
-        else
-          ptx::red_add_v4_f32_gpu(dst, x);
-      }
+      const int r = r_lo + j;  // < ROWS: a record in bounds, stale past R
+      const bool wr = r < R && ((word >> j) & 1u) && k_ok;
+      const RowInfo m = es->meta[r];
+      float* dst = args.out + static_cast<int64_t>(m.token) * K + k;
+      const float4 x = make_float4(__uint_as_float(r0), __uint_as_float(r1), __uint_as_float(r2),
+                                   __uint_as_float(r3));
+      store_or_add_v4(dst, x, wr && m.rank == 0, wr && m.rank != 0);
     }
   }
 }
