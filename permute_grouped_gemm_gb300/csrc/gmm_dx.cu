@@ -632,6 +632,18 @@ __device__ __forceinline__ void ready_rows(EpiState<ROWS>* es, const GemmArgs& a
 // sharing a row then cover its 128 contiguous bytes of this warp's quarter, and
 // one v4 store (rank 0) or v4 fp32 reduction at L2 (rank > 0) per lane writes
 // four rows per warp instruction. Needs K % 4 == 0.
+// One added to the ticket at p if `on` (a predicated reduction, no branch).
+__device__ __forceinline__ void red_add_one_if(uint32_t* p, uint32_t on) {
+  asm volatile(
+      "{\n"
+      ".reg .pred q;\n"
+      "setp.ne.u32 q, %1, 0;\n"
+      "@q red.relaxed.gpu.global.add.u32 [%0], 1;\n"
+      "}\n" ::"l"(p),
+      "r"(on)
+      : "memory");
+}
+
 // Four consecutive fp32 to p: stored if `st`, added at L2 if `add`, neither
 // otherwise (predicated instructions, no branch).
 __device__ __forceinline__ void store_or_add_v4(float* p, float4 v, bool st, bool add) {
@@ -832,9 +844,8 @@ __device__ void epilogue(Ctl<ROWS, STAGES>* ctl, uint32_t tmem_base, const GemmA
       if (mine) {
         ptx::fence_acq_rel_gpu();
         for (int r = et; r < R; r += 128)
-          if ((es->rdy[r >> 5] >> (r & 31)) & 1u)
-            ptx::red_add_u32_gpu(args.tickets + static_cast<int64_t>(es->meta[r].token) * kbs + kb,
-                                 1u);
+          red_add_one_if(args.tickets + static_cast<int64_t>(es->meta[r].token) * kbs + kb,
+                         (es->rdy[r >> 5] >> (r & 31)) & 1u);
       }
       if (et < C::kWords) es->pend[et] &= ~es->rdy[et];
       ptx::named_bar_sync(bar, 128);
