@@ -254,7 +254,13 @@ __device__ void x_gatherer(uint8_t* smem, FwdCtl* ctl, const FwdArgs& a, uint32_
     ptx::cp_async_wait<0>();
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_remote(full);
+    // the even CTA's own rows go to its own MMA thread: CTA scope suffices
+    if (lane == 0) {
+      if (rank == 0)
+        ptx::mbar_arrive(&ctl->full[w]);
+      else
+        ptx::mbar_arrive_remote(full);
+    }
     phase ^= 1u;
     kb += kStages;
     while (kb >= nks) {
