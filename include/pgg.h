@@ -393,7 +393,9 @@ int pgg_fwd_grouped_gemm(const void* x, const void* weight, const int64_t* expan
  * 0 (tensor cores on CTA pairs: row blocks of rows_per_block = 256 expanded
  * rows x 256 n, k_per_block = 64 per stage), 5 (the same with the weight rows
  * gathered by warps: N even, not a multiple of 8) or 3 (FP32 pipes: 64 rows x
- * 128 n, 32 k per step); band_k_blocks holds the n blocks per row block.
+ * 128 n, 32 k per step; also when x holds 64 GiB or more, batch * K / 8 >=
+ * 2^32 - 1, since the tensor-core kernel addresses x rows with 32-bit offsets
+ * in 16-byte units); band_k_blocks holds the n blocks per row block.
  */
 int pgg_fwd_plan(int64_t M, int64_t N, int64_t K, int64_t G, int64_t L, int64_t batch,
                  int64_t topK, int rowIdxType, pgg_dtype dtype, pgg_plan_info* info);
