@@ -117,6 +117,30 @@ def test_execute_rejects_before_any_cuda_call(lib):
     assert pgg.STATUS[rc] == "PGG_ERR_NULL"
 
 
+def test_every_compiled_configuration_fits_one_sm(lib):
+    # each (dtype, variant) the plan can report asks for at most the 227 KB of
+    # shared memory a CTA may use and at most 1024 threads
+    sizes = (108000, 2048, 7168, 60, 108000, 13500, 8, 0)
+    seen = set()
+    try:
+        for dt in (pgg.PGG_BF16, pgg.PGG_F16, pgg.PGG_F32):
+            for v in (0, 1, 2, 3, 4, 5):
+                pgg.pgg_debug_force_variant(v)
+                for plan in (pgg.pgg_dx_plan, pgg.pgg_dw_plan, pgg.pgg_fwd_plan):
+                    try:
+                        p = plan(*sizes, dt)
+                    except pgg.PggError as e:
+                        # a variant that does not exist for this dtype is refused
+                        assert pgg.STATUS[e.code] == "PGG_ERR_DTYPE", (plan.__name__, dt, v)
+                        continue
+                    seen.add((plan.__name__, dt, p["variant"]))
+                    assert 0 < p["smem_bytes"] <= 227 * 1024, (plan.__name__, dt, v, p)
+                    assert 0 < p["threads"] <= 1024 and p["threads"] % 32 == 0, (plan.__name__, dt, v, p)
+    finally:
+        pgg.pgg_debug_force_variant(-1)
+    assert len(seen) >= 10
+
+
 def test_plan_variants(lib):
     big = pgg.pgg_dx_plan(108000, 2048, 7168, 60, 108000, 13500, 8, 0, pgg.PGG_BF16)
     skinny = pgg.pgg_dx_plan(2048, 2048, 7168, 256, 2048, 256, 8, 0, pgg.PGG_BF16)
