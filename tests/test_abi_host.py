@@ -135,7 +135,8 @@ def test_every_compiled_configuration_fits_one_sm(lib):
                         continue
                     seen.add((plan.__name__, dt, p["variant"]))
                     assert 0 < p["smem_bytes"] <= 227 * 1024, (plan.__name__, dt, v, p)
-                    assert 0 < p["threads"] <= 1024 and p["threads"] % 32 == 0, (plan.__name__, dt, v, p)
+                    assert 0 < p["threads"] <= 1024 and p["threads"] % 32 == 0, \
+                        (plan.__name__, dt, v, p)
     finally:
         pgg.pgg_debug_force_variant(-1)
     assert len(seen) >= 10
