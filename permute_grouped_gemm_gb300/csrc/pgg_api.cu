@@ -230,12 +230,18 @@ CUtensorMapDataType tmap_type(int dtype) {
 
 // d_y [M, N] as 2-D maps with boxes of 32, 64, 128 and 256 rows x one
 // 128-byte row segment. weight [G, K, N] as a 3-D map; boxes of 1 expert x
-// 128 k x one segment. Rows or columns outside the tensor read as zero.
+// 128 k x one segment. Rows or columns outside the tensor read as zero. L2
+// promotion: 128 bytes (one box row) for the CTA-pair tiles, where 256 bytes
+// measured about 1% slower on the largest workload; 256 bytes for the others,
+// whose weight streams from HBM (narrow row blocks of many small experts).
 int encode_maps(const Plan& p, const void* dy, const void* w, DyMaps* tdy, CUtensorMap* tw) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PGG_ERR_CUDA;
   const cuuint64_t es = static_cast<cuuint64_t>(elem_size(p.dtype));
   const cuuint32_t box_n = static_cast<cuuint32_t>(kRowBytes / es);
+  const CUtensorMapL2promotion promo = (p.pair && p.variant == 0)
+                                           ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                           : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   for (int j = 0; j < kDyMaps; ++j) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * es};
@@ -243,7 +249,7 @@ int encode_maps(const Plan& p, const void* dy, const void* w, DyMaps* tdy, CUten
     cuuint32_t estr[2] = {1, 1};
     if (enc(&tdy->box[j], tmap_type(p.dtype), 2, const_cast<void*>(dy), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PGG_ERR_CUDA;
   }
   {
@@ -255,7 +261,7 @@ int encode_maps(const Plan& p, const void* dy, const void* w, DyMaps* tdy, CUten
     cuuint32_t estr[3] = {1, 1, 1};
     if (enc(tw, tmap_type(p.dtype), 3, const_cast<void*>(w), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PGG_ERR_CUDA;
   }
   return PGG_OK;
