@@ -62,7 +62,7 @@ KERNEL_SOURCES = {
     "gmm_dx_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx.cu", _GATHER, *_COMMON],
     "gmm_dx_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_simt.cu", *_COMMON],
     "gmm_dx_owner_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dx_owner.cu", *_COMMON],
-    "unpermute_grad_kernel": ["permute_grouped_gemm_gb300/csrc/unpermute_grad.cu"],
+    "unpermute_grad_kernel": ["permute_grouped_gemm_gb300/csrc/unpermute_grad.cu", *_COMMON],
     "gmm_dw_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw.cu", _GATHER, _EPILOGUE,
                        *_COMMON],
     "gmm_dw_simt_kernel": ["permute_grouped_gemm_gb300/csrc/gmm_dw_simt.cu", *_COMMON],

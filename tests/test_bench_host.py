@@ -4,6 +4,7 @@ operation, the launch count per plan, and the reference arm's JSON line."""
 
 import json
 import os
+import re
 import subprocess
 import sys
 
@@ -118,6 +119,16 @@ def test_reason_bits_name_the_nvml_clock_event_reasons():
     assert bench._REASON_BITS[0x8] == "hw_slowdown"
     assert bench._REASON_BITS[0x20] == "sw_thermal_slowdown"
     assert bench._REASON_BITS[0x40] == "hw_thermal_slowdown"
+
+
+def test_kernel_source_hashes_cover_the_headers_each_kernel_includes():
+    # a profile's recorded hash must change when any device header its kernel
+    # includes changes, so every included .cuh is in the kernel's source list
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        with open(os.path.join(ROOT, files[0])) as f:
+            included = set(re.findall(r'#include "([^"]+\.cuh)"', f.read()))
+        listed = {os.path.basename(x) for x in files[1:]}
+        assert included <= listed, (kernel, sorted(included - listed))
 
 
 def test_profile_summaries_match_the_current_kernel_sources():
